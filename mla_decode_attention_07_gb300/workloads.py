@@ -1,0 +1,228 @@
+"""Seeded synthetic inputs for paged MLA decode.
+
+This module only draws numbers and lays them out: it holds none of the
+attention arithmetic, so both the CUDA path and the CPU oracle can consume
+the same bits without sharing any of the method's code.
+
+Random source: SplitMix64 (Steele, Lea & Flood, "Fast splittable
+pseudorandom number generators", OOPSLA 2014), used in counter form: output k
+of the stream with start value ``s`` is ``mix(s + (k + 1) * GAMMA)`` mod 2**64.
+Each tensor has its own stream, started at ``seed ^ TENSOR_ID``.
+
+Normals: Box-Muller on two 53-bit uniforms in (0, 1], computed in float64,
+rounded to float32 and then to bfloat16 with round-to-nearest-even.
+
+Shapes (DeepSeek-style MLA decode over a paged latent cache):
+  q            [B, s_q, h_q, 576]      bf16 (uint16 bits)
+  kv_cache     [num_pages, 64, 1, 576] bf16 (uint16 bits)
+  block_table  [B, max_pages]          int32
+  cache_seqlens[B]                     int32
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+D_QK = 576          # 512 latent + 64 rope dims per cache row
+D_V = 512           # values are the first 512 dims of the same row
+PAGE = 64           # tokens per KV page
+SOFTMAX_SCALE = 192.0 ** -0.5
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+TENSOR_Q = 0x51
+TENSOR_KV = 0x4B56
+TENSOR_SEQLENS = 0x5345
+TENSOR_PERM = 0x5045
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def splitmix64(start: int, first: int, count: int) -> np.ndarray:
+    """Outputs ``first .. first+count-1`` of the SplitMix64 stream at ``start``."""
+    k = np.arange(first + 1, first + count + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(start & 0xFFFFFFFFFFFFFFFF) + k * GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _uniform01(z: np.ndarray) -> np.ndarray:
+    # 53 high bits -> (0, 1]
+    return ((z >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)
+
+
+def float32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest-even) and return the bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    with np.errstate(over="ignore"):
+        r = (u + bias) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_float32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(seed: int, tensor_id: int, n: int, chunk: int = 1 << 22) -> np.ndarray:
+    """``n`` N(0,1) samples rounded to bf16 bits, deterministic in (seed, tensor_id)."""
+    start = (seed ^ tensor_id) & 0xFFFFFFFFFFFFFFFF
+    out = np.empty(n, dtype=np.uint16)
+    pairs_total = (n + 1) // 2
+    done = 0
+    while done < pairs_total:
+        m = min(chunk, pairs_total - done)
+        z = splitmix64(start, 2 * done, 2 * m)
+        u1 = _uniform01(z[0::2])
+        u2 = _uniform01(z[1::2])
+        r = np.sqrt(-2.0 * np.log(u1))
+        th = 2.0 * math.pi * u2
+        vals = np.empty(2 * m, dtype=np.float64)
+        vals[0::2] = r * np.cos(th)
+        vals[1::2] = r * np.sin(th)
+        lo = 2 * done
+        hi = min(n, lo + 2 * m)
+        out[lo:hi] = float32_to_bf16_bits(vals[: hi - lo].astype(np.float32))
+        done += m
+    return out
+
+
+def uniform_int(seed: int, tensor_id: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """``n`` integers uniform in [lo, hi] (inclusive)."""
+    span = hi - lo + 1
+    z = splitmix64((seed ^ tensor_id) & 0xFFFFFFFFFFFFFFFF, 0, n)
+    return (lo + (z % np.uint64(span)).astype(np.int64)).astype(np.int32)
+
+
+def permutation(seed: int, tensor_id: int, n: int) -> np.ndarray:
+    """A uniformly random permutation of range(n): argsort of 64-bit keys."""
+    z = splitmix64((seed ^ tensor_id) & 0xFFFFFFFFFFFFFFFF, 0, n)
+    return np.argsort(z, kind="stable").astype(np.int32)
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    q: np.ndarray            # uint16 [B, s_q, h_q, 576]
+    kv_cache: np.ndarray     # uint16 [num_pages, 64, 1, 576]
+    block_table: np.ndarray  # int32 [B, max_pages]
+    cache_seqlens: np.ndarray  # int32 [B]
+    s_q: int
+    h_q: int
+    softmax_scale: float = SOFTMAX_SCALE
+
+    @property
+    def batch(self) -> int:
+        return int(self.cache_seqlens.shape[0])
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.kv_cache.shape[0])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+
+def make_inputs(seed: int, batch: int, s_q: int, h_q: int, seqlens, *,
+                extra_pages: int = 0, poison: bool = True,
+                q_zero: bool = False) -> DecodeInputs:
+    """Seeded decode inputs.
+
+    ``seqlens`` is a sequence of ints (one per batch entry).  The pool holds
+    exactly ``sum(ceil(L/64))`` live pages plus ``extra_pages`` decoy pages,
+    all in a random order.  With ``poison`` the unused tail slots of every last
+    page, the decoy pages and the unused block-table entries (which point at a
+    decoy page, or at page 0 when there is none) hold NaN-poisoned data, so a
+    kernel that reads anything it should not shows NaN in its output.
+    """
+    seqlens = np.asarray(seqlens, dtype=np.int32).reshape(batch)
+    if np.any(seqlens < 0):
+        raise ValueError("sequence lengths must be >= 0")
+    pages_per = [(int(L) + PAGE - 1) // PAGE for L in seqlens]
+    live = int(sum(pages_per))
+    num_pages = live + int(extra_pages)
+    if num_pages == 0:
+        num_pages = 1
+    max_pages = max(1, max(pages_per) if pages_per else 1)
+
+    perm = permutation(seed, TENSOR_PERM, num_pages)
+    block_table = np.empty((batch, max_pages), dtype=np.int32)
+    decoy = int(perm[live]) if num_pages > live else int(perm[0])
+    block_table[:] = decoy
+    off = 0
+    for b, np_b in enumerate(pages_per):
+        block_table[b, :np_b] = perm[off:off + np_b]
+        off += np_b
+
+    kv = normal_bf16(seed, TENSOR_KV, num_pages * PAGE * D_QK).reshape(num_pages, PAGE, 1, D_QK)
+    q = normal_bf16(seed, TENSOR_Q, batch * s_q * h_q * D_QK).reshape(batch, s_q, h_q, D_QK)
+    if q_zero:
+        q[:] = 0
+    if poison:
+        for b, np_b in enumerate(pages_per):
+            L = int(seqlens[b])
+            if np_b and L % PAGE:
+                kv[block_table[b, np_b - 1], L % PAGE:] = BF16_NAN
+        for p in perm[live:]:
+            kv[int(p)] = BF16_NAN
+    return DecodeInputs(q=q, kv_cache=kv, block_table=block_table,
+                        cache_seqlens=seqlens, s_q=s_q, h_q=h_q)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One named decode workload: shapes plus the seeded recipe."""
+    name: str
+    batch: int
+    s_q: int
+    h_q: int
+    seqlen: int | None      # uniform length, or None for seeded ragged lengths
+    seqlen_max: int = 0     # upper bound of the ragged draw
+    seed: int = 0
+
+    def seqlens(self) -> np.ndarray:
+        if self.seqlen is not None:
+            return np.full(self.batch, self.seqlen, dtype=np.int32)
+        return uniform_int(self.seed, TENSOR_SEQLENS, self.batch, 1, self.seqlen_max)
+
+    def make(self, **kw) -> DecodeInputs:
+        return make_inputs(self.seed, self.batch, self.s_q, self.h_q, self.seqlens(), **kw)
+
+    def visible_keys(self) -> int:
+        """Sum over (batch, query token) of visible keys (bottom-right causal)."""
+        L = self.seqlens().astype(np.int64)
+        tot = 0
+        for i in range(self.s_q):
+            tot += int(np.maximum(L - self.s_q + 1 + i, 0).sum())
+        return tot
+
+    def flops(self) -> float:
+        """Algorithmic flops: 2 * (576 + 512) per (head, visible key)."""
+        return 2.0 * (D_QK + D_V) * self.h_q * self.visible_keys()
+
+    def bytes(self) -> float:
+        """Algorithmic bytes: each live cache row once, plus q, out and lse."""
+        L = self.seqlens().astype(np.int64)
+        kv = int(L.sum()) * D_QK * 2
+        rows = self.batch * self.s_q * self.h_q
+        return float(kv + rows * D_QK * 2 + rows * D_V * 2 + rows * 4)
+
+
+# The five decode workloads: tiny, large-batch 128-head, ragged, two-token
+# speculative (causal inside the two query tokens) and long-context 16-head.
+WORKLOADS = {
+    "tiny": Workload("tiny", batch=1, s_q=1, h_q=16, seqlen=256, seed=0),
+    "b16_h128_l4096": Workload("b16_h128_l4096", batch=16, s_q=1, h_q=128, seqlen=4096, seed=1),
+    "ragged_b64_h128": Workload("ragged_b64_h128", batch=64, s_q=1, h_q=128, seqlen=None,
+                                seqlen_max=8192, seed=2),
+    "spec_b132_sq2_h128_l8192": Workload("spec_b132_sq2_h128_l8192", batch=132, s_q=2, h_q=128,
+                                         seqlen=8192, seed=3),
+    "long_b8_h16_l65536": Workload("long_b8_h16_l65536", batch=8, s_q=1, h_q=16, seqlen=65536,
+                                   seed=4),
+}

@@ -1,0 +1,69 @@
+"""Seeded input generators (CPU only)."""
+import numpy as np
+import pytest
+
+from mla_decode_attention_07_gb300 import workloads as W
+
+
+def test_splitmix64_published_vector():
+    # First outputs of SplitMix64 seeded with 1234567 (the sequence printed with
+    # the reference C implementation by Vigna) and with 0.
+    assert [int(x) for x in W.splitmix64(1234567, 0, 5)] == [
+        6457827717110365317, 3203168211198807973, 9817491932198370423,
+        4593380528125082431, 16408922859458223821]
+    assert int(W.splitmix64(0, 0, 1)[0]) == 0xE220A8397B1DCDAF
+
+
+def test_splitmix64_counter_form_is_a_stream():
+    a = W.splitmix64(77, 0, 100)
+    b = np.concatenate([W.splitmix64(77, 0, 37), W.splitmix64(77, 37, 63)])
+    assert np.array_equal(a, b)
+
+
+def test_bf16_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(100000).astype(np.float32),
+                        np.array([1.0, -2.5, 1.00390625, 1.01171875, 3.0e38, 1e-40],
+                                 dtype=np.float32)])
+    ours = W.float32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_normals_moments_and_determinism():
+    a = W.normal_bf16(5, W.TENSOR_KV, 1 << 18)
+    b = W.normal_bf16(5, W.TENSOR_KV, 1 << 18, chunk=1000)
+    assert np.array_equal(a, b)
+    x = W.bf16_bits_to_float32(a).astype(np.float64)
+    assert abs(x.mean()) < 0.01 and abs(x.std() - 1.0) < 0.01
+    assert not np.array_equal(a, W.normal_bf16(6, W.TENSOR_KV, 1 << 18))
+
+
+def test_permutation_is_a_permutation():
+    p = W.permutation(3, W.TENSOR_PERM, 1000)
+    assert sorted(p.tolist()) == list(range(1000))
+
+
+def test_make_inputs_layout_and_poison():
+    inp = W.make_inputs(9, 3, 2, 16, [65, 0, 128], extra_pages=2)
+    assert inp.q.shape == (3, 2, 16, 576) and inp.kv_cache.shape == (6, 64, 1, 576)
+    live = inp.block_table[0, :2].tolist() + inp.block_table[2, :2].tolist()
+    assert len(set(live)) == 4
+    assert np.all(inp.block_table[1] == inp.block_table[1, 0]) and inp.block_table[1, 0] not in live
+    last = inp.block_table[0, 1]
+    assert np.all(inp.kv_cache[last, 1:] == W.BF16_NAN)      # tail after token 64
+    assert not np.any(inp.kv_cache[last, 0] == W.BF16_NAN)
+    decoys = sorted(set(range(6)) - set(live))
+    for p in decoys:
+        assert np.all(inp.kv_cache[p] == W.BF16_NAN)
+
+
+def test_workload_accounting():
+    w = W.WORKLOADS["b16_h128_l4096"]
+    assert abs(w.flops() / 1e9 - 18.25) < 0.01
+    assert w.visible_keys() == 16 * 4096
+    s = W.WORKLOADS["spec_b132_sq2_h128_l8192"]
+    assert s.visible_keys() == 132 * (8192 + 8191)
+    r = W.WORKLOADS["ragged_b64_h128"].seqlens()
+    assert r.min() >= 1 and r.max() <= 8192 and len(r) == 64
