@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of paged MLA decode (libmla) on one GB300, or N replicas.
+
+A step is one pass of the whole decode path over one batch of synthetic
+input: the split-KV planner, the main attention kernel and the LSE-combine
+kernel, all launched through the C ABI.  The default workload is the
+large-batch 128-head decode (batch 16, s_q 1, h_q 128, 4096 cached tokens per
+sequence, 576/512 latent dims, 64-token pages, random page order).
+
+Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
+the launching stream, with a device synchronise (and, for N > 1, a barrier)
+on both sides; rank 0 prints one JSON line.  L2 is defeated by rotating
+input sets whose total size is well above the L2 capacity, so every step
+reads its cache pages from HBM.  Per-kernel durations come from events
+recorded between the three launches of each timed step.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+only other arm there is: the pages ship no implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_decode_attention_07_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA decode TFLOP/s, KV GB/s and % of GB300 roofline per call (1 GPU)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DEFAULT_WORKLOAD = "b16_h128_l4096"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_traffic.json")
+DECODE_SRC = os.path.join(ROOT, "mla_decode_attention_07_gb300", "csrc", "mla_decode_sm103.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU time budget of the oracle baseline leg")
+    return ap.parse_args(argv)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, \
+            "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate_max(value: float, world: int) -> float:
+    """Max over ranks of a per-rank float (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def roofline_times(w: W.Workload, peaks):
+    t_mem = w.bytes() / (peaks["hbm_gbs"] * 1e9)
+    t_flop = w.flops() / (peaks["bf16_tflops"] * 1e12)
+    return t_mem, t_flop
+
+
+def traffic_per_launch():
+    """DRAM bytes per attend launch from the committed ncu summary, if the
+    kernel source is unchanged since it was captured."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+        if rec.get("source_sha256") != sha:
+            return None
+        return float(rec["dram_bytes_per_launch_full_workload"])
+    except Exception:
+        return None
+
+
+def physical_gpu_index(logical: int) -> int:
+    """nvidia-smi numbers GPUs physically; map through CUDA_VISIBLE_DEVICES."""
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    if logical < len(vis) and vis[logical].isdigit():
+        return int(vis[logical])
+    return logical
+
+
+class ClockSampler:
+    """nvidia-smi sampling (every 200 ms) while the GPU is under load."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w: W.Workload, inp, budget_s: float):
+    """The oracle as it stands, on this host's cores, over whole passes of the
+    workload (or a row sample when one pass would exceed the budget)."""
+    import oracle
+    threads = oracle.default_threads()
+    rows_all = np.array([(b, i, h) for b in range(w.batch) for i in range(w.s_q)
+                         for h in range(w.h_q)], dtype=np.int32)
+    keys = inp.cache_seqlens.astype(np.int64)
+    flops_row = {}
+    # one small calibration call, then size the sample to the budget
+    t0 = time.perf_counter()
+    cal = rows_all[: max(1, min(len(rows_all), 8))]
+    oracle.mla_decode_rows(inp, cal, nthreads=threads)
+    dt = max(1e-6, time.perf_counter() - t0)
+
+    def fl(rows):
+        tot = 0.0
+        for b, i, h in rows:
+            n = max(0, int(keys[b]) - w.s_q + 1 + int(i))
+            tot += 2.0 * (W.D_QK + W.D_V) * n
+        return tot
+    rate = fl(cal) / dt
+    total_fl = w.flops()
+    if total_fl / rate <= budget_s:
+        sample, desc = rows_all, "full workload"
+    else:
+        n = max(1, int(len(rows_all) * budget_s * rate / total_fl / 1.2))
+        rng = np.random.default_rng(0)
+        sample = rows_all[np.sort(rng.choice(len(rows_all), size=n, replace=False))]
+        desc = f"{n} of {len(rows_all)} query rows, seeded random"
+    sfl = fl(sample)
+    passes, spent = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.mla_decode_rows(inp, sample, nthreads=threads)
+        spent += time.perf_counter() - t0
+        passes += 1
+        if spent >= 0.5 * budget_s or passes >= 50:
+            break
+    value = sfl * passes / spent / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{desc}, {passes} pass(es), {spent:.1f} s, fp64 C oracle"}
+
+
+def make_sets(torch, w: W.Workload, dev, l2_bytes: int):
+    """Input sets rotated between steps; total bytes > 2.5 x L2."""
+    per_set = w.bytes()
+    n = max(2, math.ceil(2.5 * l2_bytes / per_set))
+    seqlens = w.seqlens()
+    sets = []
+    host0 = None
+    for k in range(n):
+        inp = w.make() if k == 0 else W.make_inputs(w.seed + 7919 * k, w.batch, w.s_q, w.h_q,
+                                                    seqlens)
+        if k == 0:
+            host0 = inp
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        sets.append(dict(q=t(inp.q.view(np.int16)).view(torch.bfloat16),
+                         kv=t(inp.kv_cache.view(np.int16)).view(torch.bfloat16),
+                         bt=t(inp.block_table), sl=t(inp.cache_seqlens)))
+    return sets, host0
+
+
+def run_ours(args):
+    import torch
+    from mla_decode_attention_07_gb300 import libmla
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    libmla.load()
+    w = W.WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1024 * 1024))
+    sets, host0 = make_sets(torch, w, dev, l2)
+    B, s_q, h_q = w.batch, w.s_q, w.h_q
+    out = torch.empty((B, s_q, h_q, W.D_V), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, h_q, s_q), dtype=torch.float32, device=dev)
+    meta, ws = libmla.alloc_plan_and_workspace(B, s_q, h_q, dev.index)
+    stream = torch.cuda.current_stream(dev)
+    scale = W.SOFTMAX_SCALE
+
+    def step(k, evs=None):
+        s = sets[k % len(sets)]
+        if evs is not None:
+            evs[0].record(stream)
+        libmla.mla_decode_plan(s["sl"], s_q, h_q, meta, stream)
+        if evs is not None:
+            evs[1].record(stream)
+        libmla.mla_decode_attend(s["q"], s["kv"], s["bt"], s["sl"], meta, out, lse, scale, ws,
+                                 stream)
+        if evs is not None:
+            evs[2].record(stream)
+        libmla.mla_decode_combine(B, s_q, h_q, meta, out, lse, ws, stream)
+        if evs is not None:
+            evs[3].record(stream)
+
+    for k in range(max(3, args.warmup)):
+        step(k)
+    torch.cuda.synchronize()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error during warm-up: {libmla.mla_strerror(rc)}")
+
+    # Keep the GPU busy ~1.5 s under the clock sampler, then the timed region.
+    sampler = ClockSampler(physical_gpu_index(dev.index))
+    sampler.start()
+    t_end = time.perf_counter() + 1.5
+    k = 0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            step(k)
+            k += 1
+        torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    start.record(stream)
+    for i in range(K):
+        step(i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms_total = start.elapsed_time(end)
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error in timed region: {libmla.mla_strerror(rc)}")
+    plan_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    attend_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    combine_us = statistics.mean(e[2].elapsed_time(e[3]) for e in evs) * 1e3
+    ms_total = aggregate_max(ms_total, world)
+    ms_step = ms_total / K
+
+    # End to end through the public API from pinned host buffers: per step
+    # copy q, block table and sequence lengths in, plan + decode, copy out and
+    # lse back.  The cache pages stay resident on the device (they are the
+    # model's state, not a per-step input); sets still rotate for L2.
+    hq = torch.from_numpy(np.ascontiguousarray(host0.q.view(np.int16))).view(
+        torch.bfloat16).pin_memory()
+    hbt = torch.from_numpy(host0.block_table).pin_memory()
+    hsl = torch.from_numpy(host0.cache_seqlens).pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    def e2e_step(k):
+        s = sets[k % len(sets)]
+        s["q"].copy_(hq, non_blocking=True)
+        s["bt"].copy_(hbt, non_blocking=True)
+        s["sl"].copy_(hsl, non_blocking=True)
+        libmla.mla_decode_plan(s["sl"], s_q, h_q, meta, stream)
+        libmla.mla_decode(s["q"], s["kv"], s["bt"], s["sl"], meta, out, lse, scale, ws, stream)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for k in range(3):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e_start.record(stream)
+    for i in range(K):
+        e2e_step(i)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = aggregate_max(e_start.elapsed_time(e_end), world) / K
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error in e2e region: {libmla.mla_strerror(rc)}")
+
+    flops = w.flops() * world
+    tflops = flops / (ms_step * 1e-3) / 1e12
+    kv_bytes = float(w.seqlens().astype(np.int64).sum()) * W.D_QK * 2
+    t_mem, t_flop = roofline_times(w, peaks)
+    roof_s = max(t_mem, t_flop)
+    bound = "hbm" if t_mem >= t_flop else "tensor"
+    attend_s = attend_us * 1e-6
+    if bound == "hbm":
+        achieved = w.bytes() / attend_s / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved = w.flops() / attend_s / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    traffic = traffic_per_launch()
+
+    result = {
+        "metric": METRIC,
+        "value": round(tflops, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64 normals rounded to bf16; random page order)",
+        "config": {"workload": w.name, "batch": B, "s_q": s_q, "h_q": h_q,
+                   "seqlen": int(w.seqlen) if w.seqlen else "ragged", "d_qk": W.D_QK,
+                   "d_v": W.D_V, "page": W.PAGE, "softmax_scale": scale,
+                   "l2": f"rotating {len(sets)} input sets of {w.bytes() / 1e6:.1f} MB "
+                         f"(> 2.5 x L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_call": round(ms_step * 1e3, 3),
+        "kv_gbs": round(kv_bytes * world / (ms_step * 1e-3) / 1e9, 1),
+        "roofline_pct": round(100.0 * roof_s / (ms_step * 1e-3), 2),
+        "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "mla_decode_kernel (attend)",
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
+                     else "fallback"},
+        "kernels_us": {"plan": round(plan_us, 3), "attend": round(attend_us, 3),
+                       "combine": round(combine_us, 3)},
+        "gpu_launches": 3 * K,
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h),
+                "note": "mla_decode_plan + mla_decode from pinned host q/block_table/seqlens, "
+                        "out+lse copied back; cache pages resident"},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, host0, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """fp64 CPU oracle timed as the comparison arm (rank 0 only)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = W.WORKLOADS[args.workload]
+    inp = w.make()
+    threads = oracle.default_threads()
+    rows_all = np.array([(b, i, h) for b in range(w.batch) for i in range(w.s_q)
+                         for h in range(w.h_q)], dtype=np.int32)
+    keys = inp.cache_seqlens.astype(np.int64)
+
+    def fl(rows):
+        return sum(2.0 * (W.D_QK + W.D_V) * max(0, int(keys[b]) - w.s_q + 1 + int(i))
+                   for b, i, _h in rows)
+    cal = rows_all[:8]
+    t0 = time.perf_counter()
+    oracle.mla_decode_rows(inp, cal, nthreads=threads)
+    rate = fl(cal) / max(1e-6, time.perf_counter() - t0)
+    budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+    n = int(min(len(rows_all), max(1, len(rows_all) * budget * rate / w.flops())))
+    rng = np.random.default_rng(1)
+    sample = rows_all if n >= len(rows_all) else \
+        rows_all[np.sort(rng.choice(len(rows_all), size=n, replace=False))]
+    sfl = fl(sample)
+    for _ in range(args.warmup):
+        oracle.mla_decode_rows(inp, sample, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.mla_decode_rows(inp, sample, nthreads=threads)
+    dt = time.perf_counter() - t0
+    value = sfl * args.steps / dt / 1e12
+    desc = "full workload" if n >= len(rows_all) else f"{n} of {len(rows_all)} query rows"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "s_q": w.s_q, "h_q": w.h_q,
+                   "seqlen": int(w.seqlen) if w.seqlen else "ragged"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{desc} per step, fp64 C oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

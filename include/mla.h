@@ -1,0 +1,137 @@
+/*
+ * libmla — paged Multi-head Latent Attention (MLA) decode for NVIDIA GB300
+ * (sm_103a), behind a plain C ABI.
+ *
+ * The operation.  DeepSeek-style MLA decode, the FlashMLA kernel that the
+ * TileLang talk uses as its worked example ("Tile级原语与自动推理机制融合，
+ * TileAI社区发起人深度剖析TileLang核心技术与优势", section 什么是「TileLang」:
+ * the ~50-line MLA kernel and its accum_s -> scores_max reduce).  The pages
+ * name the kernel but print no formula; the result computed here is
+ * scaled-dot-product attention of every query row over the latent cache rows
+ * it may see:
+ *
+ *   for batch b, query token i < s_q, head h:
+ *     n        = cache_seqlens[b] - s_q + 1 + i   (bottom-right causal)
+ *     k_t      = kv_cache[block_table[b][t/64]][t%64][0][0:576],  t < n
+ *     s_t      = softmax_scale * <q[b][i][h][0:576], k_t>
+ *     lse      = ln(sum_t exp(s_t))
+ *     out[0:512] = sum_t exp(s_t - lse) * k_t[0:512]
+ *
+ * Dims 0..511 of a cache row are the latent part (also the values), dims
+ * 512..575 the rotary part.  One latent head is shared by all query heads.
+ * A row with no visible key gets out = 0 and lse = -inf.
+ *
+ * Layouts (all row-major, densely packed):
+ *   q            bf16  [batch, s_q, h_q, 576]        device
+ *   kv_cache     bf16  [num_pages, 64, 1, 576]       device
+ *   block_table  int32 [batch, max_pages]            device
+ *   cache_seqlens int32 [batch]                      device (host for the
+ *                                                    _host planner variant)
+ *   out          bf16  [batch, s_q, h_q, 512]        device
+ *   lse          fp32  [batch, h_q, s_q]             device
+ *
+ * Ownership: the caller owns every buffer; the library allocates nothing on
+ * any call.  Asynchrony: every call that takes a stream only enqueues work on
+ * it and returns; errors found on the host are returned before anything is
+ * enqueued.  Device-side faults of the bounded kind (a wait that timed out,
+ * an out-of-range page index) are recorded in a device word and reported by
+ * mla_check_device_error.  There is no CPU fallback: on a device that is not
+ * sm_103 every entry point that would launch returns MLA_ERR_UNSUPPORTED_DEVICE.
+ *
+ * Supported shapes: 1 <= h_q <= 128, 1 <= s_q <= 8 (s_q * h_q query rows per
+ * batch entry, processed in tiles of 128 rows), batch >= 1, page size 64,
+ * d_qk = 576, d_v = 512, num_pages * 64 < 2^31.  q and kv_cache must be 16-byte
+ * aligned, out 16-byte aligned, lse 4-byte aligned.
+ */
+#ifndef LIBMLA_MLA_H_
+#define LIBMLA_MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG (-1)        /* null pointer, misalignment, bad shape */
+#define MLA_ERR_WORKSPACE (-2)          /* plan or workspace buffer too small */
+#define MLA_ERR_CUDA (-3)               /* a CUDA runtime call or launch failed */
+#define MLA_ERR_DEVICE_TIMEOUT (-4)     /* a bounded device wait ran out */
+#define MLA_ERR_DEVICE_BOUNDS (-5)      /* a block_table entry was out of range */
+#define MLA_ERR_UNSUPPORTED_DEVICE (-6) /* the device is not sm_103 */
+#define MLA_ERR_PLAN (-7)               /* tile_meta does not match the call */
+
+/* Number of two-CTA clusters the decode kernel runs as a persistent grid on
+ * `device` (the SM count halved, limited by cluster occupancy).  Returns a
+ * negative code on error. */
+int mla_num_clusters(int device);
+
+/* Bytes of tile metadata for a plan of this shape on `device` (0 on error).
+ * The plan is the split-KV work partition: which pages of which batch entry
+ * each cluster processes, and how many partial results each entry has. */
+size_t mla_plan_size(int batch, int s_q, int h_q, int device);
+
+/* The same size for an explicit cluster count (what mla_decode_plan_host
+ * needs for `num_clusters`).  0 on error. */
+size_t mla_plan_size_for_clusters(int batch, int s_q, int h_q, int num_clusters);
+
+/* Bytes of scratch mla_decode needs for split partials (fp32 partial outputs
+ * and their lse) with a plan of this shape on `device` (0 on error).  The
+ * bound does not depend on sequence lengths. */
+size_t mla_workspace_size(int batch, int s_q, int h_q, int device);
+
+/* Split-KV planner (one small kernel).  Reads cache_seqlens (device int32
+ * [batch]) and writes the tile metadata to tile_meta (device, at least
+ * mla_plan_size bytes, 8-byte aligned).  One plan serves every layer of a
+ * decode step that shares the sequence lengths.  Negative lengths are
+ * treated as 0 and flagged as MLA_ERR_DEVICE_BOUNDS. */
+int mla_decode_plan(const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                    void* tile_meta, size_t tile_meta_bytes, void* stream);
+
+/* The same plan computed on the host from host sequence lengths, for
+ * `num_clusters` clusters; writes tile_meta_host (host memory).  The device
+ * planner produces bit-identical metadata for the same inputs. */
+int mla_decode_plan_host(const int32_t* cache_seqlens_host, int batch, int s_q, int h_q,
+                         int num_clusters, void* tile_meta_host, size_t tile_meta_bytes);
+
+/* Decode attention.  Launches the main kernel (persistent, two-CTA clusters;
+ * TMA page streaming, tcgen05 MMAs with TMEM accumulators, online softmax)
+ * and the LSE-combine kernel on `stream`.  tile_meta must come from
+ * mla_decode_plan (or the host variant, copied to the device) for the same
+ * batch, s_q, h_q and sequence lengths.  workspace: device scratch of at
+ * least mla_workspace_size bytes, 256-byte aligned; its contents on entry do
+ * not matter.  softmax_scale multiplies q.k before the softmax. */
+int mla_decode(const void* q, const void* kv_cache, int num_pages, const int32_t* block_table,
+               int max_pages, const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+               const void* tile_meta, void* out, float* lse, float softmax_scale,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The two halves of mla_decode, for callers that want to schedule (or time)
+ * them apart: mla_decode_attend launches only the main kernel (rows of batch
+ * entries with one split get their final out/lse; the others leave fp32
+ * partials in workspace), mla_decode_combine only the LSE-combine kernel
+ * that merges those partials into out/lse.  Same arguments and rules as
+ * mla_decode; the combine must follow the attend on the same stream with
+ * the same tile_meta and workspace. */
+int mla_decode_attend(const void* q, const void* kv_cache, int num_pages,
+                      const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                      int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
+                      float softmax_scale, void* workspace, size_t workspace_bytes, void* stream);
+int mla_decode_combine(int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device error word:
+ * MLA_OK, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_PLAN
+ * (or MLA_ERR_CUDA if the synchronisation itself failed). */
+int mla_check_device_error(void* stream);
+
+/* Static description of a return code. */
+const char* mla_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBMLA_MLA_H_ */

@@ -1,0 +1,587 @@
+// libmla C ABI: argument checks, tensor maps, the split-KV planner kernel,
+// the LSE-combine kernel, and the device error word.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "mla.h"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+__device__ int g_device_error;   // first device-side error of any launch, 0 if none
+
+constexpr int kMaxDevices = 64;
+constexpr int kPlanThreads = 1024;
+constexpr int kCombineWarps = 8;
+constexpr int kCombineRowsPerCta = kCombineWarps;
+
+// ------------------------------------------------------------------ planner
+// Exclusive prefix sum over the CTA; `total` receives the CTA-wide sum.
+__device__ long long block_exclusive_scan(long long v, long long* warp_sums, long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long s = lane < nwarps ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nwarps) warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const long long before = warp == 0 ? 0 : warp_sums[warp - 1];
+  total = warp_sums[nwarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* seqlens, int batch,
+                                                                int s_q, int h_q, int num_clusters,
+                                                                int32_t* plan, int* err) {
+  __shared__ long long warp_sums[32];
+  const int tiles = plan_tiles(s_q, h_q);
+  const int gt = plan_group_clusters(num_clusters, tiles);
+  int64_t* starts = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(plan) +
+                                               plan_off_starts(batch, gt));
+  int32_t* items = plan + plan_off_items(gt) / 4;
+  int32_t* clus = plan + H_WORDS;
+
+  // 1. unit intervals of the batch entries
+  long long run = 0;
+  for (int base = 0; base < batch; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int L = b < batch ? seqlens[b] : 0;
+    if (L < 0) {
+      atomicCAS(err, 0, MLA_ERR_DEVICE_BOUNDS);
+      L = 0;
+    }
+    const int P = pages_of(L);
+    long long tot;
+    const long long ex = block_exclusive_scan(units_of(P), warp_sums, tot);
+    if (b < batch) {
+      starts[b] = run + ex;
+      items[b * kItemWords + 0] = P;
+    }
+    run += tot;
+  }
+  if (threadIdx.x == 0) starts[batch] = run;
+  __syncthreads();
+  const long long V = run;
+  const int g = plan_used_clusters(V, gt);
+
+  // 2. cluster ranges
+  for (int c = threadIdx.x; c < gt; c += blockDim.x) {
+    int b0 = batch, p0 = 0, b1 = batch, p1 = 0, s0 = 0;
+    if (c < g) {
+      cursor_of(starts, batch, cluster_begin(c, V, g), &b0, &p0);
+      cursor_of(starts, batch, cluster_begin(c + 1, V, g), &b1, &p1);
+      if (b0 < batch) s0 = c - cluster_of(starts[b0] + kSplitOverhead, V, g);
+    }
+    int32_t* e = clus + c * kClusterWords;
+    e[0] = b0;
+    e[1] = p0;
+    e[2] = b1;
+    e[3] = p1;
+    e[4] = s0;
+    e[5] = 0;
+    e[6] = 0;
+    e[7] = 0;
+  }
+
+  // 3. splits per batch entry and where their partials go
+  run = 0;
+  for (int base = 0; base < batch; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int ns = 0, cf = -1;
+    if (b < batch) {
+      const int P = items[b * kItemWords + 0];
+      if (P > 0) {
+        cf = cluster_of(starts[b] + kSplitOverhead, V, g);
+        const int cl = cluster_of(starts[b] + kSplitOverhead + P - 1, V, g);
+        ns = cl - cf + 1;
+      }
+    }
+    long long tot;
+    const long long ex = block_exclusive_scan(ns >= 2 ? ns : 0, warp_sums, tot);
+    if (b < batch) {
+      items[b * kItemWords + 1] = ns;
+      items[b * kItemWords + 2] = (int)(run + ex);
+      items[b * kItemWords + 3] = cf;
+    }
+    run += tot;
+  }
+  if (threadIdx.x == 0) {
+    plan[H_MAGIC] = kPlanMagic;
+    plan[H_BATCH] = batch;
+    plan[H_SQ] = s_q;
+    plan[H_HQ] = h_q;
+    plan[H_TILES] = tiles;
+    plan[H_GT] = gt;
+    plan[H_GUSED] = g;
+    plan[H_STOTAL] = (int)run;
+    plan[H_OVH] = kSplitOverhead;
+    plan[H_NCLUSTERS] = num_clusters;
+    for (int k = H_NCLUSTERS + 1; k < H_WORDS; ++k) plan[k] = 0;
+  }
+}
+
+// Host mirror of mla_plan_kernel: the same integer formulas, in order.
+void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clusters,
+               int32_t* plan) {
+  const int tiles = plan_tiles(s_q, h_q);
+  const int gt = plan_group_clusters(num_clusters, tiles);
+  int64_t* starts = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(plan) +
+                                               plan_off_starts(batch, gt));
+  int32_t* items = plan + plan_off_items(gt) / 4;
+  int32_t* clus = plan + H_WORDS;
+  int64_t run = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int L = seqlens[b] < 0 ? 0 : seqlens[b];
+    const int P = pages_of(L);
+    starts[b] = run;
+    items[b * kItemWords + 0] = P;
+    run += units_of(P);
+  }
+  starts[batch] = run;
+  const int64_t V = run;
+  const int g = plan_used_clusters(V, gt);
+  for (int c = 0; c < gt; ++c) {
+    int b0 = batch, p0 = 0, b1 = batch, p1 = 0, s0 = 0;
+    if (c < g) {
+      cursor_of(starts, batch, cluster_begin(c, V, g), &b0, &p0);
+      cursor_of(starts, batch, cluster_begin(c + 1, V, g), &b1, &p1);
+      if (b0 < batch) s0 = c - cluster_of(starts[b0] + kSplitOverhead, V, g);
+    }
+    int32_t* e = clus + c * kClusterWords;
+    e[0] = b0;
+    e[1] = p0;
+    e[2] = b1;
+    e[3] = p1;
+    e[4] = s0;
+    e[5] = e[6] = e[7] = 0;
+  }
+  int64_t sb = 0;
+  for (int b = 0; b < batch; ++b) {
+    int ns = 0, cf = -1;
+    const int P = items[b * kItemWords + 0];
+    if (P > 0) {
+      cf = cluster_of(starts[b] + kSplitOverhead, V, g);
+      const int cl = cluster_of(starts[b] + kSplitOverhead + P - 1, V, g);
+      ns = cl - cf + 1;
+    }
+    items[b * kItemWords + 1] = ns;
+    items[b * kItemWords + 2] = (int)sb;
+    items[b * kItemWords + 3] = cf;
+    sb += ns >= 2 ? ns : 0;
+  }
+  plan[H_MAGIC] = kPlanMagic;
+  plan[H_BATCH] = batch;
+  plan[H_SQ] = s_q;
+  plan[H_HQ] = h_q;
+  plan[H_TILES] = tiles;
+  plan[H_GT] = gt;
+  plan[H_GUSED] = g;
+  plan[H_STOTAL] = (int)sb;
+  plan[H_OVH] = kSplitOverhead;
+  plan[H_NCLUSTERS] = num_clusters;
+  for (int k = H_NCLUSTERS + 1; k < H_WORDS; ++k) plan[k] = 0;
+}
+
+// ------------------------------------------------------------------ combine
+// Merges the split partials of every (batch entry, tile) that has two or
+// more splits:  lse = m + ln(sum_j exp(lse_j - m)),  out = sum_j
+// exp(lse_j - lse) * o_j.  Entries without pages get out = 0, lse = -inf.
+// One warp per query row; a lane owns 16 of the 512 output dims.
+__global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const DecodeParams p) {
+  const int32_t* plan = p.plan;
+  const int tiles = plan[H_TILES], gt = plan[H_GT], stotal = plan[H_STOTAL];
+  const int32_t* items = plan + plan_off_items(gt) / 4;
+  const int rows = p.s_q * p.h_q;
+  const int chunks = kTileRows / kCombineRowsPerCta;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t total = (int64_t)p.batch * tiles * chunks;
+  for (int64_t job = blockIdx.x; job < total; job += gridDim.x) {
+    const int chunk = (int)(job % chunks);
+    const int64_t item = job / chunks;
+    const int b = (int)(item % p.batch), t = (int)(item / p.batch);
+    const int ns = items[b * kItemWords + 1];
+    if (ns == 1) continue;
+    const int r = chunk * kCombineRowsPerCta + warp;
+    const int qr = t * kTileRows + r;
+    if (qr >= rows) continue;
+    const int i = qr / p.h_q, h = qr - i * p.h_q;
+    __nv_bfloat16* orow =
+        static_cast<__nv_bfloat16*>(p.out) + (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv;
+    float* lse_out = p.lse + ((int64_t)b * p.h_q + h) * p.s_q + i;
+    const int64_t slot0 = (int64_t)t * stotal + items[b * kItemWords + 2];
+    if (ns > 1 && (slot0 < 0 || slot0 + ns > workspace_slots(plan[H_NCLUSTERS]))) {
+      if (lane == 0) atomicCAS(p.err, 0, MLA_ERR_PLAN);
+      continue;
+    }
+
+    float m = -INFINITY;
+    if (ns > 1)
+      for (int j = lane; j < ns; j += 32) m = fmaxf(m, p.ws_lse[(slot0 + j) * kTileRows + r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float acc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+      float se = 0.f;
+      for (int j = lane; j < ns; j += 32) se += expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+      lse = m + logf(se);
+      for (int j = 0; j < ns; ++j) {
+        const float wgt = expf(p.ws_lse[(slot0 + j) * kTileRows + r] - lse);
+        const float4* o4 =
+            reinterpret_cast<const float4*>(p.ws_o + ((slot0 + j) * kTileRows + r) * kDv);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 v = o4[lane + 32 * q];
+          acc[4 * q + 0] += wgt * v.x;
+          acc[4 * q + 1] += wgt * v.y;
+          acc[4 * q + 2] += wgt * v.z;
+          acc[4 * q + 3] += wgt * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[4 * q + 0], acc[4 * q + 1]);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[4 * q + 2], acc[4 * q + 3]);
+      uint2 u;
+      memcpy(&u.x, &lo, 4);
+      memcpy(&u.y, &hi, 4);
+      *reinterpret_cast<uint2*>(orow + 4 * (lane + 32 * q)) = u;
+    }
+    if (lane == 0) *lse_out = lse;
+  }
+}
+
+// ------------------------------------------------------------------ device state
+struct DeviceState {
+  std::once_flag once;
+  int status = MLA_ERR_CUDA;  // MLA_OK once set up
+  int num_sms = 0;
+  int num_clusters = 0;
+  int* err = nullptr;         // address of g_device_error on this device
+};
+DeviceState g_dev[kMaxDevices];
+
+int setup_device(int device) {
+  if (device < 0 || device >= kMaxDevices) return MLA_ERR_INVALID_ARG;
+  DeviceState& d = g_dev[device];
+  std::call_once(d.once, [&]() {
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    if (prev != device && cudaSetDevice(device) != cudaSuccess) return;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      d.status = MLA_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      d.status = MLA_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      void* addr = nullptr;
+      const int maxc = decode_max_clusters(device);
+      if (maxc <= 0 || cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) {
+        d.status = MLA_ERR_CUDA;
+      } else {
+        d.num_sms = sms;
+        d.num_clusters = maxc < sms / 2 ? maxc : sms / 2;
+        d.err = static_cast<int*>(addr);
+        d.status = MLA_OK;
+      }
+    }
+    if (prev != device) cudaSetDevice(prev);
+  });
+  return d.status;
+}
+
+bool shape_ok(int batch, int s_q, int h_q) {
+  return batch >= 1 && s_q >= 1 && s_q <= 8 && h_q >= 1 && h_q <= 128;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over [rows, 576] with a (box_cols x box_rows) box.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows, CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kDqk, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDqk * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int64_t workspace_bytes_for(int num_clusters) {
+  const int64_t slots = workspace_slots(num_clusters);
+  return slots * kSlotFloats * 4 + slots * kTileRows * 4;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_num_clusters(int device) {
+  const int st = setup_device(device);
+  return st == MLA_OK ? g_dev[device].num_clusters : st;
+}
+
+size_t mla_plan_size_for_clusters(int batch, int s_q, int h_q, int num_clusters) {
+  if (!shape_ok(batch, s_q, h_q) || num_clusters < 1) return 0;
+  const int gt = plan_group_clusters(num_clusters, plan_tiles(s_q, h_q));
+  if (gt < 1) return 0;
+  return (size_t)plan_bytes(batch, gt);
+}
+
+size_t mla_plan_size(int batch, int s_q, int h_q, int device) {
+  const int nc = mla_num_clusters(device);
+  return nc > 0 ? mla_plan_size_for_clusters(batch, s_q, h_q, nc) : 0;
+}
+
+size_t mla_workspace_size(int batch, int s_q, int h_q, int device) {
+  if (!shape_ok(batch, s_q, h_q)) return 0;
+  const int nc = mla_num_clusters(device);
+  return nc > 0 ? (size_t)workspace_bytes_for(nc) : 0;
+}
+
+int mla_decode_plan_host(const int32_t* cache_seqlens_host, int batch, int s_q, int h_q,
+                         int num_clusters, void* tile_meta_host, size_t tile_meta_bytes) {
+  if (!cache_seqlens_host || !tile_meta_host || !shape_ok(batch, s_q, h_q) || num_clusters < 1 ||
+      !aligned(tile_meta_host, 8))
+    return MLA_ERR_INVALID_ARG;
+  const size_t need = mla_plan_size_for_clusters(batch, s_q, h_q, num_clusters);
+  if (need == 0) return MLA_ERR_INVALID_ARG;
+  if (tile_meta_bytes < need) return MLA_ERR_WORKSPACE;
+  plan_host(cache_seqlens_host, batch, s_q, h_q, num_clusters,
+            static_cast<int32_t*>(tile_meta_host));
+  return MLA_OK;
+}
+
+int mla_decode_plan(const int32_t* cache_seqlens, int batch, int s_q, int h_q, void* tile_meta,
+                    size_t tile_meta_bytes, void* stream) {
+  if (!cache_seqlens || !tile_meta || !shape_ok(batch, s_q, h_q) || !aligned(tile_meta, 8) ||
+      !aligned(cache_seqlens, 4))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = setup_device(device);
+  if (st != MLA_OK) return st;
+  const DeviceState& d = g_dev[device];
+  const size_t need = mla_plan_size_for_clusters(batch, s_q, h_q, d.num_clusters);
+  if (need == 0) return MLA_ERR_INVALID_ARG;
+  if (tile_meta_bytes < need) return MLA_ERR_WORKSPACE;
+  mla_plan_kernel<<<1, kPlanThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      cache_seqlens, batch, s_q, h_q, d.num_clusters, static_cast<int32_t*>(tile_meta), d.err);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Shared checks of the decode entry points; fills the kernel parameters.
+int prepare_decode(const void* q, const void* kv_cache, int num_pages, const int32_t* block_table,
+                   int max_pages, const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                   const void* tile_meta, void* out, float* lse, float softmax_scale,
+                   void* workspace, size_t workspace_bytes, DecodeParams* p, int* num_clusters,
+                   int* num_sms) {
+  if (!q || !kv_cache || !block_table || !cache_seqlens || !tile_meta || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if (!shape_ok(batch, s_q, h_q) || num_pages < 1 || max_pages < 1 ||
+      (int64_t)num_pages * kPageTokens >= ((int64_t)1 << 31) || !isfinite(softmax_scale))
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(block_table, 4) || !aligned(cache_seqlens, 4) || !aligned(tile_meta, 8))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = setup_device(device);
+  if (st != MLA_OK) return st;
+  const DeviceState& d = g_dev[device];
+  if (plan_group_clusters(d.num_clusters, plan_tiles(s_q, h_q)) < 1) return MLA_ERR_INVALID_ARG;
+  const int64_t need = workspace_bytes_for(d.num_clusters);
+  if (!workspace || (int64_t)workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  p->block_table = block_table;
+  p->seqlens = cache_seqlens;
+  p->plan = static_cast<const int32_t*>(tile_meta);
+  p->out = out;
+  p->lse = lse;
+  const int64_t slots = workspace_slots(d.num_clusters);
+  p->ws_o = static_cast<float*>(workspace);
+  p->ws_lse = static_cast<float*>(workspace) + slots * kSlotFloats;
+  p->err = d.err;
+  p->batch = batch;
+  p->s_q = s_q;
+  p->h_q = h_q;
+  p->max_pages = max_pages;
+  p->num_pages = num_pages;
+  p->scale_log2 = softmax_scale * 1.4426950408889634f;
+  *num_clusters = d.num_clusters;
+  *num_sms = d.num_sms;
+  return MLA_OK;
+}
+
+int attend(const void* q, const void* kv_cache, const DecodeParams& p, int num_clusters,
+           cudaStream_t s) {
+  TensorMaps maps;
+  const uint64_t q_rows = (uint64_t)p.batch * p.s_q * p.h_q;
+  const uint64_t kv_rows = (uint64_t)p.num_pages * kPageTokens;
+  if (!make_map(&maps.q_lat, q, q_rows, 64, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&maps.q_rope, q, q_rows, 32, kTileRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_map(&maps.kv_lat, kv_cache, kv_rows, 64, kPageTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map(&maps.kv_rope, kv_cache, kv_rows, 32, kPageTokens, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MLA_ERR_CUDA;
+  return launch_decode(maps, p, num_clusters, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_attend(const void* q, const void* kv_cache, int num_pages,
+                      const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                      int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
+                      float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  DecodeParams p;
+  int nc = 0, sms = 0;
+  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens,
+                                batch, s_q, h_q, tile_meta, out, lse, softmax_scale, workspace,
+                                workspace_bytes, &p, &nc, &sms);
+  if (rc != MLA_OK) return rc;
+  return attend(q, kv_cache, p, nc, static_cast<cudaStream_t>(stream));
+}
+
+int mla_decode_combine(int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!tile_meta || !out || !lse || !shape_ok(batch, s_q, h_q) || !aligned(tile_meta, 8) ||
+      !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = setup_device(device);
+  if (st != MLA_OK) return st;
+  const DeviceState& d = g_dev[device];
+  const int64_t need = workspace_bytes_for(d.num_clusters);
+  if (!workspace || (int64_t)workspace_bytes < need) return MLA_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  DecodeParams p = {};
+  p.plan = static_cast<const int32_t*>(tile_meta);
+  p.out = out;
+  p.lse = lse;
+  const int64_t slots = workspace_slots(d.num_clusters);
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_lse = static_cast<float*>(workspace) + slots * kSlotFloats;
+  p.err = d.err;
+  p.batch = batch;
+  p.s_q = s_q;
+  p.h_q = h_q;
+  return launch_combine(p, d.num_clusters, d.num_sms, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_decode(const void* q, const void* kv_cache, int num_pages, const int32_t* block_table,
+               int max_pages, const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+               const void* tile_meta, void* out, float* lse, float softmax_scale,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  DecodeParams p;
+  int nc = 0, sms = 0;
+  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens,
+                                batch, s_q, h_q, tile_meta, out, lse, softmax_scale, workspace,
+                                workspace_bytes, &p, &nc, &sms);
+  if (rc != MLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int a = attend(q, kv_cache, p, nc, s);
+  if (a != MLA_OK) return a;
+  return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_check_device_error(void* stream) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = setup_device(device);
+  if (st != MLA_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, g_dev[device].err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(g_dev[device].err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  return v;
+}
+
+const char* mla_strerror(int code) {
+  switch (code) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument (null pointer, misalignment or unsupported shape)";
+    case MLA_ERR_WORKSPACE: return "plan or workspace buffer too small";
+    case MLA_ERR_CUDA: return "CUDA runtime error";
+    case MLA_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
+    case MLA_ERR_DEVICE_BOUNDS: return "out-of-range page index or negative sequence length";
+    case MLA_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300)";
+    case MLA_ERR_PLAN: return "tile metadata does not match this call";
+    default: return "unknown error";
+  }
+}
+
+}  // extern "C"
+
+namespace mla {
+cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_sms,
+                           cudaStream_t stream) {
+  const int tiles = plan_tiles(p.s_q, p.h_q);
+  const int64_t jobs = (int64_t)p.batch * tiles * (kTileRows / kCombineRowsPerCta);
+  const int64_t cap = (int64_t)num_sms * 8;
+  const int grid = (int)(jobs < cap ? jobs : cap);
+  mla_combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+}  // namespace mla

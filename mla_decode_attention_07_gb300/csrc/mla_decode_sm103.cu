@@ -1,0 +1,712 @@
+// Paged MLA decode, main kernel, for sm_103a (GB300).
+//
+// What it computes: for each query row (batch b, query token i, head h),
+// softmax(scale * q . k_t) weighted sum of the first 512 dims of the visible
+// latent cache rows k_t, plus the log-sum-exp, over the pages assigned to this
+// cluster by the split-KV plan.  This is the DeepSeek MLA / FlashMLA decode
+// kernel that the TileLang talk walks through ("Tile级原语与自动推理机制融合，
+// TileAI社区发起人深度剖析TileLang核心技术与优势", section 什么是「TileLang」);
+// its online-softmax row max is the "accum_s -> scores_max" reduce whose
+// layout follows from the GEMM that produces accum_s (same section, step 2 of
+// layout inference): here that GEMM is a tcgen05 MMA with a 128-lane TMEM
+// accumulator, so one thread owns one row and the reduce is a per-thread loop.
+// As the talk's pipeline section says, only copies and GEMMs are truly
+// asynchronous, and the copies get their own pipeline stage: here a TMA
+// producer warp streams 64-token pages through an mbarrier ring.
+//
+// GB300 design (not the talk's):
+//  * One work unit is a cluster of two CTAs on two SMs.  A 128-row tile of
+//    queries has an fp32 output of 128 x 512 = all 512 TMEM columns of one SM,
+//    so CTA r owns output dims [256 r, 256 r + 256).
+//  * The 576-wide Q.K^T reduction is split between the CTAs as well: CTA r
+//    multiplies its latent half (dims [256 r, 256 r + 256)) plus half of the
+//    rotary dims ([512 + 32 r, 512 + 32 r + 32)).  Each CTA therefore loads
+//    exactly 36 KB of every 72 KB page: the pair reads each page once, with
+//    no duplicated tensor work.  The two 128 x 64 fp32 partial score tiles
+//    are exchanged over distributed shared memory (st.async with mbarrier
+//    transaction counts) and summed; both CTAs then run the same softmax on
+//    bit-identical scores, so their running maxima agree exactly.
+//  * Warp roles: warps 0-3 softmax + epilogue (one thread per TMEM lane =
+//    query row), warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.
+//  * S = Q K^T: M=128, N=64, 18 K-steps (16 latent + 2 rotary) into a double
+//    buffered TMEM score tile; O += P V: M=128, N=256, K=64 with V read from
+//    the same shared-memory page as K (as an MN-major operand).
+//  * Online softmax in the log2 domain with a lazy rescale: O is rescaled only
+//    when the row max grows by more than 2^8; the final 1/l and lse use the
+//    same (possibly stale) max, so the result is exact.
+//  * Every mbarrier wait is bounded (globaltimer); on expiry the kernel
+//    records MLA_ERR_DEVICE_TIMEOUT, tells the peer CTA, lets in-flight copies
+//    land, frees TMEM and returns.  No trap, no unbounded spin.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include "mla.h"
+#include "mla_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after an abort
+constexpr float kRescaleThreshold = 8.0f;           // log2 units
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// TMEM columns (fp32 / packed-bf16x2 32-bit cells, 128 lanes).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;     // [0, 256): this CTA's half of O
+constexpr uint32_t kColS = 256;   // two 64-column score tiles
+constexpr uint32_t kColP = 384;   // two 32-column bf16x2 probability tiles
+
+// Bytes moved per stage / per Q tile by one CTA.
+constexpr uint32_t kStageTx = 4 * 8192 + 4096;   // 4 latent boxes + rotary half
+constexpr uint32_t kQTx = 4 * 16384 + 8192;
+constexpr uint32_t kRecvTx = 128 * 64 * 4;
+
+template <bool P_TMEM>
+struct Cfg {
+  static constexpr int kStages = P_TMEM ? 3 : 2;
+  static constexpr int kPBufs = P_TMEM ? 2 : 1;
+  static constexpr uint32_t kQLat = 0;                 // 4 x [128 x 64] bf16, 128B swizzle
+  static constexpr uint32_t kQRope = 65536;            // [128 x 32] bf16, 64B swizzle
+  static constexpr uint32_t kStage0 = 73728;           // kStages x 36 KB
+  static constexpr uint32_t kStageBytes = 36864;
+  static constexpr uint32_t kStageRope = 32768;        // rotary box inside a stage
+  static constexpr uint32_t kP = kStage0 + kStages * kStageBytes;  // smem P (if used)
+  static constexpr uint32_t kRecv = kP + (P_TMEM ? 0u : 16384u);   // [128 x 64] fp32
+  static constexpr uint32_t kBar = kRecv + kRecvTx;
+  static constexpr uint32_t kMisc = kBar + 8 * 32;
+  static constexpr uint32_t kBytes = kMisc + 64;
+  static constexpr uint32_t kAlloc = kBytes + 1024;    // slack for 1024-byte alignment
+};
+
+enum Bar : uint32_t {
+  B_FULL = 0,      // [3] stage loaded (TMA tx)
+  B_EMPTY = 3,     // [3] stage consumed (MMA commit)
+  B_QFULL = 6,
+  B_QEMPTY = 7,
+  B_SFULL = 8,     // [2]
+  B_SEMPTY = 10,   // [2]
+  B_PFULL = 12,    // [2]
+  B_PEMPTY = 14,   // [2]
+  B_OFULL = 16,
+  B_OEMPTY = 17,
+  B_RFULL = 18,    // peer's partial scores arrived (st.async tx)
+  B_REMPTY = 19,   // peer consumed what this CTA sent
+  B_TEARDOWN = 20,
+};
+
+struct Ctx {
+  uint32_t sbase;       // 1024-aligned shared base
+  uint32_t tmem;        // TMEM base address
+  uint32_t rank, peer;
+  uint32_t abort_addr, peer_abort_addr;
+  int* err;
+  __device__ __forceinline__ uint32_t bar(uint32_t i) const { return sbase + kBarOff + 8u * i; }
+  uint32_t kBarOff;
+};
+
+__device__ __forceinline__ void abort_all(const Ctx& x) {
+  atomicCAS(x.err, 0, MLA_ERR_DEVICE_TIMEOUT);
+  ptx::st_shared_u32(x.abort_addr, 1u);
+  ptx::st_cluster_u32(x.peer_abort_addr, 1u);
+}
+
+// Bounded wait for the phase with parity `parity` of mbarrier `bar`.
+__device__ __forceinline__ bool wait_bar(const Ctx& x, uint32_t bar, uint32_t parity,
+                                         bool cluster_scope = false) {
+  if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+    return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity))
+      return true;
+    if ((i & 63u) == 0u) {
+      if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) return false;
+      if (ptx::globaltimer() - t0 > kWaitTimeoutNs) {
+        abort_all(x);
+        return false;
+      }
+    }
+  }
+}
+
+// The same, decided for the whole warp: a lane that gives up makes every lane
+// give up, so warp-collective tcgen05 instructions after it are never reached
+// by part of a warp.
+__device__ __forceinline__ bool wait_warp(const Ctx& x, uint32_t bar, uint32_t parity,
+                                          bool cluster_scope = false) {
+  const bool ok = wait_bar(x, bar, parity, cluster_scope);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Segments of the cluster's page range: item b, pages [pb, pe).
+struct SegIter {
+  int b, p, b1, p1;
+  const int32_t* items;
+  __device__ __forceinline__ bool next(int& sb, int& spb, int& spe) {
+    while (b < b1 || (b == b1 && p < p1)) {
+      const int P = items[b * kItemWords + 0];
+      const int pe = (b == b1) ? p1 : P;
+      const int cb = b, cp = p;
+      b += 1;
+      p = 0;
+      if (cp < pe) {
+        sb = cb;
+        spb = cp;
+        spe = pe;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+struct Work {
+  int tile, rows, b0, p0, b1, p1, split0, stotal;
+  const int32_t* items;
+};
+
+// 32 consecutive TMEM columns of this warp's 32 lanes, loaded and waited on
+// in one statement so no use of the registers can be scheduled before the
+// wait.
+__device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// ------------------------------------------------------------------ producer
+template <bool P_TMEM>
+__device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const DecodeParams& prm,
+                                             const CUtensorMap* tm_q_lat,
+                                             const CUtensorMap* tm_q_rope,
+                                             const CUtensorMap* tm_kv_lat,
+                                             const CUtensorMap* tm_kv_rope) {
+  using C = Cfg<P_TMEM>;
+  const uint64_t policy = ptx::policy_evict_first();
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0, n_item = 0;
+  const int32_t xq_lat = 256 * (int32_t)x.rank, xq_rope = 512 + 32 * (int32_t)x.rank;
+  while (it.next(b, pb, pe)) {
+    if (!wait_bar(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
+    ptx::mbar_arrive_expect_tx(x.bar(B_QFULL), kQTx);
+    const int32_t row0 = b * w.rows + w.tile * kTileRows;
+    for (int ch = 0; ch < 4; ++ch)
+      ptx::tma_load_2d(x.sbase + C::kQLat + ch * 16384, tm_q_lat, xq_lat + 64 * ch, row0,
+                       x.bar(B_QFULL));
+    ptx::tma_load_2d(x.sbase + C::kQRope, tm_q_rope, xq_rope, row0, x.bar(B_QFULL));
+
+    // Entries past max_pages are never read: a sequence longer than its
+    // block-table row is reported and served from page 0.
+    const int32_t* bt = prm.block_table + (size_t)b * prm.max_pages;
+    int next_page = pb < prm.max_pages ? bt[pb] : -1;
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      int page = next_page;
+      if (pg + 1 < pe) next_page = pg + 1 < prm.max_pages ? bt[pg + 1] : -1;
+      const uint32_t s = g % C::kStages, k = g / C::kStages;
+      if (!wait_bar(x, x.bar(B_EMPTY + s), (k & 1u) ^ 1u)) return false;
+      if ((unsigned)page >= (unsigned)prm.num_pages) {
+        atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+        page = 0;
+      }
+      ptx::mbar_arrive_expect_tx(x.bar(B_FULL + s), kStageTx);
+      const int32_t y = page * kPageTokens;
+      const uint32_t st = x.sbase + C::kStage0 + s * C::kStageBytes;
+      for (int ch = 0; ch < 4; ++ch)
+        ptx::tma_load_2d_hint(st + ch * 8192, tm_kv_lat, xq_lat + 64 * ch, y, x.bar(B_FULL + s),
+                              policy);
+      ptx::tma_load_2d_hint(st + C::kStageRope, tm_kv_rope, xq_rope, y, x.bar(B_FULL + s), policy);
+    }
+    ++n_item;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <bool P_TMEM>
+__device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
+  using C = Cfg<P_TMEM>;
+  constexpr uint32_t id_qk = ptx::idesc_bf16_f32(128, 64, 0, 0);
+  constexpr uint32_t id_pv = ptx::idesc_bf16_f32(128, 256, 0, 1);
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0, n_item = 0;
+  bool have_prev = false, prev_first = false, prev_last = false;
+  uint32_t prev_g = 0, prev_item = 0;
+
+  auto issue_pv = [&]() -> bool {
+    const uint32_t s = prev_g % C::kStages;
+    if (prev_first && !wait_bar(x, x.bar(B_OEMPTY), (prev_item & 1u) ^ 1u)) return false;
+    const uint32_t pbuf = prev_g % C::kPBufs, pk = prev_g / C::kPBufs;
+    if (!wait_bar(x, x.bar(B_PFULL + pbuf), pk & 1u)) return false;
+    ptx::tc_fence_after();
+    const uint32_t vbase = x.sbase + C::kStage0 + s * C::kStageBytes;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      // V as the MN-major B operand: 64-dim swizzle atoms 8 KB apart along N,
+      // 8-token row groups 1 KB apart along K; 16 tokens per K-step.
+      const uint64_t bdesc = ptx::smem_desc(vbase + k * 2048, 8192, 1024, ptx::kLayoutSw128);
+      const uint32_t acc = (prev_first && k == 0) ? 0u : 1u;
+      if constexpr (P_TMEM) {
+        ptx::mma_ts(x.tmem + kColO, x.tmem + kColP + pbuf * 32 + k * 8, bdesc, id_pv, acc);
+      } else {
+        const uint64_t adesc =
+            ptx::smem_desc(x.sbase + C::kP + k * 32, 16, 1024, ptx::kLayoutSw128);
+        ptx::mma_ss(x.tmem + kColO, adesc, bdesc, id_pv, acc);
+      }
+    }
+    ptx::mma_commit(x.bar(B_EMPTY + s));
+    ptx::mma_commit(x.bar(B_PEMPTY + pbuf));
+    if (prev_last) ptx::mma_commit(x.bar(B_OFULL));
+    return true;
+  };
+
+  while (it.next(b, pb, pe)) {
+    if (!wait_bar(x, x.bar(B_QFULL), n_item & 1u)) return false;
+    ptx::tc_fence_after();
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      const uint32_t s = g % C::kStages;
+      if (!wait_bar(x, x.bar(B_FULL + s), (g / C::kStages) & 1u)) return false;
+      const uint32_t sb = g & 1u;
+      if (!wait_bar(x, x.bar(B_SEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
+      ptx::tc_fence_after();
+      const uint32_t st = x.sbase + C::kStage0 + s * C::kStageBytes;
+      const uint32_t d_s = x.tmem + kColS + sb * 64;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t adesc =
+              ptx::smem_desc(x.sbase + C::kQLat + ch * 16384 + k * 32, 16, 1024, ptx::kLayoutSw128);
+          const uint64_t bdesc =
+              ptx::smem_desc(st + ch * 8192 + k * 32, 16, 1024, ptx::kLayoutSw128);
+          ptx::mma_ss(d_s, adesc, bdesc, id_qk, (ch | k) ? 1u : 0u);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint64_t adesc =
+            ptx::smem_desc(x.sbase + C::kQRope + k * 32, 16, 512, ptx::kLayoutSw64);
+        const uint64_t bdesc =
+            ptx::smem_desc(st + C::kStageRope + k * 32, 16, 512, ptx::kLayoutSw64);
+        ptx::mma_ss(d_s, adesc, bdesc, id_qk, 1u);
+      }
+      ptx::mma_commit(x.bar(B_SFULL + sb));
+      if (pg == pe - 1) ptx::mma_commit(x.bar(B_QEMPTY));
+      if (have_prev && !issue_pv()) return false;
+      have_prev = true;
+      prev_g = g;
+      prev_first = (pg == pb);
+      prev_last = (pg == pe - 1);
+      prev_item = n_item;
+    }
+    ++n_item;
+  }
+  if (have_prev && !issue_pv()) return false;
+  return true;
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+template <bool P_TMEM>
+__device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const DecodeParams& prm,
+                                            int warp, int lane) {
+  using C = Cfg<P_TMEM>;
+  const int r = warp * 32 + lane;                   // tile row == TMEM lane
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t recv_row = x.sbase + C::kRecv + (uint32_t)r * 256u;
+  const uint32_t peer_recv_row = ptx::map_to_rank(recv_row, x.peer);
+  const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
+  const uint32_t peer_rempty = ptx::map_to_rank(x.bar(B_REMPTY), x.peer);
+  const uint32_t swz = (uint32_t)(r & 15);
+  const float scale_log2 = prm.scale_log2;
+
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0, n_item = 0;
+  while (it.next(b, pb, pe)) {
+    const int qr = w.tile * kTileRows + r;
+    const bool valid = qr < w.rows;
+    const int i = qr / prm.h_q;
+    const int h = qr - i * prm.h_q;
+    const int L = prm.seqlens[b];
+    const int n_valid = valid ? L - prm.s_q + 1 + i : 0;
+    const int P_total = w.items[b * kItemWords + 0];
+    float m_run = -INFINITY, l_run = 0.f;
+
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      const bool first = (pg == pb);
+      const uint32_t sb = g & 1u;
+      if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
+      ptx::tc_fence_after();
+      float s[64];
+      {
+        uint32_t v[32];
+        tmem_load32(x.tmem + lane_base + kColS + sb * 64, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
+        tmem_load32(x.tmem + lane_base + kColS + sb * 64 + 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(v[k]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+
+      // Exchange partial scores with the peer CTA: send mine into its receive
+      // buffer, take its partial from mine.  16-byte chunks are XOR-swizzled
+      // by row to spread the rows over the shared-memory banks.
+      if (!wait_warp(x, x.bar(B_REMPTY), (g & 1u) ^ 1u, true)) return false;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        ptx::st_async_v4(peer_recv_row + (((uint32_t)c ^ swz) << 4), s[4 * c], s[4 * c + 1],
+                         s[4 * c + 2], s[4 * c + 3], peer_rfull);
+      if (r == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL), kRecvTx);
+      if (!wait_warp(x, x.bar(B_RFULL), g & 1u, true)) return false;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float4 v = ptx::ld_shared_v4f(recv_row + (((uint32_t)c ^ swz) << 4));
+        s[4 * c] += v.x;   // addition commutes: both CTAs get identical sums
+        s[4 * c + 1] += v.y;
+        s[4 * c + 2] += v.z;
+        s[4 * c + 3] += v.w;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(peer_rempty);
+
+      // Mask, scale into log2 units, row max (the accum_s -> scores_max reduce).
+      const int tok0 = pg * kPageTokens;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        s[k] = (tok0 + k < n_valid) ? s[k] * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
+
+      const uint32_t pbuf = g % C::kPBufs;
+      if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / C::kPBufs) & 1u) ^ 1u)) return false;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (C::kPBufs == 2) {
+          // O must hold every page before this one: wait for the previous P.V.
+          const uint32_t gp = g - 1;
+          if (!wait_warp(x, x.bar(B_PEMPTY + (gp & 1u)), (gp >> 1) & 1u)) return false;
+        }
+        ptx::tc_fence_after();
+        const float alpha = rescale ? exp2f(m_run - m_new) : 1.0f;
+#pragma unroll 1
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t v[32];
+          const uint32_t ta = x.tmem + lane_base + kColO + ch * 32;
+          tmem_load32(ta, v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+          ptx::tmem_st32(ta, v);
+        }
+        ptx::tmem_wait_st();
+        if (rescale) {
+          l_run *= alpha;
+          m_run = m_new;
+        }
+      }
+      if (first) m_run = m_new;
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      uint32_t pk[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a = exp2f(s[2 * j] - m_use);
+        const float c = exp2f(s[2 * j + 1] - m_use);
+        psum += a + c;
+        pk[j] = ptx::pack_bf16x2(a, c);
+      }
+      l_run += psum;
+
+      // Past the end of the sequence the cache slots of the last page hold
+      // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
+      // the P.V MMA, so zero those value rows first.
+      if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
+        const int t0 = L & (kPageTokens - 1);
+        const uint32_t st = x.sbase + C::kStage0 + (g % C::kStages) * C::kStageBytes;
+        const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
+        for (int idx = r; idx < n16; idx += kSoftmaxWarps * 32) {
+          const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
+          ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+        }
+      }
+      if constexpr (P_TMEM) {
+        ptx::tmem_st32(x.tmem + lane_base + kColP + pbuf * 32, pk);
+        ptx::tmem_wait_st();
+      } else {
+        const uint32_t prow = x.sbase + C::kP + (uint32_t)r * 128u;
+        const uint32_t pswz = (uint32_t)(r & 7);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
+                            pk[4 * c + 2], pk[4 * c + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
+    }
+
+    // Epilogue: O / l, lse = (m + log2 l) * ln 2.
+    if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
+    ptx::tc_fence_after();
+    const int ns = w.items[b * kItemWords + 1];
+    const bool direct = (ns == 1);
+    const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+    const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+    const int sidx = (n_item == 0) ? w.split0 : 0;
+    const int64_t slot = (int64_t)w.tile * w.stotal + w.items[b * kItemWords + 2] + sidx;
+    const int64_t orow = ((int64_t)b * prm.s_q + i) * prm.h_q + h;
+#pragma unroll 1
+    for (int ch = 0; ch < 8; ++ch) {
+      uint32_t v[32];
+      tmem_load32(x.tmem + lane_base + kColO + ch * 32, v);
+      if (valid) {
+        const int d0 = (int)x.rank * 256 + ch * 32;
+        if (direct) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
+                                                orow * kDv + d0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv_l,
+                                   __uint_as_float(v[8 * q + 1]) * inv_l);
+            u.y = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv_l,
+                                   __uint_as_float(v[8 * q + 3]) * inv_l);
+            u.z = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv_l,
+                                   __uint_as_float(v[8 * q + 5]) * inv_l);
+            u.w = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv_l,
+                                   __uint_as_float(v[8 * q + 7]) * inv_l);
+            dst[q] = u;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(prm.ws_o + (slot * kTileRows + r) * kDv + d0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l,
+                                 __uint_as_float(v[4 * q + 1]) * inv_l,
+                                 __uint_as_float(v[4 * q + 2]) * inv_l,
+                                 __uint_as_float(v[4 * q + 3]) * inv_l);
+        }
+      }
+    }
+    if (valid && x.rank == 0) {
+      if (direct)
+        prm.lse[((int64_t)b * prm.h_q + h) * prm.s_q + i] = lse_v;
+      else
+        prm.ws_lse[slot * kTileRows + r] = lse_v;
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(x.bar(B_OEMPTY));
+    ++n_item;
+  }
+  return true;
+}
+
+template <bool P_TMEM>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
+                      const __grid_constant__ CUtensorMap tm_q_rope,
+                      const __grid_constant__ CUtensorMap tm_kv_lat,
+                      const __grid_constant__ CUtensorMap tm_kv_rope, const DecodeParams prm) {
+  using C = Cfg<P_TMEM>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();
+  const int cluster = (int)(blockIdx.x >> 1);
+
+  // The plan must describe this call; both CTAs of a cluster take the same
+  // early exits, before any barrier or TMEM is set up.
+  const int32_t* plan = prm.plan;
+  if (plan[H_MAGIC] != kPlanMagic || plan[H_BATCH] != prm.batch || plan[H_SQ] != prm.s_q ||
+      plan[H_HQ] != prm.h_q || plan[H_NCLUSTERS] != (int)(gridDim.x >> 1)) {
+    if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
+    return;
+  }
+  Work w;
+  const int tiles = plan[H_TILES], gt = plan[H_GT], gused = plan[H_GUSED];
+  if (gt <= 0) return;
+  w.tile = cluster / gt;
+  const int c = cluster - w.tile * gt;
+  if (w.tile >= tiles || c >= gused) return;
+  const int32_t* cl = plan + H_WORDS + c * kClusterWords;
+  w.b0 = cl[0];
+  w.p0 = cl[1];
+  w.b1 = cl[2];
+  w.p1 = cl[3];
+  w.split0 = cl[4];
+  if (w.b0 < 0 || w.p0 < 0 || w.p1 < 0 || w.b0 > w.b1 || w.b1 > prm.batch ||
+      (w.b1 == prm.batch && w.p1 != 0)) {
+    if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
+    return;
+  }
+  if (w.b0 == w.b1 && w.p0 >= w.p1) return;
+  w.rows = prm.s_q * prm.h_q;
+  w.stotal = plan[H_STOTAL];
+  w.items = plan + plan_off_items(gt) / 4;
+
+  Ctx x;
+  x.sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
+  x.kBarOff = C::kBar;
+  x.rank = rank;
+  x.peer = rank ^ 1u;
+  x.err = prm.err;
+  const uint32_t tmem_slot = x.sbase + C::kMisc;
+  x.abort_addr = x.sbase + C::kMisc + 4;
+  x.peer_abort_addr = ptx::map_to_rank(x.abort_addr, x.peer);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(x.bar(B_FULL + s), 1);
+      ptx::mbar_init(x.bar(B_EMPTY + s), 1);
+    }
+    ptx::mbar_init(x.bar(B_QFULL), 1);
+    ptx::mbar_init(x.bar(B_QEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(x.bar(B_SFULL + s), 1);
+      ptx::mbar_init(x.bar(B_SEMPTY + s), kSoftmaxWarps);
+      ptx::mbar_init(x.bar(B_PFULL + s), kSoftmaxWarps);
+      ptx::mbar_init(x.bar(B_PEMPTY + s), 1);
+    }
+    ptx::mbar_init(x.bar(B_OFULL), 1);
+    ptx::mbar_init(x.bar(B_OEMPTY), kSoftmaxWarps);
+    ptx::mbar_init(x.bar(B_RFULL), 1);
+    ptx::mbar_init(x.bar(B_REMPTY), kSoftmaxWarps);
+    ptx::mbar_init(x.bar(B_TEARDOWN), 1);
+    ptx::st_shared_u32(x.abort_addr, 0u);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&tm_q_lat);
+    ptx::prefetch_tmap(&tm_q_rope);
+    ptx::prefetch_tmap(&tm_kv_lat);
+    ptx::prefetch_tmap(&tm_kv_rope);
+  }
+  ptx::tc_fence_before();
+  ptx::cluster_sync();   // both CTAs' barriers initialised and TMEM allocated
+  ptx::tc_fence_after();
+  x.tmem = ptx::ld_shared_u32_volatile(tmem_slot);
+
+  if (warp == kProducerWarp) {
+    if (lane == 0)
+      run_producer<P_TMEM>(x, w, prm, &tm_q_lat, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) run_mma<P_TMEM>(x, w);
+    __syncwarp();
+  } else {
+    run_softmax<P_TMEM>(x, w, prm, warp, lane);
+    __syncwarp();
+  }
+
+  // Teardown.  After an abort, give in-flight copies and MMAs time to land
+  // before the shared memory and TMEM are released.
+  const bool aborted = ptx::ld_shared_u32_volatile(x.abort_addr) != 0u;
+  if (warp == kMmaWarp && lane == 0) {
+    ptx::mma_commit(x.bar(B_TEARDOWN));
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(x.bar(B_TEARDOWN), 0u)) {
+      if (ptx::globaltimer() - t0 > kWaitTimeoutNs) {
+        atomicCAS(x.err, 0, MLA_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+    }
+  }
+  if (aborted) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < kDrainNs) __nanosleep(1000);
+  }
+  __syncwarp();
+  ptx::tc_fence_before();
+  ptx::cluster_sync();   // no remote traffic into either CTA after this point
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(x.tmem, kTmemCols);
+  }
+}
+
+bool use_p_tmem() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("MLA_DECODE_P_SMEM");
+    v = (e && e[0] == '1') ? 0 : 1;
+  }
+  return v == 1;
+}
+
+}  // namespace
+
+int decode_smem_bytes() {
+  return use_p_tmem() ? (int)Cfg<true>::kAlloc : (int)Cfg<false>::kAlloc;
+}
+
+cudaError_t decode_kernel_setup(int /*device*/) {
+  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)Cfg<true>::kAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)Cfg<false>::kAlloc);
+}
+
+int decode_max_clusters(int device) {
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return -1;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return -1;
+  int n = -1;
+  if (decode_kernel_setup(device) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)decode_smem_bytes();
+    int m = 0;
+    cudaError_t e = use_p_tmem()
+                        ? cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel<true>, &cfg)
+                        : cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel<false>, &cfg);
+    if (e == cudaSuccess) n = m;
+  }
+  if (prev != device) cudaSetDevice(prev);
+  return n;
+}
+
+cudaError_t launch_decode(const TensorMaps& m, const DecodeParams& p, int num_clusters,
+                          cudaStream_t stream) {
+  const dim3 grid(2 * num_clusters), block(kThreads);
+  if (use_p_tmem())
+    mla_decode_kernel<true><<<grid, block, Cfg<true>::kAlloc, stream>>>(m.q_lat, m.q_rope,
+                                                                         m.kv_lat, m.kv_rope, p);
+  else
+    mla_decode_kernel<false><<<grid, block, Cfg<false>::kAlloc, stream>>>(m.q_lat, m.q_rope,
+                                                                           m.kv_lat, m.kv_rope, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

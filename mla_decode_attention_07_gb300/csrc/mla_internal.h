@@ -1,0 +1,51 @@
+// Internal interfaces between the translation units of libmla.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla_plan.h"
+
+namespace mla {
+
+constexpr int kDqk = 576;  // latent (512) + rotary (64) dims per cache row
+constexpr int kDv = 512;   // value dims = the first 512 dims of the row
+
+// Everything the decode kernel needs besides its four tensor maps.
+struct DecodeParams {
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  const int32_t* plan;
+  void* out;          // bf16 [B, s_q, h_q, 512]
+  float* lse;         // fp32 [B, h_q, s_q]
+  float* ws_o;        // fp32 [slots, 128, 512]
+  float* ws_lse;      // fp32 [slots, 128]
+  int* err;           // device error word
+  int batch, s_q, h_q, max_pages, num_pages;
+  float scale_log2;   // softmax_scale * log2(e)
+};
+
+struct TensorMaps {
+  CUtensorMap q_lat, q_rope, kv_lat, kv_rope;
+};
+
+// Partial results: one slot holds 128 rows x 512 fp32 plus 128 lse values.
+constexpr int64_t kSlotFloats = (int64_t)kTileRows * kDv;
+
+// Upper bound on the split slots any plan for `num_clusters` clusters needs:
+// every group of clusters has at most 2 * (clusters in group) split parts
+// belonging to entries with two or more splits.
+MLA_HD int64_t workspace_slots(int num_clusters) { return 2 * (int64_t)num_clusters; }
+
+// Decode kernel (mla_decode_sm103.cu).
+int decode_smem_bytes();
+cudaError_t decode_kernel_setup(int device);
+int decode_max_clusters(int device);  // co-resident 2-CTA clusters, or < 0
+cudaError_t launch_decode(const TensorMaps& maps, const DecodeParams& p, int num_clusters,
+                          cudaStream_t stream);
+
+// Combine kernel (mla_api.cu).
+cudaError_t launch_combine(const DecodeParams& p, int num_clusters, int num_sms,
+                           cudaStream_t stream);
+
+}  // namespace mla

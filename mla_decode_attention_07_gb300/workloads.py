@@ -70,26 +70,38 @@ def bf16_bits_to_float32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def normal_bf16(seed: int, tensor_id: int, n: int, chunk: int = 1 << 22) -> np.ndarray:
-    """``n`` N(0,1) samples rounded to bf16 bits, deterministic in (seed, tensor_id)."""
+def _normal_chunk(start: int, first_pair: int, pairs: int, out: np.ndarray, n: int) -> None:
+    z = splitmix64(start, 2 * first_pair, 2 * pairs)
+    u1 = _uniform01(z[0::2])
+    u2 = _uniform01(z[1::2])
+    r = np.sqrt(-2.0 * np.log(u1))
+    th = 2.0 * math.pi * u2
+    vals = np.empty(2 * pairs, dtype=np.float64)
+    vals[0::2] = r * np.cos(th)
+    vals[1::2] = r * np.sin(th)
+    lo = 2 * first_pair
+    hi = min(n, lo + 2 * pairs)
+    out[lo:hi] = float32_to_bf16_bits(vals[: hi - lo].astype(np.float32))
+
+
+def normal_bf16(seed: int, tensor_id: int, n: int, chunk: int = 1 << 20) -> np.ndarray:
+    """``n`` N(0,1) samples rounded to bf16 bits, deterministic in (seed, tensor_id).
+
+    Large requests are cut into fixed chunks that threads fill independently;
+    the values do not depend on the chunking or the thread count.
+    """
     start = (seed ^ tensor_id) & 0xFFFFFFFFFFFFFFFF
     out = np.empty(n, dtype=np.uint16)
     pairs_total = (n + 1) // 2
-    done = 0
-    while done < pairs_total:
-        m = min(chunk, pairs_total - done)
-        z = splitmix64(start, 2 * done, 2 * m)
-        u1 = _uniform01(z[0::2])
-        u2 = _uniform01(z[1::2])
-        r = np.sqrt(-2.0 * np.log(u1))
-        th = 2.0 * math.pi * u2
-        vals = np.empty(2 * m, dtype=np.float64)
-        vals[0::2] = r * np.cos(th)
-        vals[1::2] = r * np.sin(th)
-        lo = 2 * done
-        hi = min(n, lo + 2 * m)
-        out[lo:hi] = float32_to_bf16_bits(vals[: hi - lo].astype(np.float32))
-        done += m
+    jobs = [(p0, min(chunk, pairs_total - p0)) for p0 in range(0, pairs_total, chunk)]
+    if len(jobs) <= 1:
+        for p0, m in jobs:
+            _normal_chunk(start, p0, m, out, n)
+        return out
+    import concurrent.futures as cf
+    import os
+    with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 1)) as ex:
+        list(ex.map(lambda j: _normal_chunk(start, j[0], j[1], out, n), jobs))
     return out
 
 

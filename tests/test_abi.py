@@ -1,0 +1,82 @@
+"""The C ABI loads, exports every declared symbol, and rejects bad arguments
+on the host before touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_decode_attention_07_gb300 import libmla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    return libmla.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names and set(names) == set(libmla.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror(lib):
+    for code in range(0, -8, -1):
+        s = libmla.mla_strerror(code)
+        assert s and s != "unknown error"
+    assert libmla.mla_strerror(-99) == "unknown error"
+
+
+def _decode(lib, **kw):
+    a = dict(q=0x1000, kv=0x2000, num_pages=4, bt=0x3000, max_pages=4, sl=0x4000, batch=1, s_q=1,
+             h_q=16, meta=0x5000, out=0x6000, lse=0x7000, scale=0.07, ws=0x8000,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.mla_decode(a["q"], a["kv"], a["num_pages"], a["bt"], a["max_pages"], a["sl"],
+                          a["batch"], a["s_q"], a["h_q"], a["meta"], a["out"], a["lse"],
+                          ctypes.c_float(a["scale"]), a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(kv=None), dict(bt=None), dict(sl=None), dict(meta=None), dict(out=None),
+    dict(lse=None), dict(batch=0), dict(s_q=0), dict(s_q=9), dict(h_q=0), dict(h_q=129),
+    dict(num_pages=0), dict(max_pages=0), dict(num_pages=1 << 25), dict(q=0x1008),
+    dict(kv=0x2004), dict(out=0x6002), dict(lse=0x7002), dict(scale=float("nan")),
+])
+def test_decode_rejects_bad_args_on_host(lib, kw):
+    assert _decode(lib, **kw) == libmla.MLA_ERR_INVALID_ARG
+
+
+def test_plan_rejects_bad_args_on_host(lib):
+    assert lib.mla_decode_plan(None, 1, 1, 16, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_plan(0x4000, 1, 1, 0, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
+    assert lib.mla_decode_plan(0x4000, 1, 1, 16, 0x5004, 4096, None) == libmla.MLA_ERR_INVALID_ARG
+
+
+def test_plan_host_checks_buffer_size(lib):
+    import numpy as np
+    sl = np.array([100], dtype=np.int32)
+    meta = np.zeros(4, dtype=np.int64)
+    rc = lib.mla_decode_plan_host(sl.ctypes.data, 1, 1, 16, 8, meta.ctypes.data, meta.nbytes)
+    assert rc == libmla.MLA_ERR_WORKSPACE
+
+
+def test_no_gpu_means_error_not_fallback(lib):
+    from conftest import gpu_available
+    if gpu_available():
+        pytest.skip("a GPU is present")
+    # Valid-looking arguments: the only thing missing is the device.
+    assert _decode(lib) in (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
+    assert lib.mla_num_clusters(0) < 0
+    assert lib.mla_plan_size(1, 1, 16, 0) == 0
