@@ -350,7 +350,10 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
     const int L = prm.seqlens[b];
     const int n_valid = valid ? L - prm.s_q + 1 + i : 0;
     const int P_total = w.items[b * kItemWords + 0];
-    float m_run = -INFINITY, l_run = 0.f;
+    // l_run sums the fp32 probabilities (for lse); lb_run sums them after the
+    // bf16 rounding the P.V MMA sees, so out = sum(p v) / sum(p) uses one set
+    // of weights and stays a true weighted average of the value rows.
+    float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
 
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const bool first = (pg == pb);
@@ -425,21 +428,24 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
         ptx::tmem_wait_st();
         if (rescale) {
           l_run *= alpha;
+          lb_run *= alpha;
           m_run = m_new;
         }
       }
       if (first) m_run = m_new;
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       uint32_t pk[32];
-      float psum = 0.f;
+      float psum = 0.f, pbsum = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float a = exp2f(s[2 * j] - m_use);
         const float c = exp2f(s[2 * j + 1] - m_use);
         psum += a + c;
         pk[j] = ptx::pack_bf16x2(a, c);
+        pbsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
       }
       l_run += psum;
+      lb_run += pbsum;
 
       // Past the end of the sequence the cache slots of the last page hold
       // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
@@ -475,7 +481,7 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
     ptx::tc_fence_after();
     const int ns = w.items[b * kItemWords + 1];
     const bool direct = (ns == 1);
-    const float inv_l = l_run > 0.f ? 1.0f / l_run : 0.f;
+    const float inv_l = lb_run > 0.f ? 1.0f / lb_run : 0.f;
     const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     const int sidx = (n_item == 0) ? w.split0 : 0;
     const int64_t slot = (int64_t)w.tile * w.stotal + w.items[b * kItemWords + 2] + sidx;
