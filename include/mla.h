@@ -122,6 +122,24 @@ int mla_decode_attend(const void* q, const void* kv_cache, int num_pages,
 int mla_decode_combine(int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* mla_decode for callers that cannot allocate device memory: the same
+ * arguments minus the workspace.  The paper has no counterpart; this entry
+ * point exists for host frameworks whose allocator owns all device memory
+ * (operators there may not call cudaMalloc) and for serving loops that must
+ * never enter the CUDA allocator.  The split partials go to a static device
+ * array inside the library, 38.1 MiB, enough for a plan on up to 76 two-CTA
+ * clusters (a 152-SM GB300); a device needing more returns
+ * MLA_ERR_WORKSPACE before anything is enqueued.  Every GPU that loads the
+ * library keeps that array until the process exits.  All calls share it and
+ * it keeps the last call's contents (nothing in it needs to start at zero),
+ * so calls that overlap on the GPU race: serialise them.  The first call on
+ * a device looks up the array's address with that device current; make it
+ * before any stream capture.  Allocates nothing. */
+int mla_decode_noalloc(const void* q, const void* kv_cache, int num_pages,
+                       const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                       int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
+                       float softmax_scale, void* stream);
+
 /* Synchronises `stream`, then returns and clears the device error word:
  * MLA_OK, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_PLAN
  * (or MLA_ERR_CUDA if the synchronisation itself failed). */

@@ -29,7 +29,8 @@ MLA_ERR_PLAN = -7
 
 EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_workspace_size", "mla_decode_plan", "mla_decode_plan_host", "mla_decode",
-            "mla_decode_attend", "mla_decode_combine", "mla_check_device_error", "mla_strerror"]
+            "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc",
+            "mla_check_device_error", "mla_strerror"]
 
 _lib = None
 
@@ -67,6 +68,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_decode_attend.restype = I
     lib.mla_decode_combine.argtypes = [I, I, I, V, V, V, V, Z, V]
     lib.mla_decode_combine.restype = I
+    lib.mla_decode_noalloc.argtypes = [V, V, I, V, I, V, I, I, I, V, V, V, F, V]
+    lib.mla_decode_noalloc.restype = I
     lib.mla_check_device_error.argtypes = [V]
     lib.mla_check_device_error.restype = I
     lib.mla_strerror.argtypes = [I]
@@ -182,6 +185,19 @@ def mla_decode_combine(batch: int, s_q: int, h_q: int, tile_meta, out, lse, work
                                    int(workspace.numel() * workspace.element_size()),
                                    _stream(stream))
     _check(rc, "mla_decode_combine")
+
+
+def mla_decode_noalloc(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
+                       softmax_scale: float, stream=None) -> None:
+    """mla_decode without a workspace argument, for callers that cannot
+    allocate device memory: the library's own static scratch holds the split
+    partials (shared by all calls, so calls must not overlap on the GPU)."""
+    B, s_q, h_q = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    rc = load().mla_decode_noalloc(_ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]),
+                                   _ptr(block_table), int(block_table.shape[1]),
+                                   _ptr(cache_seqlens), B, s_q, h_q, _ptr(tile_meta), _ptr(out),
+                                   _ptr(lse), float(softmax_scale), _stream(stream))
+    _check(rc, "mla_decode_noalloc")
 
 
 def mla_check_device_error(stream=None) -> int:
