@@ -21,7 +21,6 @@ __device__ int g_device_error;   // first device-side error of any launch, 0 if 
 constexpr int kMaxDevices = 64;
 constexpr int kPlanThreads = 1024;
 constexpr int kCombineWarps = 8;
-constexpr int kCombineRowsPerCta = kCombineWarps;
 
 // ------------------------------------------------------------------ planner
 // Exclusive prefix sum over the CTA; `total` receives the CTA-wide sum.
@@ -51,14 +50,21 @@ __device__ long long block_exclusive_scan(long long v, long long* warp_sums, lon
   return before + x - v;
 }
 
+// The unit prefix sums are searched many times (two binary searches per
+// cluster, two lookups per batch entry); they live in shared memory when they
+// fit (kPlanSmemBatch entries), in the plan buffer otherwise.
+constexpr int kPlanSmemBatch = 6000;
+
 __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* seqlens, int batch,
                                                                 int s_q, int h_q, int num_clusters,
                                                                 int32_t* plan, int* err) {
   __shared__ long long warp_sums[32];
+  extern __shared__ int64_t starts_smem[];
   const int tiles = plan_tiles(s_q, h_q);
   const int gt = plan_group_clusters(num_clusters, tiles);
-  int64_t* starts = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(plan) +
-                                               plan_off_starts(batch, gt));
+  int64_t* starts_g = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(plan) +
+                                                 plan_off_starts(batch, gt));
+  int64_t* starts = batch <= kPlanSmemBatch ? starts_smem : starts_g;
   int32_t* items = plan + plan_off_items(gt) / 4;
   int32_t* clus = plan + H_WORDS;
 
@@ -76,11 +82,15 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
     const long long ex = block_exclusive_scan(units_of(P), warp_sums, tot);
     if (b < batch) {
       starts[b] = run + ex;
+      starts_g[b] = run + ex;
       items[b * kItemWords + 0] = P;
     }
     run += tot;
   }
-  if (threadIdx.x == 0) starts[batch] = run;
+  if (threadIdx.x == 0) {
+    starts[batch] = run;
+    starts_g[batch] = run;
+  }
   __syncthreads();
   const long long V = run;
   const int g = plan_used_clusters(V, gt);
@@ -207,73 +217,87 @@ void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clus
 // Merges the split partials of every (batch entry, tile) that has two or
 // more splits:  lse = m + ln(sum_j exp(lse_j - m)),  out = sum_j
 // exp(lse_j - lse) * o_j.  Entries without pages get out = 0, lse = -inf.
-// One warp per query row; a lane owns 16 of the 512 output dims.
+// A CTA takes 32 rows x 128 output dims of one (entry, tile); partials are
+// stored [slot][dim/4][row][4], so a warp reads 32 consecutive rows of one
+// 4-dim group (512 contiguous bytes).  The bf16 block is staged in shared
+// memory and written back row by row.
+constexpr int kCombineRows = 32;
+constexpr int kCombineQuads = 32;    // 4-dim groups per CTA (128 dims)
+
 __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const DecodeParams p) {
+  __shared__ uint2 tile[kCombineRows][kCombineQuads + 1];
   const int32_t* plan = p.plan;
   const int tiles = plan[H_TILES], gt = plan[H_GT], stotal = plan[H_STOTAL];
   const int32_t* items = plan + plan_off_items(gt) / 4;
+  const int64_t max_slots = workspace_slots(plan[H_NCLUSTERS]);
   const int rows = p.s_q * p.h_q;
-  const int chunks = kTileRows / kCombineRowsPerCta;
+  const int row_blocks = kTileRows / kCombineRows, quad_blocks = (kDv / 4) / kCombineQuads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)p.batch * tiles * chunks;
+  const int64_t total = (int64_t)p.batch * tiles * row_blocks * quad_blocks;
   for (int64_t job = blockIdx.x; job < total; job += gridDim.x) {
-    const int chunk = (int)(job % chunks);
-    const int64_t item = job / chunks;
+    const int qb = (int)(job % quad_blocks);
+    const int rb = (int)((job / quad_blocks) % row_blocks);
+    const int64_t item = job / (quad_blocks * row_blocks);
     const int b = (int)(item % p.batch), t = (int)(item / p.batch);
     const int ns = items[b * kItemWords + 1];
-    if (ns == 1) continue;
-    const int r = chunk * kCombineRowsPerCta + warp;
-    const int qr = t * kTileRows + r;
-    if (qr >= rows) continue;
-    const int i = qr / p.h_q, h = qr - i * p.h_q;
-    __nv_bfloat16* orow =
-        static_cast<__nv_bfloat16*>(p.out) + (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv;
-    float* lse_out = p.lse + ((int64_t)b * p.h_q + h) * p.s_q + i;
+    if (ns == 1) continue;                                  // written by the main kernel
+    if (t * kTileRows + rb * kCombineRows >= rows) continue;  // padding rows only
     const int64_t slot0 = (int64_t)t * stotal + items[b * kItemWords + 2];
-    if (ns > 1 && (slot0 < 0 || slot0 + ns > workspace_slots(plan[H_NCLUSTERS]))) {
-      if (lane == 0) atomicCAS(p.err, 0, MLA_ERR_PLAN);
+    if (ns > 1 && (slot0 < 0 || slot0 + ns > max_slots)) {
+      if (threadIdx.x == 0) atomicCAS(p.err, 0, MLA_ERR_PLAN);
       continue;
     }
-
+    const int r = rb * kCombineRows + lane;                  // tile row of this lane
+    const int qr = t * kTileRows + r;
+    // merge weights of this row
     float m = -INFINITY;
-    if (ns > 1)
-      for (int j = lane; j < ns; j += 32) m = fmaxf(m, p.ws_lse[(slot0 + j) * kTileRows + r]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float acc[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-    float lse = -INFINITY;
+    for (int j = 0; j < ns; ++j) m = fmaxf(m, p.ws_lse[(slot0 + j) * kTileRows + r]);
+    float lse = -INFINITY, se = 0.f;
     if (m != -INFINITY) {
-      float se = 0.f;
-      for (int j = lane; j < ns; j += 32) se += expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+      for (int j = 0; j < ns; ++j) se += expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m);
       lse = m + logf(se);
-      for (int j = 0; j < ns; ++j) {
-        const float wgt = expf(p.ws_lse[(slot0 + j) * kTileRows + r] - lse);
-        const float4* o4 =
-            reinterpret_cast<const float4*>(p.ws_o + ((slot0 + j) * kTileRows + r) * kDv);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 v = o4[lane + 32 * q];
-          acc[4 * q + 0] += wgt * v.x;
-          acc[4 * q + 1] += wgt * v.y;
-          acc[4 * q + 2] += wgt * v.z;
-          acc[4 * q + 3] += wgt * v.w;
+    }
+    for (int k = 0; k < kCombineQuads / kCombineWarps; ++k) {
+      const int ql = warp + kCombineWarps * k;
+      const int q = qb * kCombineQuads + ql;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (m != -INFINITY) {
+        for (int j = 0; j < ns; ++j) {
+          const float wgt = expf(p.ws_lse[(slot0 + j) * kTileRows + r] - lse);
+          const float4 v = reinterpret_cast<const float4*>(
+              p.ws_o)[((slot0 + j) * (kDv / 4) + q) * kTileRows + r];
+          acc.x += wgt * v.x;
+          acc.y += wgt * v.y;
+          acc.z += wgt * v.z;
+          acc.w += wgt * v.w;
         }
       }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc[4 * q + 0], acc[4 * q + 1]);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc[4 * q + 2], acc[4 * q + 3]);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
       uint2 u;
       memcpy(&u.x, &lo, 4);
       memcpy(&u.y, &hi, 4);
-      *reinterpret_cast<uint2*>(orow + 4 * (lane + 32 * q)) = u;
+      tile[lane][ql] = u;
     }
-    if (lane == 0) *lse_out = lse;
+    if (qb == 0 && warp == 0 && qr < rows) {
+      const int i = qr / p.h_q, h = qr - i * p.h_q;
+      p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
+    }
+    __syncthreads();
+    // write back: 8 threads per row, 32 contiguous bytes each
+    for (int e = threadIdx.x; e < kCombineRows * 8; e += blockDim.x) {
+      const int rl = e >> 3, part = e & 7;
+      const int qr2 = t * kTileRows + rb * kCombineRows + rl;
+      if (qr2 < rows) {
+        const int i = qr2 / p.h_q, h = qr2 - i * p.h_q;
+        uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) +
+                                              (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv +
+                                              (qb * kCombineQuads + part * 4) * 4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) dst[k] = tile[rl][part * 4 + k];
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -413,7 +437,8 @@ int mla_decode_plan(const int32_t* cache_seqlens, int batch, int s_q, int h_q, v
   const size_t need = mla_plan_size_for_clusters(batch, s_q, h_q, d.num_clusters);
   if (need == 0) return MLA_ERR_INVALID_ARG;
   if (tile_meta_bytes < need) return MLA_ERR_WORKSPACE;
-  mla_plan_kernel<<<1, kPlanThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+  const size_t smem = batch <= kPlanSmemBatch ? sizeof(int64_t) * (size_t)(batch + 1) : 0;
+  mla_plan_kernel<<<1, kPlanThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       cache_seqlens, batch, s_q, h_q, d.num_clusters, static_cast<int32_t*>(tile_meta), d.err);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -445,6 +470,7 @@ int prepare_decode(const void* q, const void* kv_cache, int num_pages, const int
   const int64_t need = workspace_bytes_for(d.num_clusters);
   if (!workspace || (int64_t)workspace_bytes < need) return MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
+  p->q = q;
   p->block_table = block_table;
   p->seqlens = cache_seqlens;
   p->plan = static_cast<const int32_t*>(tile_meta);
@@ -470,8 +496,7 @@ int attend(const void* q, const void* kv_cache, const DecodeParams& p, int num_c
   TensorMaps maps;
   const uint64_t q_rows = (uint64_t)p.batch * p.s_q * p.h_q;
   const uint64_t kv_rows = (uint64_t)p.num_pages * kPageTokens;
-  if (!make_map(&maps.q_lat, q, q_rows, 64, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map(&maps.q_rope, q, q_rows, 32, kTileRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_map(&maps.q_rope, q, q_rows, 32, kTileRows, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_map(&maps.kv_lat, kv_cache, kv_rows, 64, kPageTokens, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map(&maps.kv_rope, kv_cache, kv_rows, 32, kPageTokens, CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
@@ -578,7 +603,8 @@ namespace mla {
 cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_sms,
                            cudaStream_t stream) {
   const int tiles = plan_tiles(p.s_q, p.h_q);
-  const int64_t jobs = (int64_t)p.batch * tiles * (kTileRows / kCombineRowsPerCta);
+  const int64_t jobs = (int64_t)p.batch * tiles * (kTileRows / kCombineRows) *
+                       ((kDv / 4) / kCombineQuads);
   const int64_t cap = (int64_t)num_sms * 8;
   const int grid = (int)(jobs < cap ? jobs : cap);
   mla_combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(p);

@@ -23,26 +23,33 @@
 //    rotary dims ([512 + 32 r, 512 + 32 r + 32)).  Each CTA therefore loads
 //    exactly 36 KB of every 72 KB page: the pair reads each page once, with
 //    no duplicated tensor work.  The two 128 x 64 fp32 partial score tiles
-//    are exchanged over distributed shared memory (st.async with mbarrier
-//    transaction counts) and summed; both CTAs then run the same softmax on
-//    bit-identical scores, so their running maxima agree exactly.
+//    are exchanged through distributed shared memory and summed; both CTAs
+//    then run the same softmax on bit-identical scores, so their running
+//    maxima agree exactly.
+//  * Dedicated exchange warps ship each page's partial scores as soon as the
+//    score MMA has written them, into a double-buffered receive buffer, so
+//    the cross-SM transfer of page g+1 overlaps the softmax of page g.
 //  * Warp roles: warps 0-3 softmax + epilogue (one thread per TMEM lane =
-//    query row), warp 4 TMA producer, warp 5 MMA issuer and TMEM owner.
-//  * S = Q K^T: M=128, N=64, 18 K-steps (16 latent + 2 rotary) into a double
-//    buffered TMEM score tile; O += P V: M=128, N=256, K=64 with V read from
-//    the same shared-memory page as K (as an MN-major operand).
+//    query row), warps 4-7 score exchange (and the per-tile load of Q's
+//    latent half into TMEM), warp 8 TMA producer, warp 9 MMA issuer and TMEM
+//    owner.  The MMA issuer polls its barriers and issues whichever MMA is
+//    ready, so a page still in flight from HBM never holds back the P.V of an
+//    earlier one.
+//  * S = Q K^T: M=128, N=64, 18 K-steps (16 latent with Q read from TMEM, 2
+//    rotary from shared memory) into a double buffered TMEM score tile;
+//    O += P V: M=128, N=256, K=64 with P from shared memory and V from the
+//    same shared-memory page as K (as an MN-major operand).
 //  * Online softmax in the log2 domain with a lazy rescale: O is rescaled only
 //    when the row max grows by more than 2^8; the final 1/l and lse use the
 //    same (possibly stale) max, so the result is exact.
-//  * Every mbarrier wait is bounded (globaltimer); on expiry the kernel
-//    records MLA_ERR_DEVICE_TIMEOUT, tells the peer CTA, lets in-flight copies
-//    land, frees TMEM and returns.  No trap, no unbounded spin.
+//  * Every wait is bounded (globaltimer); on expiry the kernel records
+//    MLA_ERR_DEVICE_TIMEOUT, tells the peer CTA, lets in-flight copies land,
+//    frees TMEM and returns.  No trap, no unbounded spin.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
-#include <stdlib.h>
 
 #include "mla.h"
 #include "mla_internal.h"
@@ -51,10 +58,13 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 192;
+// Warp roles: 0-3 softmax, 4-7 score exchange, 8 TMA producer, 9 MMA
+// issuer.  Warp w reaches TMEM lanes [32 (w % 4), 32 (w % 4) + 32).
+constexpr int kThreads = 320;
 constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kExchangeWarp0 = 4;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after an abort
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
@@ -64,45 +74,47 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;     // [0, 256): this CTA's half of O
 constexpr uint32_t kColS = 256;   // two 64-column score tiles
-constexpr uint32_t kColP = 384;   // two 32-column bf16x2 probability tiles
+constexpr uint32_t kColQ = 384;   // Q's latent half, bf16x2: 128 rows x 256 dims
+
+// Shared memory (offsets from a 1024-byte aligned base).
+constexpr int kStages = 3;
+constexpr uint32_t kQRope = 0;            // [128 x 32] bf16, 64-byte swizzle
+constexpr uint32_t kStage0 = 8192;        // kStages x 36 KB
+constexpr uint32_t kStageBytes = 36864;
+constexpr uint32_t kStageRope = 32768;    // rotary box inside a stage
+constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][128 rows] x 16 B
+constexpr uint32_t kRecvBytes = 128 * 64 * 4;
+constexpr uint32_t kP = kRecv + 2 * kRecvBytes;               // [128 x 64] bf16, 128-byte swizzle
+constexpr uint32_t kPBytes = 128 * 64 * 2;
+constexpr uint32_t kXStage = kP + kPBytes;                     // [8 chunks][128 rows] x 16 B
+constexpr uint32_t kXStageBytes = kRecvBytes / 2;
+constexpr uint32_t kBar = kXStage + kXStageBytes;
+constexpr uint32_t kMisc = kBar + 8 * 32;
+constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
+static_assert(kP % 1024 == 0 && kStage0 % 1024 == 0, "swizzled buffers need 1 KB alignment");
 
 // Bytes moved per stage / per Q tile by one CTA.
 constexpr uint32_t kStageTx = 4 * 8192 + 4096;   // 4 latent boxes + rotary half
-constexpr uint32_t kQTx = 4 * 16384 + 8192;
-constexpr uint32_t kRecvTx = 128 * 64 * 4;
-
-template <bool P_TMEM>
-struct Cfg {
-  static constexpr int kStages = P_TMEM ? 3 : 2;
-  static constexpr int kPBufs = P_TMEM ? 2 : 1;
-  static constexpr uint32_t kQLat = 0;                 // 4 x [128 x 64] bf16, 128B swizzle
-  static constexpr uint32_t kQRope = 65536;            // [128 x 32] bf16, 64B swizzle
-  static constexpr uint32_t kStage0 = 73728;           // kStages x 36 KB
-  static constexpr uint32_t kStageBytes = 36864;
-  static constexpr uint32_t kStageRope = 32768;        // rotary box inside a stage
-  static constexpr uint32_t kP = kStage0 + kStages * kStageBytes;  // smem P (if used)
-  static constexpr uint32_t kRecv = kP + (P_TMEM ? 0u : 16384u);   // [128 x 64] fp32
-  static constexpr uint32_t kBar = kRecv + kRecvTx;
-  static constexpr uint32_t kMisc = kBar + 8 * 32;
-  static constexpr uint32_t kBytes = kMisc + 64;
-  static constexpr uint32_t kAlloc = kBytes + 1024;    // slack for 1024-byte alignment
-};
+constexpr uint32_t kQRopeTx = 8192;
 
 enum Bar : uint32_t {
-  B_FULL = 0,      // [3] stage loaded (TMA tx)
-  B_EMPTY = 3,     // [3] stage consumed (MMA commit)
-  B_QFULL = 6,
-  B_QEMPTY = 7,
-  B_SFULL = 8,     // [2]
-  B_SEMPTY = 10,   // [2]
-  B_PFULL = 12,    // [2]
-  B_PEMPTY = 14,   // [2]
-  B_OFULL = 16,
-  B_OEMPTY = 17,
-  B_RFULL = 18,    // peer's partial scores arrived (st.async tx)
-  B_REMPTY = 19,   // peer consumed what this CTA sent
-  B_TEARDOWN = 20,
+  B_FULL = 0,      // [kStages] stage loaded (TMA tx)
+  B_EMPTY = 4,     // [kStages] stage consumed (MMA commit)
+  B_QFULL = 8,     // Q tile ready: rotary half (TMA) + latent half (exchange warps)
+  B_QEMPTY = 9,    // last score MMA of a tile done
+  B_SFULL = 10,    // [2] score tile ready (MMA commit)
+  B_SEMPTY = 12,   // [2] score tile read (softmax + exchange warps)
+  B_PFULL = 14,    // probabilities written (softmax warps)
+  B_PEMPTY = 16,   // P.V done (MMA commit)
+  B_OFULL = 18,
+  B_OEMPTY = 19,
+  B_RFULL = 20,    // [2] the peer's partial scores are in receive buffer i (bulk-copy tx)
+  B_REMPTY = 22,   // [2] the peer has read receive buffer i of this CTA's sends
+  B_TEARDOWN = 24,
+  B_XREADY = 25,   // the exchange staging buffer is written (4 exchange warps)
+  B_XFREE = 26,    // the bulk copy has finished reading the staging buffer
 };
+static_assert(kStages <= 4, "barrier slots");
 
 struct Ctx {
   uint32_t sbase;       // 1024-aligned shared base
@@ -110,8 +122,7 @@ struct Ctx {
   uint32_t rank, peer;
   uint32_t abort_addr, peer_abort_addr;
   int* err;
-  __device__ __forceinline__ uint32_t bar(uint32_t i) const { return sbase + kBarOff + 8u * i; }
-  uint32_t kBarOff;
+  __device__ __forceinline__ uint32_t bar(uint32_t i) const { return sbase + kBar + 8u * i; }
 };
 
 __device__ __forceinline__ void abort_all(const Ctx& x) {
@@ -175,6 +186,29 @@ struct Work {
   const int32_t* items;
 };
 
+// Page-by-page walk of the cluster's work, with the segment (item) index.
+struct Cursor {
+  SegIter it;
+  int b, pb, pe, pg;
+  uint32_t item;
+  bool valid;
+  __device__ __forceinline__ void init(const Work& w) {
+    it = SegIter{w.b0, w.p0, w.b1, w.p1, w.items};
+    item = 0;
+    valid = it.next(b, pb, pe);
+    pg = pb;
+  }
+  __device__ __forceinline__ void advance() {
+    if (++pg >= pe) {
+      valid = it.next(b, pb, pe);
+      pg = pb;
+      ++item;
+    }
+  }
+  __device__ __forceinline__ bool first() const { return pg == pb; }
+  __device__ __forceinline__ bool last() const { return pg == pe - 1; }
+};
+
 // 32 consecutive TMEM columns of this warp's 32 lanes, loaded and waited on
 // in one statement so no use of the registers can be scheduled before the
 // wait.
@@ -194,35 +228,28 @@ __device__ __forceinline__ void tmem_load32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 
 // ------------------------------------------------------------------ producer
-template <bool P_TMEM>
 __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const DecodeParams& prm,
-                                             const CUtensorMap* tm_q_lat,
                                              const CUtensorMap* tm_q_rope,
                                              const CUtensorMap* tm_kv_lat,
                                              const CUtensorMap* tm_kv_rope) {
-  using C = Cfg<P_TMEM>;
   const uint64_t policy = ptx::policy_evict_first();
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
   const int32_t xq_lat = 256 * (int32_t)x.rank, xq_rope = 512 + 32 * (int32_t)x.rank;
   while (it.next(b, pb, pe)) {
-    if (!wait_bar(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
-    ptx::mbar_arrive_expect_tx(x.bar(B_QFULL), kQTx);
-    const int32_t row0 = b * w.rows + w.tile * kTileRows;
-    for (int ch = 0; ch < 4; ++ch)
-      ptx::tma_load_2d(x.sbase + C::kQLat + ch * 16384, tm_q_lat, xq_lat + 64 * ch, row0,
-                       x.bar(B_QFULL));
-    ptx::tma_load_2d(x.sbase + C::kQRope, tm_q_rope, xq_rope, row0, x.bar(B_QFULL));
-
     // Entries past max_pages are never read: a sequence longer than its
     // block-table row is reported and served from page 0.
     const int32_t* bt = prm.block_table + (size_t)b * prm.max_pages;
     int next_page = pb < prm.max_pages ? bt[pb] : -1;
+    if (!wait_bar(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
+    ptx::mbar_arrive_expect_tx(x.bar(B_QFULL), kQRopeTx);
+    const int32_t row0 = b * w.rows + w.tile * kTileRows;
+    ptx::tma_load_2d(x.sbase + kQRope, tm_q_rope, xq_rope, row0, x.bar(B_QFULL));
     for (int pg = pb; pg < pe; ++pg, ++g) {
       int page = next_page;
       if (pg + 1 < pe) next_page = pg + 1 < prm.max_pages ? bt[pg + 1] : -1;
-      const uint32_t s = g % C::kStages, k = g / C::kStages;
+      const uint32_t s = g % kStages, k = g / kStages;
       if (!wait_bar(x, x.bar(B_EMPTY + s), (k & 1u) ^ 1u)) return false;
       if ((unsigned)page >= (unsigned)prm.num_pages) {
         atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
@@ -230,11 +257,11 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
       }
       ptx::mbar_arrive_expect_tx(x.bar(B_FULL + s), kStageTx);
       const int32_t y = page * kPageTokens;
-      const uint32_t st = x.sbase + C::kStage0 + s * C::kStageBytes;
+      const uint32_t st = x.sbase + kStage0 + s * kStageBytes;
       for (int ch = 0; ch < 4; ++ch)
         ptx::tma_load_2d_hint(st + ch * 8192, tm_kv_lat, xq_lat + 64 * ch, y, x.bar(B_FULL + s),
                               policy);
-      ptx::tma_load_2d_hint(st + C::kStageRope, tm_kv_rope, xq_rope, y, x.bar(B_FULL + s), policy);
+      ptx::tma_load_2d_hint(st + kStageRope, tm_kv_rope, xq_rope, y, x.bar(B_FULL + s), policy);
     }
     ++n_item;
   }
@@ -242,101 +269,213 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <bool P_TMEM>
-__device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
-  using C = Cfg<P_TMEM>;
+// Issues S = Q K^T for page gq and O += P V for page gp (gp < gq), each as
+// soon as its inputs are ready, in page order within each kind.
+__device__ __forceinline__ void issue_qk(const Ctx& x, uint32_t g) {
   constexpr uint32_t id_qk = ptx::idesc_bf16_f32(128, 64, 0, 0);
+  const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
+  const uint32_t d_s = x.tmem + kColS + (g & 1u) * 64;
+  // latent dims: A = Q from TMEM (8 columns = 16 dims per K-step), B = K page
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint64_t bdesc =
+        ptx::smem_desc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024, ptx::kLayoutSw128);
+    ptx::mma_ts(d_s, x.tmem + kColQ + k * 8, bdesc, id_qk, k ? 1u : 0u);
+  }
+  // rotary dims: both operands from shared memory
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint64_t adesc = ptx::smem_desc(x.sbase + kQRope + k * 32, 16, 512, ptx::kLayoutSw64);
+    const uint64_t bdesc = ptx::smem_desc(st + kStageRope + k * 32, 16, 512, ptx::kLayoutSw64);
+    ptx::mma_ss(d_s, adesc, bdesc, id_qk, 1u);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(const Ctx& x, uint32_t g, bool first) {
   constexpr uint32_t id_pv = ptx::idesc_bf16_f32(128, 256, 0, 1);
+  const uint32_t vbase = x.sbase + kStage0 + (g % kStages) * kStageBytes;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    // V as the MN-major B operand: 64-dim swizzle atoms 8 KB apart along N,
+    // 8-token row groups 1 KB apart along K; 16 tokens per K-step.
+    const uint64_t bdesc = ptx::smem_desc(vbase + k * 2048, 8192, 1024, ptx::kLayoutSw128);
+    const uint64_t adesc = ptx::smem_desc(x.sbase + kP + k * 32, 16, 1024, ptx::kLayoutSw128);
+    ptx::mma_ss(x.tmem + kColO, adesc, bdesc, id_pv, (first && k == 0) ? 0u : 1u);
+  }
+}
+
+__device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
+  Cursor cq, cp;
+  cq.init(w);
+  cp.init(w);
+  uint32_t gq = 0, gp = 0;
+  int q_ok_item = -1, o_ok_item = -1;
+  uint64_t idle_t0 = 0;
+  uint32_t idle = 0;
+  while (cp.valid) {
+    bool progress = false;
+    // P.V of the oldest page whose probabilities are ready.
+    if (gp < gq) {
+      bool ok = true;
+      if (cp.first() && (int)cp.item != o_ok_item) {
+        if (ptx::mbar_test_wait(x.bar(B_OEMPTY), (cp.item & 1u) ^ 1u))
+          o_ok_item = (int)cp.item;
+        else
+          ok = false;
+      }
+      if (ok) ok = ptx::mbar_test_wait(x.bar(B_PFULL), gp & 1u);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_pv(x, gp, cp.first());
+        ptx::mma_commit(x.bar(B_EMPTY + gp % kStages));
+        ptx::mma_commit(x.bar(B_PEMPTY));
+        if (cp.last()) ptx::mma_commit(x.bar(B_OFULL));
+        cp.advance();
+        ++gp;
+        progress = true;
+      }
+    }
+    // Scores of the next page once it is loaded and its TMEM tile is free.
+    if (cq.valid) {
+      bool ok = true;
+      if ((int)cq.item != q_ok_item) {
+        if (ptx::mbar_test_wait(x.bar(B_QFULL), cq.item & 1u))
+          q_ok_item = (int)cq.item;
+        else
+          ok = false;
+      }
+      if (ok) ok = ptx::mbar_test_wait(x.bar(B_FULL + gq % kStages), (gq / kStages) & 1u);
+      if (ok) ok = ptx::mbar_test_wait(x.bar(B_SEMPTY + (gq & 1u)), ((gq >> 1) & 1u) ^ 1u);
+      if (ok) {
+        ptx::tc_fence_after();
+        issue_qk(x, gq);
+        ptx::mma_commit(x.bar(B_SFULL + (gq & 1u)));
+        if (cq.last()) ptx::mma_commit(x.bar(B_QEMPTY));
+        cq.advance();
+        ++gq;
+        progress = true;
+      }
+    }
+    if (progress) {
+      idle = 0;
+      continue;
+    }
+    // Nothing ready: back off briefly (this warp shares a scheduler with a
+    // softmax warp) and keep the wait bounded.
+    __nanosleep(20);
+    if ((++idle & 63u) == 0u) {
+      if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) return false;
+      const uint64_t now = ptx::globaltimer();
+      if (idle == 64u) idle_t0 = now;
+      if (now - idle_t0 > kWaitTimeoutNs) {
+        abort_all(x);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ score exchange
+// Warps 4-7 (a) put the latent half of each Q tile into TMEM, one row per
+// thread, and (b) ship this CTA's partial scores of every page to the peer
+// CTA as soon as the score MMA has written them, into receive buffer g % 2,
+// so the transfer overlaps the softmax of the previous page.  Receive buffer
+// layout [16-byte chunk c][row r].  The partial scores are staged in local
+// shared memory and moved by the TMA engine (bulk copy shared::cta ->
+// shared::cluster), which completes the bytes on the peer's barrier; the
+// receiving side posts the expected byte count itself.
+__device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const DecodeParams& prm,
+                                             int e, int lane) {
+  const int r = e * 32 + lane;
+  const uint32_t lane_base = (uint32_t)(e * 32) << 16;
+  const uint32_t peer_recv = ptx::map_to_rank(x.sbase + kRecv, x.peer);
+  const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
-  bool have_prev = false, prev_first = false, prev_last = false;
-  uint32_t prev_g = 0, prev_item = 0;
-
-  auto issue_pv = [&]() -> bool {
-    const uint32_t s = prev_g % C::kStages;
-    if (prev_first && !wait_bar(x, x.bar(B_OEMPTY), (prev_item & 1u) ^ 1u)) return false;
-    const uint32_t pbuf = prev_g % C::kPBufs, pk = prev_g / C::kPBufs;
-    if (!wait_bar(x, x.bar(B_PFULL + pbuf), pk & 1u)) return false;
-    ptx::tc_fence_after();
-    const uint32_t vbase = x.sbase + C::kStage0 + s * C::kStageBytes;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      // V as the MN-major B operand: 64-dim swizzle atoms 8 KB apart along N,
-      // 8-token row groups 1 KB apart along K; 16 tokens per K-step.
-      const uint64_t bdesc = ptx::smem_desc(vbase + k * 2048, 8192, 1024, ptx::kLayoutSw128);
-      const uint32_t acc = (prev_first && k == 0) ? 0u : 1u;
-      if constexpr (P_TMEM) {
-        ptx::mma_ts(x.tmem + kColO, x.tmem + kColP + pbuf * 32 + k * 8, bdesc, id_pv, acc);
-      } else {
-        const uint64_t adesc =
-            ptx::smem_desc(x.sbase + C::kP + k * 32, 16, 1024, ptx::kLayoutSw128);
-        ptx::mma_ss(x.tmem + kColO, adesc, bdesc, id_pv, acc);
-      }
-    }
-    ptx::mma_commit(x.bar(B_EMPTY + s));
-    ptx::mma_commit(x.bar(B_PEMPTY + pbuf));
-    if (prev_last) ptx::mma_commit(x.bar(B_OFULL));
-    return true;
-  };
-
   while (it.next(b, pb, pe)) {
-    if (!wait_bar(x, x.bar(B_QFULL), n_item & 1u)) return false;
-    ptx::tc_fence_after();
+    // Q latent half of this tile -> TMEM columns [kColQ, kColQ + 128) once the
+    // previous tile's last score MMA is done.  Rows past the batch entry's
+    // query rows are zero.
+    if (!wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
+    const int qr = w.tile * kTileRows + r;
+    const bool valid = qr < w.rows;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        q + ((int64_t)b * w.rows + (valid ? qr : 0)) * kDqk + 256 * (int)x.rank);
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+      uint32_t v[32];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 u = valid ? src[ch * 8 + j] : make_uint4(0u, 0u, 0u, 0u);
+        v[4 * j] = u.x;
+        v[4 * j + 1] = u.y;
+        v[4 * j + 2] = u.z;
+        v[4 * j + 3] = u.w;
+      }
+      ptx::tmem_st32(x.tmem + lane_base + kColQ + ch * 32, v);
+    }
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(x.bar(B_QFULL));
+
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      const uint32_t s = g % C::kStages;
-      if (!wait_bar(x, x.bar(B_FULL + s), (g / C::kStages) & 1u)) return false;
       const uint32_t sb = g & 1u;
-      if (!wait_bar(x, x.bar(B_SEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
+      if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
       ptx::tc_fence_after();
-      const uint32_t st = x.sbase + C::kStage0 + s * C::kStageBytes;
-      const uint32_t d_s = x.tmem + kColS + sb * 64;
+      // the peer has read what was sent into this buffer two pages ago
+      if (!wait_warp(x, x.bar(B_REMPTY + sb), ((g >> 1) & 1u) ^ 1u, true)) return false;
+      // Two 16 KB halves: stage columns [32 h, 32 h + 32) of every row, then
+      // one thread hands the block to the TMA engine for the cross-SM copy.
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t use = 2u * g + (uint32_t)half;
+        if (!wait_warp(x, x.bar(B_XFREE), (use & 1u) ^ 1u)) return false;
+        uint32_t v[32];
+        tmem_load32(x.tmem + lane_base + kColS + sb * 64 + half * 32, v);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t adesc =
-              ptx::smem_desc(x.sbase + C::kQLat + ch * 16384 + k * 32, 16, 1024, ptx::kLayoutSw128);
-          const uint64_t bdesc =
-              ptx::smem_desc(st + ch * 8192 + k * 32, 16, 1024, ptx::kLayoutSw128);
-          ptx::mma_ss(d_s, adesc, bdesc, id_qk, (ch | k) ? 1u : 0u);
+        for (int c = 0; c < 8; ++c)
+          ptx::st_shared_v4(x.sbase + kXStage + (uint32_t)c * 2048u + (uint32_t)r * 16u, v[4 * c],
+                            v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(x.bar(B_XREADY));
+        bool ok = true;
+        if (e == 0 && lane == 0) {
+          ok = wait_bar(x, x.bar(B_XREADY), use & 1u);
+          if (ok) {
+            ptx::bulk_copy_to_peer(peer_recv + sb * kRecvBytes + (uint32_t)half * kXStageBytes,
+                                   x.sbase + kXStage, kXStageBytes, peer_rfull + 8u * sb);
+            ptx::bulk_commit();
+            ptx::bulk_wait_read_all();
+            ptx::mbar_arrive(x.bar(B_XFREE));
+          }
         }
+        if (!__all_sync(0xffffffffu, ok)) return false;
       }
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint64_t adesc =
-            ptx::smem_desc(x.sbase + C::kQRope + k * 32, 16, 512, ptx::kLayoutSw64);
-        const uint64_t bdesc =
-            ptx::smem_desc(st + C::kStageRope + k * 32, 16, 512, ptx::kLayoutSw64);
-        ptx::mma_ss(d_s, adesc, bdesc, id_qk, 1u);
-      }
-      ptx::mma_commit(x.bar(B_SFULL + sb));
-      if (pg == pe - 1) ptx::mma_commit(x.bar(B_QEMPTY));
-      if (have_prev && !issue_pv()) return false;
-      have_prev = true;
-      prev_g = g;
-      prev_first = (pg == pb);
-      prev_last = (pg == pe - 1);
-      prev_item = n_item;
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
     }
     ++n_item;
   }
-  if (have_prev && !issue_pv()) return false;
   return true;
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
-template <bool P_TMEM>
 __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const DecodeParams& prm,
                                             int warp, int lane) {
-  using C = Cfg<P_TMEM>;
   const int r = warp * 32 + lane;                   // tile row == TMEM lane
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t recv_row = x.sbase + C::kRecv + (uint32_t)r * 256u;
-  const uint32_t peer_recv_row = ptx::map_to_rank(recv_row, x.peer);
-  const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
+  // Receive buffer layout [16-byte chunk c][row r]: chunk c of row r at
+  // (c * 128 + r) * 16, so one warp's store (or load) of a chunk covers 512
+  // contiguous bytes.
+  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)r * 16u;
   const uint32_t peer_rempty = ptx::map_to_rank(x.bar(B_REMPTY), x.peer);
-  const uint32_t swz = (uint32_t)(r & 15);
+  const uint32_t pswz = (uint32_t)(r & 7);
   const float scale_log2 = prm.scale_log2;
 
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
@@ -358,7 +497,12 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const bool first = (pg == pb);
       const uint32_t sb = g & 1u;
+
+      // 1. Full scores of page g: own partial (TMEM, once this CTA's score MMA
+      //    is done) + the peer's (received).
+      if (r == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + sb), kRecvBytes);
       if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
+      if (!wait_warp(x, x.bar(B_RFULL + sb), (g >> 1) & 1u, true)) return false;
       ptx::tc_fence_after();
       float s[64];
       {
@@ -370,52 +514,40 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
 #pragma unroll
         for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(v[k]);
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
-
-      // Exchange partial scores with the peer CTA: send mine into its receive
-      // buffer, take its partial from mine.  16-byte chunks are XOR-swizzled
-      // by row to spread the rows over the shared-memory banks.
-      if (!wait_warp(x, x.bar(B_REMPTY), (g & 1u) ^ 1u, true)) return false;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        ptx::st_async_v4(peer_recv_row + (((uint32_t)c ^ swz) << 4), s[4 * c], s[4 * c + 1],
-                         s[4 * c + 2], s[4 * c + 3], peer_rfull);
-      if (r == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL), kRecvTx);
-      if (!wait_warp(x, x.bar(B_RFULL), g & 1u, true)) return false;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        const float4 v = ptx::ld_shared_v4f(recv_row + (((uint32_t)c ^ swz) << 4));
+        const float4 v = ptx::ld_shared_v4f(recv_row + sb * kRecvBytes + (uint32_t)c * 2048u);
         s[4 * c] += v.x;   // addition commutes: both CTAs get identical sums
         s[4 * c + 1] += v.y;
         s[4 * c + 2] += v.z;
         s[4 * c + 3] += v.w;
       }
+      ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(peer_rempty);
-
-      // Mask, scale into log2 units, row max (the accum_s -> scores_max reduce).
-      const int tok0 = pg * kPageTokens;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        s[k] = (tok0 + k < n_valid) ? s[k] * scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[k]);
+      if (lane == 0) {
+        ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+        ptx::mbar_arrive_cluster(peer_rempty + 8u * sb);
       }
-      const float m_new = fmaxf(m_run, mx);
+
+      // 2. Mask, row max (the accum_s -> scores_max reduce), exp2, sums.
+      const int tok0 = pg * kPageTokens;
+      if (__any_sync(0xffffffffu, tok0 + kPageTokens > n_valid)) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (tok0 + k >= n_valid) s[k] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
+      const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
       const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
 
-      const uint32_t pbuf = g % C::kPBufs;
-      if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / C::kPBufs) & 1u) ^ 1u)) return false;
+      // The previous page's P.V must be done: it frees the probability tile
+      // and leaves O holding every page before this one.
+      if (!wait_warp(x, x.bar(B_PEMPTY), (g & 1u) ^ 1u)) return false;
       if (__any_sync(0xffffffffu, rescale)) {
-        if (C::kPBufs == 2) {
-          // O must hold every page before this one: wait for the previous P.V.
-          const uint32_t gp = g - 1;
-          if (!wait_warp(x, x.bar(B_PEMPTY + (gp & 1u)), (gp >> 1) & 1u)) return false;
-        }
         ptx::tc_fence_after();
-        const float alpha = rescale ? exp2f(m_run - m_new) : 1.0f;
+        const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
 #pragma unroll 1
         for (int ch = 0; ch < 8; ++ch) {
           uint32_t v[32];
@@ -433,13 +565,13 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
         }
       }
       if (first) m_run = m_new;
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
       uint32_t pk[32];
       float psum = 0.f, pbsum = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float a = exp2f(s[2 * j] - m_use);
-        const float c = exp2f(s[2 * j + 1] - m_use);
+        const float a = ptx::ex2(fmaf(s[2 * j], scale_log2, neg_m));
+        const float c = ptx::ex2(fmaf(s[2 * j + 1], scale_log2, neg_m));
         psum += a + c;
         pk[j] = ptx::pack_bf16x2(a, c);
         pbsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
@@ -452,19 +584,17 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
       // the P.V MMA, so zero those value rows first.
       if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
         const int t0 = L & (kPageTokens - 1);
-        const uint32_t st = x.sbase + C::kStage0 + (g % C::kStages) * C::kStageBytes;
+        const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
         const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
         for (int idx = r; idx < n16; idx += kSoftmaxWarps * 32) {
           const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
           ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
         }
+        ptx::fence_proxy_async_smem();
       }
-      if constexpr (P_TMEM) {
-        ptx::tmem_st32(x.tmem + lane_base + kColP + pbuf * 32, pk);
-        ptx::tmem_wait_st();
-      } else {
-        const uint32_t prow = x.sbase + C::kP + (uint32_t)r * 128u;
-        const uint32_t pswz = (uint32_t)(r & 7);
+      {
+        // P row r, 128-byte swizzle: 16-byte chunk c at position c ^ (r % 8)
+        const uint32_t prow = x.sbase + kP + (uint32_t)r * 128u;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
@@ -473,10 +603,11 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL));
     }
 
-    // Epilogue: O / l, lse = (m + log2 l) * ln 2.
+    // Epilogue: O / l, lse = (m + log2 l) * ln 2.  Split partials go out in a
+    // [slot][dim/4][row][4] layout so a warp's stores are contiguous.
     if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
     ptx::tc_fence_after();
     const int ns = w.items[b * kItemWords + 1];
@@ -509,13 +640,15 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
             dst[q] = u;
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(prm.ws_o + (slot * kTileRows + r) * kDv + d0);
+          float4* base =
+              reinterpret_cast<float4*>(prm.ws_o) + slot * (kDv / 4) * kTileRows + r;
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv_l,
-                                 __uint_as_float(v[4 * q + 1]) * inv_l,
-                                 __uint_as_float(v[4 * q + 2]) * inv_l,
-                                 __uint_as_float(v[4 * q + 3]) * inv_l);
+            base[(int64_t)(d0 / 4 + q) * kTileRows] =
+                make_float4(__uint_as_float(v[4 * q]) * inv_l,
+                            __uint_as_float(v[4 * q + 1]) * inv_l,
+                            __uint_as_float(v[4 * q + 2]) * inv_l,
+                            __uint_as_float(v[4 * q + 3]) * inv_l);
         }
       }
     }
@@ -533,13 +666,10 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
   return true;
 }
 
-template <bool P_TMEM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_lat,
-                      const __grid_constant__ CUtensorMap tm_q_rope,
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_rope,
                       const __grid_constant__ CUtensorMap tm_kv_lat,
                       const __grid_constant__ CUtensorMap tm_kv_rope, const DecodeParams prm) {
-  using C = Cfg<P_TMEM>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();
@@ -577,31 +707,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   Ctx x;
   x.sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
-  x.kBarOff = C::kBar;
   x.rank = rank;
   x.peer = rank ^ 1u;
   x.err = prm.err;
-  const uint32_t tmem_slot = x.sbase + C::kMisc;
-  x.abort_addr = x.sbase + C::kMisc + 4;
+  const uint32_t tmem_slot = x.sbase + kMisc;
+  x.abort_addr = x.sbase + kMisc + 4;
   x.peer_abort_addr = ptx::map_to_rank(x.abort_addr, x.peer);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(x.bar(B_FULL + s), 1);
       ptx::mbar_init(x.bar(B_EMPTY + s), 1);
     }
-    ptx::mbar_init(x.bar(B_QFULL), 1);
+    ptx::mbar_init(x.bar(B_QFULL), 1 + 4);   // rotary TMA + 4 exchange warps
     ptx::mbar_init(x.bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(B_SFULL + s), 1);
-      ptx::mbar_init(x.bar(B_SEMPTY + s), kSoftmaxWarps);
-      ptx::mbar_init(x.bar(B_PFULL + s), kSoftmaxWarps);
-      ptx::mbar_init(x.bar(B_PEMPTY + s), 1);
+      ptx::mbar_init(x.bar(B_SEMPTY + s), 2 * kSoftmaxWarps);   // softmax + exchange warps
     }
+    ptx::mbar_init(x.bar(B_PFULL), kSoftmaxWarps);
+    ptx::mbar_init(x.bar(B_PEMPTY), 1);
+    ptx::mbar_init(x.bar(B_XREADY), 4);
+    ptx::mbar_init(x.bar(B_XFREE), 1);
     ptx::mbar_init(x.bar(B_OFULL), 1);
     ptx::mbar_init(x.bar(B_OEMPTY), kSoftmaxWarps);
-    ptx::mbar_init(x.bar(B_RFULL), 1);
-    ptx::mbar_init(x.bar(B_REMPTY), kSoftmaxWarps);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(x.bar(B_RFULL + s), 1);   // own expect_tx + the peer's bulk-copy bytes
+      ptx::mbar_init(x.bar(B_REMPTY + s), kSoftmaxWarps);
+    }
     ptx::mbar_init(x.bar(B_TEARDOWN), 1);
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
@@ -611,7 +744,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0) {
-    ptx::prefetch_tmap(&tm_q_lat);
     ptx::prefetch_tmap(&tm_q_rope);
     ptx::prefetch_tmap(&tm_kv_lat);
     ptx::prefetch_tmap(&tm_kv_rope);
@@ -622,14 +754,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   x.tmem = ptx::ld_shared_u32_volatile(tmem_slot);
 
   if (warp == kProducerWarp) {
-    if (lane == 0)
-      run_producer<P_TMEM>(x, w, prm, &tm_q_lat, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
+    if (lane == 0) run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma<P_TMEM>(x, w);
+    if (lane == 0) run_mma(x, w);
     __syncwarp();
-  } else {
-    run_softmax<P_TMEM>(x, w, prm, warp, lane);
+  } else if (warp >= kExchangeWarp0 && warp < kExchangeWarp0 + 4) {
+    run_exchange(x, w, prm, warp - kExchangeWarp0, lane);
+    __syncwarp();
+  } else if (warp < kSoftmaxWarps) {
+    run_softmax(x, w, prm, warp, lane);
     __syncwarp();
   }
 
@@ -659,28 +793,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-bool use_p_tmem() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("MLA_DECODE_P_SMEM");
-    v = (e && e[0] == '1') ? 0 : 1;
-  }
-  return v == 1;
-}
-
 }  // namespace
 
-int decode_smem_bytes() {
-  return use_p_tmem() ? (int)Cfg<true>::kAlloc : (int)Cfg<false>::kAlloc;
-}
+int decode_smem_bytes() { return (int)kSmemAlloc; }
 
 cudaError_t decode_kernel_setup(int /*device*/) {
-  cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)Cfg<true>::kAlloc);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)Cfg<false>::kAlloc);
+  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemAlloc);
 }
 
 int decode_max_clusters(int device) {
@@ -692,12 +811,9 @@ int decode_max_clusters(int device) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * 1024, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)decode_smem_bytes();
+    cfg.dynamicSmemBytes = (size_t)kSmemAlloc;
     int m = 0;
-    cudaError_t e = use_p_tmem()
-                        ? cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel<true>, &cfg)
-                        : cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel<false>, &cfg);
-    if (e == cudaSuccess) n = m;
+    if (cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel, &cfg) == cudaSuccess) n = m;
   }
   if (prev != device) cudaSetDevice(prev);
   return n;
@@ -705,13 +821,8 @@ int decode_max_clusters(int device) {
 
 cudaError_t launch_decode(const TensorMaps& m, const DecodeParams& p, int num_clusters,
                           cudaStream_t stream) {
-  const dim3 grid(2 * num_clusters), block(kThreads);
-  if (use_p_tmem())
-    mla_decode_kernel<true><<<grid, block, Cfg<true>::kAlloc, stream>>>(m.q_lat, m.q_rope,
-                                                                         m.kv_lat, m.kv_rope, p);
-  else
-    mla_decode_kernel<false><<<grid, block, Cfg<false>::kAlloc, stream>>>(m.q_lat, m.q_rope,
-                                                                           m.kv_lat, m.kv_rope, p);
+  mla_decode_kernel<<<dim3(2 * num_clusters), dim3(kThreads), kSmemAlloc, stream>>>(
+      m.q_rope, m.kv_lat, m.kv_rope, p);
   return cudaGetLastError();
 }
 

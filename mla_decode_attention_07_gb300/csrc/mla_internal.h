@@ -13,6 +13,7 @@ constexpr int kDv = 512;   // value dims = the first 512 dims of the row
 
 // Everything the decode kernel needs besides its four tensor maps.
 struct DecodeParams {
+  const void* q;      // bf16 [B, s_q, h_q, 576]
   const int32_t* block_table;
   const int32_t* seqlens;
   const int32_t* plan;
@@ -26,7 +27,7 @@ struct DecodeParams {
 };
 
 struct TensorMaps {
-  CUtensorMap q_lat, q_rope, kv_lat, kv_rope;
+  CUtensorMap q_rope, kv_lat, kv_rope;
 };
 
 // Partial results: one slot holds 128 rows x 512 fp32 plus 128 lse values.
