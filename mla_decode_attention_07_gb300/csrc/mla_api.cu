@@ -19,7 +19,7 @@ namespace {
 __device__ int g_device_error;   // first device-side error of any launch, 0 if none
 
 constexpr int kMaxDevices = 64;
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
 constexpr int kCombineWarps = 8;
 
 // ------------------------------------------------------------------ planner
@@ -51,21 +51,28 @@ __device__ long long block_exclusive_scan(long long v, long long* warp_sums, lon
 }
 
 // The unit prefix sums are searched many times (two binary searches per
-// cluster, two lookups per batch entry); they live in shared memory when they
-// fit (kPlanSmemBatch entries), in the plan buffer otherwise.
-constexpr int kPlanSmemBatch = 6000;
+// cluster, two lookups per batch entry); they and the page counts live in
+// shared memory when they fit (kPlanSmemBatch entries), in the plan buffer
+// otherwise.
+constexpr int kPlanSmemBatch = 4000;
 
 __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* seqlens, int batch,
                                                                 int s_q, int h_q, int num_clusters,
                                                                 int32_t* plan, int* err) {
   __shared__ long long warp_sums[32];
   extern __shared__ int64_t starts_smem[];
+  // The decode kernel may launch now: it reads the plan only after waiting
+  // for this grid to complete.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tiles = plan_tiles(s_q, h_q);
   const int gt = plan_group_clusters(num_clusters, tiles);
   int64_t* starts_g = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(plan) +
                                                  plan_off_starts(batch, gt));
-  int64_t* starts = batch <= kPlanSmemBatch ? starts_smem : starts_g;
+  const bool in_smem = batch <= kPlanSmemBatch;
+  int64_t* starts = in_smem ? starts_smem : starts_g;
   int32_t* items = plan + plan_off_items(gt) / 4;
+  int32_t* pages = in_smem ? reinterpret_cast<int32_t*>(starts_smem + batch + 1) : items;
+  const int pstride = in_smem ? 1 : kItemWords;
   int32_t* clus = plan + H_WORDS;
 
   // 1. unit intervals of the batch entries
@@ -84,6 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
       starts[b] = run + ex;
       starts_g[b] = run + ex;
       items[b * kItemWords + 0] = P;
+      pages[b * pstride] = P;
     }
     run += tot;
   }
@@ -120,7 +128,7 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
     const int b = base + threadIdx.x;
     int ns = 0, cf = -1;
     if (b < batch) {
-      const int P = items[b * kItemWords + 0];
+      const int P = pages[b * pstride];
       if (P > 0) {
         cf = cluster_of(starts[b] + kSplitOverhead, V, g);
         const int cl = cluster_of(starts[b] + kSplitOverhead + P - 1, V, g);
@@ -224,8 +232,12 @@ void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clus
 constexpr int kCombineRows = 32;
 constexpr int kCombineQuads = 32;    // 4-dim groups per CTA (128 dims)
 
+constexpr int kCombineMaxSplitsFast = 16;   // weights kept in registers up to this many splits
+
 __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const DecodeParams p) {
   __shared__ uint2 tile[kCombineRows][kCombineQuads + 1];
+  // Launched as a programmatic dependent of the decode kernel: wait for it.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t* plan = p.plan;
   const int tiles = plan[H_TILES], gt = plan[H_GT], stotal = plan[H_STOTAL];
   const int32_t* items = plan + plan_off_items(gt) / 4;
@@ -253,31 +265,64 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const D
     float m = -INFINITY;
     for (int j = 0; j < ns; ++j) m = fmaxf(m, p.ws_lse[(slot0 + j) * kTileRows + r]);
     float lse = -INFINITY, se = 0.f;
+    float wf[kCombineMaxSplitsFast];
     if (m != -INFINITY) {
-      for (int j = 0; j < ns; ++j) se += expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m);
+#pragma unroll
+      for (int j = 0; j < kCombineMaxSplitsFast; ++j) {
+        wf[j] = j < ns ? expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m) : 0.f;
+        se += wf[j];
+      }
+      for (int j = kCombineMaxSplitsFast; j < ns; ++j)
+        se += expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m);
       lse = m + logf(se);
+#pragma unroll
+      for (int j = 0; j < kCombineMaxSplitsFast; ++j) wf[j] /= se;
     }
-    for (int k = 0; k < kCombineQuads / kCombineWarps; ++k) {
-      const int ql = warp + kCombineWarps * k;
-      const int q = qb * kCombineQuads + ql;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (m != -INFINITY) {
-        for (int j = 0; j < ns; ++j) {
-          const float wgt = expf(p.ws_lse[(slot0 + j) * kTileRows + r] - lse);
-          const float4 v = reinterpret_cast<const float4*>(
-              p.ws_o)[((slot0 + j) * (kDv / 4) + q) * kTileRows + r];
-          acc.x += wgt * v.x;
-          acc.y += wgt * v.y;
-          acc.z += wgt * v.z;
-          acc.w += wgt * v.w;
+    // All loads of this thread (4 dim groups x up to 16 splits) are issued
+    // before any is used, so they are in flight together.
+    constexpr int kQPerThread = kCombineQuads / kCombineWarps;
+    float4 acc[kQPerThread];
+#pragma unroll
+    for (int k = 0; k < kQPerThread; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m != -INFINITY) {
+      const float4* base = reinterpret_cast<const float4*>(p.ws_o) + slot0 * (kDv / 4) * kTileRows +
+                           (int64_t)(qb * kCombineQuads + warp) * kTileRows + r;
+#pragma unroll
+      for (int j = 0; j < kCombineMaxSplitsFast; ++j) {
+        if (j < ns) {
+          float4 v[kQPerThread];
+#pragma unroll
+          for (int k = 0; k < kQPerThread; ++k)
+            v[k] = base[((int64_t)j * (kDv / 4) + kCombineWarps * k) * kTileRows];
+#pragma unroll
+          for (int k = 0; k < kQPerThread; ++k) {
+            acc[k].x += wf[j] * v[k].x;
+            acc[k].y += wf[j] * v[k].y;
+            acc[k].z += wf[j] * v[k].z;
+            acc[k].w += wf[j] * v[k].w;
+          }
         }
       }
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      for (int j = kCombineMaxSplitsFast; j < ns; ++j) {
+        const float wgt = expf(p.ws_lse[(slot0 + j) * kTileRows + r] - lse);
+#pragma unroll
+        for (int k = 0; k < kQPerThread; ++k) {
+          const float4 v = base[((int64_t)j * (kDv / 4) + kCombineWarps * k) * kTileRows];
+          acc[k].x += wgt * v.x;
+          acc[k].y += wgt * v.y;
+          acc[k].z += wgt * v.z;
+          acc[k].w += wgt * v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kQPerThread; ++k) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
       uint2 u;
       memcpy(&u.x, &lo, 4);
       memcpy(&u.y, &hi, 4);
-      tile[lane][ql] = u;
+      tile[lane][warp + kCombineWarps * k] = u;
     }
     if (qb == 0 && warp == 0 && qr < rows) {
       const int i = qr / p.h_q, h = qr - i * p.h_q;
@@ -437,7 +482,9 @@ int mla_decode_plan(const int32_t* cache_seqlens, int batch, int s_q, int h_q, v
   const size_t need = mla_plan_size_for_clusters(batch, s_q, h_q, d.num_clusters);
   if (need == 0) return MLA_ERR_INVALID_ARG;
   if (tile_meta_bytes < need) return MLA_ERR_WORKSPACE;
-  const size_t smem = batch <= kPlanSmemBatch ? sizeof(int64_t) * (size_t)(batch + 1) : 0;
+  const size_t smem = batch <= kPlanSmemBatch
+                          ? sizeof(int64_t) * (size_t)(batch + 1) + sizeof(int32_t) * (size_t)batch
+                          : 0;
   mla_plan_kernel<<<1, kPlanThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       cache_seqlens, batch, s_q, h_q, d.num_clusters, static_cast<int32_t*>(tile_meta), d.err);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
@@ -607,7 +654,15 @@ cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_
                        ((kDv / 4) / kCombineQuads);
   const int64_t cap = (int64_t)num_sms * 8;
   const int grid = (int)(jobs < cap ? jobs : cap);
-  mla_combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
 }
 }  // namespace mla

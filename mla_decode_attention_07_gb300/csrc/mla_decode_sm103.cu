@@ -675,36 +675,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = ptx::cluster_ctarank();
   const int cluster = (int)(blockIdx.x >> 1);
 
-  // The plan must describe this call; both CTAs of a cluster take the same
-  // early exits, before any barrier or TMEM is set up.
-  const int32_t* plan = prm.plan;
-  if (plan[H_MAGIC] != kPlanMagic || plan[H_BATCH] != prm.batch || plan[H_SQ] != prm.s_q ||
-      plan[H_HQ] != prm.h_q || plan[H_NCLUSTERS] != (int)(gridDim.x >> 1)) {
-    if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
-    return;
-  }
-  Work w;
-  const int tiles = plan[H_TILES], gt = plan[H_GT], gused = plan[H_GUSED];
-  if (gt <= 0) return;
-  w.tile = cluster / gt;
-  const int c = cluster - w.tile * gt;
-  if (w.tile >= tiles || c >= gused) return;
-  const int32_t* cl = plan + H_WORDS + c * kClusterWords;
-  w.b0 = cl[0];
-  w.p0 = cl[1];
-  w.b1 = cl[2];
-  w.p1 = cl[3];
-  w.split0 = cl[4];
-  if (w.b0 < 0 || w.p0 < 0 || w.p1 < 0 || w.b0 > w.b1 || w.b1 > prm.batch ||
-      (w.b1 == prm.batch && w.p1 != 0)) {
-    if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
-    return;
-  }
-  if (w.b0 == w.b1 && w.p0 >= w.p1) return;
-  w.rows = prm.s_q * prm.h_q;
-  w.stotal = plan[H_STOTAL];
-  w.items = plan + plan_off_items(gt) / 4;
-
   Ctx x;
   x.sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
   x.rank = rank;
@@ -714,6 +684,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   x.abort_addr = x.sbase + kMisc + 4;
   x.peer_abort_addr = ptx::map_to_rank(x.abort_addr, x.peer);
 
+  // Set-up that needs nothing from earlier kernels; with programmatic
+  // dependent launch it overlaps the planner's tail.
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(x.bar(B_FULL + s), 1);
@@ -753,7 +725,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   x.tmem = ptx::ld_shared_u32_volatile(tmem_slot);
 
-  if (warp == kProducerWarp) {
+  // The plan (and the inputs) come from earlier kernels on the stream.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // The plan must describe this call.  Both CTAs of a cluster read the same
+  // plan and take the same branch.
+  const int32_t* plan = prm.plan;
+  Work w;
+  bool has_work = false;
+  if (plan[H_MAGIC] != kPlanMagic || plan[H_BATCH] != prm.batch || plan[H_SQ] != prm.s_q ||
+      plan[H_HQ] != prm.h_q || plan[H_NCLUSTERS] != (int)(gridDim.x >> 1) || plan[H_GT] <= 0) {
+    if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
+  } else {
+    const int tiles = plan[H_TILES], gt = plan[H_GT], gused = plan[H_GUSED];
+    w.tile = cluster / gt;
+    const int c = cluster - w.tile * gt;
+    if (w.tile < tiles && c < gused) {
+      const int32_t* cl = plan + H_WORDS + c * kClusterWords;
+      w.b0 = cl[0];
+      w.p0 = cl[1];
+      w.b1 = cl[2];
+      w.p1 = cl[3];
+      w.split0 = cl[4];
+      if (w.b0 < 0 || w.p0 < 0 || w.p1 < 0 || w.b0 > w.b1 || w.b1 > prm.batch ||
+          (w.b1 == prm.batch && w.p1 != 0)) {
+        if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
+      } else if (!(w.b0 == w.b1 && w.p0 >= w.p1)) {
+        has_work = true;
+        w.rows = prm.s_q * prm.h_q;
+        w.stotal = plan[H_STOTAL];
+        w.items = plan + plan_off_items(gt) / 4;
+      }
+    }
+  }
+
+  if (!has_work) {
+    // nothing to do: fall through to the teardown
+  } else if (warp == kProducerWarp) {
     if (lane == 0) run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -821,9 +830,17 @@ int decode_max_clusters(int device) {
 
 cudaError_t launch_decode(const TensorMaps& m, const DecodeParams& p, int num_clusters,
                           cudaStream_t stream) {
-  mla_decode_kernel<<<dim3(2 * num_clusters), dim3(kThreads), kSmemAlloc, stream>>>(
-      m.q_rope, m.kv_lat, m.kv_rope, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_clusters);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, m.q_rope, m.kv_lat, m.kv_rope, p);
 }
 
 }  // namespace mla
