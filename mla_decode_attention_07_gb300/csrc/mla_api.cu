@@ -12,6 +12,7 @@
 
 #include "mla.h"
 #include "mla_internal.h"
+#include "ptx_sm103.cuh"
 
 namespace mla {
 namespace {
@@ -225,17 +226,27 @@ void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clus
 // Merges the split partials of every (batch entry, tile) that has two or
 // more splits:  lse = m + ln(sum_j exp(lse_j - m)),  out = sum_j
 // exp(lse_j - lse) * o_j.  Entries without pages get out = 0, lse = -inf.
-// A CTA takes 32 rows x 128 output dims of one (entry, tile); partials are
-// stored [slot][dim/4][row][4], so a warp reads 32 consecutive rows of one
-// 4-dim group (512 contiguous bytes).  The bf16 block is staged in shared
-// memory and written back row by row.
-constexpr int kCombineRows = 32;
-constexpr int kCombineQuads = 32;    // 4-dim groups per CTA (128 dims)
-
-constexpr int kCombineMaxSplitsFast = 16;   // weights kept in registers up to this many splits
+// The decode kernel stores partials as [slot][dim/4][row][4] fp32, so the 4
+// dim groups (16 dims) x 128 rows that one CTA merges are 8 KB contiguous per
+// split: one thread moves all of a job's splits into shared memory with TMA
+// bulk copies (up to kCombineChunk splits, 64 KB, in flight at once), then
+// 256 threads (one per row and pair of dim groups) merge them.  The merge
+// weights come straight from the per-split lse values.
+constexpr int kCombineQuads = 4;                                        // dim groups per job
+constexpr int kCombineChunk = 8;                                        // splits per pass
+constexpr uint32_t kCombineSplitBytes = kCombineQuads * kTileRows * 16;  // 8 KB
+constexpr uint32_t kCombineSmem = kCombineChunk * kCombineSplitBytes + 64;
+constexpr uint64_t kCombineWaitNs = 2000000000ull;
 
 __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const DecodeParams p) {
-  __shared__ uint2 tile[kCombineRows][kCombineQuads + 1];
+  extern __shared__ __align__(128) uint8_t csmem[];
+  const uint32_t buf = ptx::smem_addr(csmem);
+  const uint32_t bar = buf + kCombineChunk * kCombineSplitBytes;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   // Launched as a programmatic dependent of the decode kernel: wait for it.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t* plan = p.plan;
@@ -243,106 +254,119 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const D
   const int32_t* items = plan + plan_off_items(gt) / 4;
   const int64_t max_slots = workspace_slots(plan[H_NCLUSTERS]);
   const int rows = p.s_q * p.h_q;
-  const int row_blocks = kTileRows / kCombineRows, quad_blocks = (kDv / 4) / kCombineQuads;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)p.batch * tiles * row_blocks * quad_blocks;
-  for (int64_t job = blockIdx.x; job < total; job += gridDim.x) {
-    const int qb = (int)(job % quad_blocks);
-    const int rb = (int)((job / quad_blocks) % row_blocks);
-    const int64_t item = job / (quad_blocks * row_blocks);
+  constexpr int kQuadBlocks = (kDv / 4) / kCombineQuads;   // 32
+  const int r = threadIdx.x & (kTileRows - 1);             // tile row of this thread
+  const int qpair = threadIdx.x >> 7;                      // dim groups 2 qpair, 2 qpair + 1
+  uint32_t phase = 0;
+  bool ok = true;
+  const int64_t total = (int64_t)p.batch * tiles * kQuadBlocks;
+  for (int64_t job = blockIdx.x; job < total && ok; job += gridDim.x) {
+    const int qb = (int)(job % kQuadBlocks);
+    const int64_t item = job / kQuadBlocks;
     const int b = (int)(item % p.batch), t = (int)(item / p.batch);
     const int ns = items[b * kItemWords + 1];
-    if (ns == 1) continue;                                  // written by the main kernel
-    if (t * kTileRows + rb * kCombineRows >= rows) continue;  // padding rows only
+    if (ns == 1) continue;                                   // written by the main kernel
+    if (t * kTileRows >= rows) continue;                      // padding tile
     const int64_t slot0 = (int64_t)t * stotal + items[b * kItemWords + 2];
     if (ns > 1 && (slot0 < 0 || slot0 + ns > max_slots)) {
       if (threadIdx.x == 0) atomicCAS(p.err, 0, MLA_ERR_PLAN);
       continue;
     }
-    const int r = rb * kCombineRows + lane;                  // tile row of this lane
     const int qr = t * kTileRows + r;
-    // merge weights of this row
+    const float* lse_col = p.ws_lse + slot0 * kTileRows + r;
+    // the first kCombineChunk lse values are loaded together (predicated)
+    float lj[kCombineChunk];
+#pragma unroll
+    for (int j = 0; j < kCombineChunk; ++j)
+      lj[j] = j < ns ? lse_col[(int64_t)j * kTileRows] : -INFINITY;
     float m = -INFINITY;
-    for (int j = 0; j < ns; ++j) m = fmaxf(m, p.ws_lse[(slot0 + j) * kTileRows + r]);
-    float lse = -INFINITY, se = 0.f;
-    float wf[kCombineMaxSplitsFast];
-    if (m != -INFINITY) {
 #pragma unroll
-      for (int j = 0; j < kCombineMaxSplitsFast; ++j) {
-        wf[j] = j < ns ? expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m) : 0.f;
-        se += wf[j];
+    for (int j = 0; j < kCombineChunk; ++j) m = fmaxf(m, lj[j]);
+    for (int j = kCombineChunk; j < ns; ++j) m = fmaxf(m, lse_col[(int64_t)j * kTileRows]);
+    float se = 0.f;
+    float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+    for (int c0 = 0; c0 < ns; c0 += kCombineChunk) {
+      const int nc = ns - c0 < kCombineChunk ? ns - c0 : kCombineChunk;
+      if (threadIdx.x == 0) {
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)nc * kCombineSplitBytes);
+        for (int j = 0; j < nc; ++j) {
+          const float* src = p.ws_o + (slot0 + c0 + j) * kSlotFloats +
+                             (int64_t)qb * kCombineQuads * kTileRows * 4;
+          ptx::bulk_load_global(buf + j * kCombineSplitBytes, src, kCombineSplitBytes, bar);
+        }
       }
-      for (int j = kCombineMaxSplitsFast; j < ns; ++j)
-        se += expf(p.ws_lse[(slot0 + j) * kTileRows + r] - m);
-      lse = m + logf(se);
+      // weights of this chunk while the copies are in flight
+      float wj[kCombineChunk];
 #pragma unroll
-      for (int j = 0; j < kCombineMaxSplitsFast; ++j) wf[j] /= se;
-    }
-    // All loads of this thread (4 dim groups x up to 16 splits) are issued
-    // before any is used, so they are in flight together.
-    constexpr int kQPerThread = kCombineQuads / kCombineWarps;
-    float4 acc[kQPerThread];
-#pragma unroll
-    for (int k = 0; k < kQPerThread; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
-      const float4* base = reinterpret_cast<const float4*>(p.ws_o) + slot0 * (kDv / 4) * kTileRows +
-                           (int64_t)(qb * kCombineQuads + warp) * kTileRows + r;
-#pragma unroll
-      for (int j = 0; j < kCombineMaxSplitsFast; ++j) {
-        if (j < ns) {
-          float4 v[kQPerThread];
-#pragma unroll
-          for (int k = 0; k < kQPerThread; ++k)
-            v[k] = base[((int64_t)j * (kDv / 4) + kCombineWarps * k) * kTileRows];
-#pragma unroll
-          for (int k = 0; k < kQPerThread; ++k) {
-            acc[k].x += wf[j] * v[k].x;
-            acc[k].y += wf[j] * v[k].y;
-            acc[k].z += wf[j] * v[k].z;
-            acc[k].w += wf[j] * v[k].w;
+      for (int j = 0; j < kCombineChunk; ++j) {
+        const float lv = c0 == 0 ? lj[j]
+                         : (j < nc ? lse_col[(int64_t)(c0 + j) * kTileRows] : -INFINITY);
+        wj[j] = (j < nc && m != -INFINITY) ? expf(lv - m) : 0.f;
+        se += wj[j];
+      }
+      // bounded wait for the chunk
+      if (!ptx::mbar_try_wait(bar, phase)) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(bar, phase)) {
+          if (ptx::globaltimer() - t0 > kCombineWaitNs) {
+            ok = false;
+            break;
           }
         }
       }
-      for (int j = kCombineMaxSplitsFast; j < ns; ++j) {
-        const float wgt = expf(p.ws_lse[(slot0 + j) * kTileRows + r] - lse);
+      if (!__syncthreads_and(ok)) {
+        ok = false;
+        break;
+      }
+      phase ^= 1u;
 #pragma unroll
-        for (int k = 0; k < kQPerThread; ++k) {
-          const float4 v = base[((int64_t)j * (kDv / 4) + kCombineWarps * k) * kTileRows];
-          acc[k].x += wgt * v.x;
-          acc[k].y += wgt * v.y;
-          acc[k].z += wgt * v.z;
-          acc[k].w += wgt * v.w;
+      for (int j = 0; j < kCombineChunk; ++j) {
+        if (j < nc) {
+          const uint32_t a = buf + j * kCombineSplitBytes + ((2 * qpair) * kTileRows + r) * 16;
+          const float4 v0 = ptx::ld_shared_v4f(a);
+          const float4 v1 = ptx::ld_shared_v4f(a + kTileRows * 16);
+          acc0.x += wj[j] * v0.x;
+          acc0.y += wj[j] * v0.y;
+          acc0.z += wj[j] * v0.z;
+          acc0.w += wj[j] * v0.w;
+          acc1.x += wj[j] * v1.x;
+          acc1.y += wj[j] * v1.y;
+          acc1.z += wj[j] * v1.z;
+          acc1.w += wj[j] * v1.w;
         }
       }
+      __syncthreads();   // the buffer is free for the next chunk or job
     }
-#pragma unroll
-    for (int k = 0; k < kQPerThread; ++k) {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-      uint2 u;
-      memcpy(&u.x, &lo, 4);
-      memcpy(&u.y, &hi, 4);
-      tile[lane][warp + kCombineWarps * k] = u;
+    if (!ok) break;
+    if (qr >= rows) continue;
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+      const float inv = 1.0f / se;
+      acc0.x *= inv; acc0.y *= inv; acc0.z *= inv; acc0.w *= inv;
+      acc1.x *= inv; acc1.y *= inv; acc1.z *= inv; acc1.w *= inv;
+      lse = m + logf(se);
     }
-    if (qb == 0 && warp == 0 && qr < rows) {
-      const int i = qr / p.h_q, h = qr - i * p.h_q;
-      p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
-    }
-    __syncthreads();
-    // write back: 8 threads per row, 32 contiguous bytes each
-    for (int e = threadIdx.x; e < kCombineRows * 8; e += blockDim.x) {
-      const int rl = e >> 3, part = e & 7;
-      const int qr2 = t * kTileRows + rb * kCombineRows + rl;
-      if (qr2 < rows) {
-        const int i = qr2 / p.h_q, h = qr2 - i * p.h_q;
-        uint2* dst = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) +
-                                              (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv +
-                                              (qb * kCombineQuads + part * 4) * 4);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) dst[k] = tile[rl][part * 4 + k];
-      }
-    }
-    __syncthreads();
+    const int i = qr / p.h_q, h = qr - i * p.h_q;
+    uint4 u;
+    const __nv_bfloat162 a0 = __floats2bfloat162_rn(acc0.x, acc0.y);
+    const __nv_bfloat162 a1 = __floats2bfloat162_rn(acc0.z, acc0.w);
+    const __nv_bfloat162 a2 = __floats2bfloat162_rn(acc1.x, acc1.y);
+    const __nv_bfloat162 a3 = __floats2bfloat162_rn(acc1.z, acc1.w);
+    memcpy(&u.x, &a0, 4);
+    memcpy(&u.y, &a1, 4);
+    memcpy(&u.z, &a2, 4);
+    memcpy(&u.w, &a3, 4);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                              (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv +
+                              (qb * kCombineQuads + 2 * qpair) * 4) = u;
+    if (qb == 0 && qpair == 0) p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
+  }
+  if (!ok) {
+    // a copy never completed: record it and let anything in flight land
+    // before the shared memory is released
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, MLA_ERR_DEVICE_TIMEOUT);
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 2000000ull) __nanosleep(1000);
   }
 }
 
@@ -373,7 +397,9 @@ int setup_device(int device) {
     } else {
       void* addr = nullptr;
       const int maxc = decode_max_clusters(device);
-      if (maxc <= 0 || cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) {
+      if (maxc <= 0 || cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess ||
+          cudaFuncSetAttribute(mla_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kCombineSmem) != cudaSuccess) {
         d.status = MLA_ERR_CUDA;
       } else {
         d.num_sms = sms;
@@ -650,13 +676,13 @@ namespace mla {
 cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_sms,
                            cudaStream_t stream) {
   const int tiles = plan_tiles(p.s_q, p.h_q);
-  const int64_t jobs = (int64_t)p.batch * tiles * (kTileRows / kCombineRows) *
-                       ((kDv / 4) / kCombineQuads);
-  const int64_t cap = (int64_t)num_sms * 8;
+  const int64_t jobs = (int64_t)p.batch * tiles * ((kDv / 4) / kCombineQuads);
+  const int64_t cap = (int64_t)num_sms * 3;
   const int grid = (int)(jobs < cap ? jobs : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = kCombineSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -17,24 +17,35 @@
 // GB300 design (not the talk's):
 //  * One work unit is a cluster of two CTAs on two SMs.  A 128-row tile of
 //    queries has an fp32 output of 128 x 512 = all 512 TMEM columns of one SM,
-//    so CTA r owns output dims [256 r, 256 r + 256).
+//    so CTA r owns output dims [256 r, 256 r + 256) for all 128 rows.
 //  * The 576-wide Q.K^T reduction is split between the CTAs as well: CTA r
 //    multiplies its latent half (dims [256 r, 256 r + 256)) plus half of the
 //    rotary dims ([512 + 32 r, 512 + 32 r + 32)).  Each CTA therefore loads
 //    exactly 36 KB of every 72 KB page: the pair reads each page once, with
-//    no duplicated tensor work.  The two 128 x 64 fp32 partial score tiles
-//    are exchanged through distributed shared memory and summed; both CTAs
-//    then run the same softmax on bit-identical scores, so their running
-//    maxima agree exactly.
-//  * Dedicated exchange warps ship each page's partial scores as soon as the
-//    score MMA has written them, into a double-buffered receive buffer, so
-//    the cross-SM transfer of page g+1 overlaps the softmax of page g.
-//  * Warp roles: warps 0-3 softmax + epilogue (one thread per TMEM lane =
-//    query row), warps 4-7 score exchange (and the per-tile load of Q's
-//    latent half into TMEM), warp 8 TMA producer, warp 9 MMA issuer and TMEM
-//    owner.  The MMA issuer polls its barriers and issues whichever MMA is
-//    ready, so a page still in flight from HBM never holds back the P.V of an
-//    earlier one.
+//    no duplicated tensor work.
+//  * The softmax is split by rows: CTA r owns query rows [64 r, 64 r + 64).
+//    For every page it sends the peer the 64 x 64 fp32 partial scores of the
+//    peer's rows (16 KB), adds the peer's partial for its own rows, runs the
+//    online softmax for them and sends back their bf16 probabilities (8 KB)
+//    and rescale factors, so both CTAs hold P for all 128 rows for their
+//    halves of O.  All cross-SM traffic is TMA bulk copies between the two
+//    CTAs' shared memories, completed on mbarriers.  Distributed shared
+//    memory moves about 37 GB/s per SM on GB300, so the 24 KB per page this
+//    costs is close to the HBM time of a page; sending the whole 32 KB
+//    partial tile both ways would not be.
+//  * Warp roles: warps 0-3 own TMEM lanes 32w..32w+31 (= query rows); in
+//    CTA r the two warps on rows [64 r, 64 r + 64) run the softmax, the other
+//    two import the peer's probabilities (and rescale those rows of O).
+//    Warps 4-7 load Q's latent half into TMEM per tile, and the two of them on
+//    the peer's rows ship those rows' partial scores.  Warp 8 is the TMA
+//    producer, warp 9 the MMA issuer and TMEM owner; it polls its barriers
+//    and issues whichever MMA is ready.  One thread of warp 10 ships this
+//    CTA's probability rows to the peer, so the softmax warps go straight on
+//    to the next page.
+//  * A thread that has a remote operation in flight (a copy or an arrive on
+//    the peer's barrier) does not also signal the local barriers of the
+//    critical path: a release arrive may wait for that remote operation to
+//    complete, which the transfers queued ahead of it make slow.
 //  * S = Q K^T: M=128, N=64, 18 K-steps (16 latent with Q read from TMEM, 2
 //    rotary from shared memory) into a double buffered TMEM score tile;
 //    O += P V: M=128, N=256, K=64 with P from shared memory and V from the
@@ -58,17 +69,19 @@
 namespace mla {
 namespace {
 
-// Warp roles: 0-3 softmax, 4-7 score exchange, 8 TMA producer, 9 MMA
-// issuer.  Warp w reaches TMEM lanes [32 (w % 4), 32 (w % 4) + 32).
-constexpr int kThreads = 320;
-constexpr int kSoftmaxWarps = 4;
+// Warp roles (see above).  Warp w reaches TMEM lanes [32 (w % 4), +32).
+constexpr int kThreads = 352;
+constexpr int kRowWarps = 4;
 constexpr int kExchangeWarp0 = 4;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kPSendWarp = 10;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after an abort
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kHalfRows = 64;                        // softmax rows owned by one CTA
+constexpr int kRemoteLane = 31;   // the lane that issues a warp's remote copies and arrives
 
 // TMEM columns (fp32 / packed-bf16x2 32-bit cells, 128 lanes).
 constexpr uint32_t kTmemCols = 512;
@@ -77,44 +90,52 @@ constexpr uint32_t kColS = 256;   // two 64-column score tiles
 constexpr uint32_t kColQ = 384;   // Q's latent half, bf16x2: 128 rows x 256 dims
 
 // Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr uint32_t kQRope = 0;            // [128 x 32] bf16, 64-byte swizzle
 constexpr uint32_t kStage0 = 8192;        // kStages x 36 KB
 constexpr uint32_t kStageBytes = 36864;
 constexpr uint32_t kStageRope = 32768;    // rotary box inside a stage
-constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][128 rows] x 16 B
-constexpr uint32_t kRecvBytes = 128 * 64 * 4;
-constexpr uint32_t kP = kRecv + 2 * kRecvBytes;               // [128 x 64] bf16, 128-byte swizzle
+constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][64 rows] x 16 B
+constexpr uint32_t kRecvBytes = kHalfRows * 64 * 4;
+constexpr uint32_t kXStage = kRecv + 2 * kRecvBytes;        // [16 chunks][64 rows] x 16 B
+constexpr uint32_t kP = kXStage + kRecvBytes;                // [128 x 64] bf16, 128-byte swizzle
 constexpr uint32_t kPBytes = 128 * 64 * 2;
-constexpr uint32_t kXStage = kP + kPBytes;                     // [8 chunks][128 rows] x 16 B
-constexpr uint32_t kXStageBytes = kRecvBytes / 2;
-constexpr uint32_t kBar = kXStage + kXStageBytes;
-constexpr uint32_t kMisc = kBar + 8 * 32;
+constexpr uint32_t kAlpha = kP + kPBytes;                    // float[128] rescale factors
+constexpr uint32_t kInvL = kAlpha + 128 * 4;                 // float[2][128] 1/l per tile parity
+constexpr uint32_t kBar = kInvL + 2 * 128 * 4;
+constexpr uint32_t kMisc = kBar + 8 * 40;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
 static_assert(kP % 1024 == 0 && kStage0 % 1024 == 0, "swizzled buffers need 1 KB alignment");
+static_assert(kSmemAlloc <= 232448, "shared memory");
 
 // Bytes moved per stage / per Q tile by one CTA.
 constexpr uint32_t kStageTx = 4 * 8192 + 4096;   // 4 latent boxes + rotary half
 constexpr uint32_t kQRopeTx = 8192;
+constexpr uint32_t kPRowsBytes = kHalfRows * 128;    // one CTA's 64 rows of P
+constexpr uint32_t kAlphaBytes = kHalfRows * 4;
 
 enum Bar : uint32_t {
-  B_FULL = 0,      // [kStages] stage loaded (TMA tx)
-  B_EMPTY = 4,     // [kStages] stage consumed (MMA commit)
-  B_QFULL = 8,     // Q tile ready: rotary half (TMA) + latent half (exchange warps)
-  B_QEMPTY = 9,    // last score MMA of a tile done
-  B_SFULL = 10,    // [2] score tile ready (MMA commit)
-  B_SEMPTY = 12,   // [2] score tile read (softmax + exchange warps)
-  B_PFULL = 14,    // probabilities written (softmax warps)
-  B_PEMPTY = 16,   // P.V done (MMA commit)
-  B_OFULL = 18,
-  B_OEMPTY = 19,
-  B_RFULL = 20,    // [2] the peer's partial scores are in receive buffer i (bulk-copy tx)
-  B_REMPTY = 22,   // [2] the peer has read receive buffer i of this CTA's sends
-  B_TEARDOWN = 24,
-  B_XREADY = 25,   // the exchange staging buffer is written (4 exchange warps)
-  B_XFREE = 26,    // the bulk copy has finished reading the staging buffer
+  B_FULL = 0,       // [4] stage loaded (TMA tx)
+  B_EMPTY = 4,      // [4] stage consumed (MMA commit)
+  B_QFULL = 8,      // Q tile ready: rotary half (TMA) + latent half (4 exchange warps)
+  B_QEMPTY = 9,     // last score MMA of a tile done
+  B_SFULL = 10,     // [2] score tile ready (MMA commit)
+  B_SEMPTY = 12,    // [2] score tile read (2 softmax warps + 2 sending warps)
+  B_PFULL = 14,     // all 128 rows of P in shared memory and O rescaled (4 row warps)
+  B_PEMPTY = 15,    // P.V done (MMA commit)
+  B_OFULL = 16,
+  B_OEMPTY = 17,    // 4 row warps
+  B_RFULL = 18,     // [2] the peer's partial scores for my rows (bulk-copy tx)
+  B_REMPTY = 20,    // [2] the peer's softmax warps have read what I sent (2 remote arrives)
+  B_XREADY = 22,    // staging written (2 sending warps)
+  B_XFREE = 23,     // staging read by the bulk copy
+  B_PRECV = 24,     // the peer's P rows and rescale factors arrived (bulk-copy tx)
+  B_PFREE = 25,     // the peer's P buffer may take my next rows (peer's P.V done)
+  B_PLOCAL = 26,    // my 2 softmax warps wrote their P rows
+  B_PSENT = 27,     // my P rows have been read by the bulk copy to the peer (P sender)
+  B_LRECV = 28,     // [2] the peer's 1/l for its rows arrived (per tile parity)
+  B_TEARDOWN = 30,
 };
-static_assert(kStages <= 4, "barrier slots");
 
 struct Ctx {
   uint32_t sbase;       // 1024-aligned shared base
@@ -314,16 +335,25 @@ __device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
   uint32_t idle = 0;
   while (cp.valid) {
     bool progress = false;
+    // The first barrier found not ready, for the idle wait below.
+    uint32_t blk_bar = 0, blk_par = 0;
     // P.V of the oldest page whose probabilities are ready.
     if (gp < gq) {
       bool ok = true;
       if (cp.first() && (int)cp.item != o_ok_item) {
-        if (ptx::mbar_test_wait(x.bar(B_OEMPTY), (cp.item & 1u) ^ 1u))
+        if (ptx::mbar_test_wait(x.bar(B_OEMPTY), (cp.item & 1u) ^ 1u)) {
           o_ok_item = (int)cp.item;
-        else
+        } else {
           ok = false;
+          blk_bar = x.bar(B_OEMPTY);
+          blk_par = (cp.item & 1u) ^ 1u;
+        }
       }
-      if (ok) ok = ptx::mbar_test_wait(x.bar(B_PFULL), gp & 1u);
+      if (ok && !ptx::mbar_test_wait(x.bar(B_PFULL), gp & 1u)) {
+        ok = false;
+        blk_bar = x.bar(B_PFULL);
+        blk_par = gp & 1u;
+      }
       if (ok) {
         ptx::tc_fence_after();
         issue_pv(x, gp, cp.first());
@@ -337,16 +367,19 @@ __device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
     }
     // Scores of the next page once it is loaded and its TMEM tile is free.
     if (cq.valid) {
-      bool ok = true;
+      uint32_t bq = 0, pq = 0;
       if ((int)cq.item != q_ok_item) {
         if (ptx::mbar_test_wait(x.bar(B_QFULL), cq.item & 1u))
           q_ok_item = (int)cq.item;
         else
-          ok = false;
+          bq = x.bar(B_QFULL), pq = cq.item & 1u;
       }
-      if (ok) ok = ptx::mbar_test_wait(x.bar(B_FULL + gq % kStages), (gq / kStages) & 1u);
-      if (ok) ok = ptx::mbar_test_wait(x.bar(B_SEMPTY + (gq & 1u)), ((gq >> 1) & 1u) ^ 1u);
-      if (ok) {
+      if (bq == 0u && !ptx::mbar_test_wait(x.bar(B_FULL + gq % kStages), (gq / kStages) & 1u))
+        bq = x.bar(B_FULL + gq % kStages), pq = (gq / kStages) & 1u;
+      if (bq == 0u &&
+          !ptx::mbar_test_wait(x.bar(B_SEMPTY + (gq & 1u)), ((gq >> 1) & 1u) ^ 1u))
+        bq = x.bar(B_SEMPTY + (gq & 1u)), pq = ((gq >> 1) & 1u) ^ 1u;
+      if (bq == 0u) {
         ptx::tc_fence_after();
         issue_qk(x, gq);
         ptx::mma_commit(x.bar(B_SFULL + (gq & 1u)));
@@ -354,15 +387,21 @@ __device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
         cq.advance();
         ++gq;
         progress = true;
+      } else if (blk_bar == 0u) {
+        blk_bar = bq;
+        blk_par = pq;
       }
     }
     if (progress) {
       idle = 0;
       continue;
     }
-    // Nothing ready: back off briefly (this warp shares a scheduler with a
-    // softmax warp) and keep the wait bounded.
-    __nanosleep(20);
+    // Nothing ready: sleep on the first barrier that blocked (the oldest MMA
+    // still to issue comes first).  The thread is woken as soon as that phase
+    // completes, or after a short limit so the other kind is polled too, and
+    // takes no issue slots from the softmax warp on this scheduler meanwhile.
+    // The wait as a whole stays bounded.
+    if (blk_bar != 0u) ptx::mbar_try_wait_for(blk_bar, blk_par, 200u);
     if ((++idle & 63u) == 0u) {
       if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) return false;
       const uint64_t now = ptx::globaltimer();
@@ -376,21 +415,24 @@ __device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
   return true;
 }
 
-// ------------------------------------------------------------------ score exchange
-// Warps 4-7 (a) put the latent half of each Q tile into TMEM, one row per
-// thread, and (b) ship this CTA's partial scores of every page to the peer
-// CTA as soon as the score MMA has written them, into receive buffer g % 2,
-// so the transfer overlaps the softmax of the previous page.  Receive buffer
-// layout [16-byte chunk c][row r].  The partial scores are staged in local
-// shared memory and moved by the TMA engine (bulk copy shared::cta ->
-// shared::cluster), which completes the bytes on the peer's barrier; the
-// receiving side posts the expected byte count itself.
+// ------------------------------------------------------------------ exchange warps
+// Warps 4-7 put the latent half of each Q tile into TMEM (one row per
+// thread).  The two of them whose lanes are the peer's softmax rows then ship
+// those rows' partial scores of every page to the peer, as soon as the score
+// MMA has written them: staged in local shared memory as [16-byte chunk c]
+// [row] and moved by one TMA bulk copy (shared::cta -> shared::cluster) into
+// the peer's receive buffer g % 2, completing the bytes on the peer's
+// barrier; the receiving side posts the expected byte count itself.
 __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const DecodeParams& prm,
                                              int e, int lane) {
   const int r = e * 32 + lane;
   const uint32_t lane_base = (uint32_t)(e * 32) << 16;
+  const bool sender = (uint32_t)(e >> 1) != x.rank;   // lanes of the peer's rows
+  // The copy is issued by a lane that signals no local barrier.
+  const bool issuer = sender && (e & 1) == 0 && lane == kRemoteLane;
   const uint32_t peer_recv = ptx::map_to_rank(x.sbase + kRecv, x.peer);
   const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
+  const uint32_t stage_row = x.sbase + kXStage + (uint32_t)(r & (kHalfRows - 1)) * 16u;
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
@@ -404,16 +446,20 @@ __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const 
     const bool valid = qr < w.rows;
     const uint4* src = reinterpret_cast<const uint4*>(
         q + ((int64_t)b * w.rows + (valid ? qr : 0)) * kDqk + 256 * (int)x.rank);
-#pragma unroll 1
+    // All 32 loads of the row are issued before the first use: the tile's
+    // first score MMA waits on this, so it costs one memory latency, not four.
+    uint4 qv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) qv[j] = valid ? src[j] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
       uint32_t v[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint4 u = valid ? src[ch * 8 + j] : make_uint4(0u, 0u, 0u, 0u);
-        v[4 * j] = u.x;
-        v[4 * j + 1] = u.y;
-        v[4 * j + 2] = u.z;
-        v[4 * j + 3] = u.w;
+        v[4 * j] = qv[ch * 8 + j].x;
+        v[4 * j + 1] = qv[ch * 8 + j].y;
+        v[4 * j + 2] = qv[ch * 8 + j].z;
+        v[4 * j + 3] = qv[ch * 8 + j].w;
       }
       ptx::tmem_st32(x.tmem + lane_base + kColQ + ch * 32, v);
     }
@@ -422,59 +468,69 @@ __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const 
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(x.bar(B_QFULL));
 
+    if (!sender) {
+      g += (uint32_t)(pe - pb);
+      ++n_item;
+      continue;
+    }
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const uint32_t sb = g & 1u;
       if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
       ptx::tc_fence_after();
-      // the peer has read what was sent into this buffer two pages ago
+      // the peer has read what was sent into this buffer two pages ago, and
+      // the staging buffer is free again
       if (!wait_warp(x, x.bar(B_REMPTY + sb), ((g >> 1) & 1u) ^ 1u, true)) return false;
-      // Two 16 KB halves: stage columns [32 h, 32 h + 32) of every row, then
-      // one thread hands the block to the TMA engine for the cross-SM copy.
-#pragma unroll 1
+      if (!wait_warp(x, x.bar(B_XFREE), (g & 1u) ^ 1u)) return false;
+#pragma unroll
       for (int half = 0; half < 2; ++half) {
-        const uint32_t use = 2u * g + (uint32_t)half;
-        if (!wait_warp(x, x.bar(B_XFREE), (use & 1u) ^ 1u)) return false;
         uint32_t v[32];
         tmem_load32(x.tmem + lane_base + kColS + sb * 64 + half * 32, v);
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          ptx::st_shared_v4(x.sbase + kXStage + (uint32_t)c * 2048u + (uint32_t)r * 16u, v[4 * c],
+          ptx::st_shared_v4(stage_row + (uint32_t)(half * 8 + c) * (kHalfRows * 16), v[4 * c],
                             v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(x.bar(B_XREADY));
-        bool ok = true;
-        if (e == 0 && lane == 0) {
-          ok = wait_bar(x, x.bar(B_XREADY), use & 1u);
-          if (ok) {
-            ptx::bulk_copy_to_peer(peer_recv + sb * kRecvBytes + (uint32_t)half * kXStageBytes,
-                                   x.sbase + kXStage, kXStageBytes, peer_rfull + 8u * sb);
-            ptx::bulk_commit();
-            ptx::bulk_wait_read_all();
-            ptx::mbar_arrive(x.bar(B_XFREE));
-          }
-        }
-        if (!__all_sync(0xffffffffu, ok)) return false;
       }
+      ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+      if (lane == 0) {
+        ptx::mbar_arrive(x.bar(B_XREADY));
+        ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+      }
+      bool ok = true;
+      if (issuer) {
+        ok = wait_bar(x, x.bar(B_XREADY), g & 1u);
+        if (ok) {
+          ptx::bulk_copy_to_peer(peer_recv + sb * kRecvBytes, x.sbase + kXStage, kRecvBytes,
+                                 peer_rfull + 8u * sb);
+          ptx::bulk_commit();
+          ptx::bulk_wait_read_all();
+          ptx::mbar_arrive_relaxed(x.bar(B_XFREE));   // the copy has read the staging
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) return false;
     }
     ++n_item;
   }
   return true;
 }
 
-// ------------------------------------------------------------------ softmax + epilogue
-__device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const DecodeParams& prm,
-                                            int warp, int lane) {
+// ------------------------------------------------------------------ row warps
+// Warps 0-3, one thread per query row (= TMEM lane).  In CTA r the warps on
+// rows [64 r, 64 r + 64) own those rows' softmax; the other two import the
+// peer's probability rows.  Both kinds write the epilogue of their rows for
+// this CTA's half of the output dims.
+__device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const DecodeParams& prm,
+                                         int warp, int lane) {
   const int r = warp * 32 + lane;                   // tile row == TMEM lane
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  // Receive buffer layout [16-byte chunk c][row r]: chunk c of row r at
-  // (c * 128 + r) * 16, so one warp's store (or load) of a chunk covers 512
-  // contiguous bytes.
-  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)r * 16u;
+  const bool owner = (uint32_t)(warp >> 1) == x.rank;
+  const bool lead = (warp & 1) == 0 && lane == 0;   // first lane of the pair of warps
+  const int hr = r & (kHalfRows - 1);               // row inside its half
+  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)hr * 16u;
   const uint32_t peer_rempty = ptx::map_to_rank(x.bar(B_REMPTY), x.peer);
+  const uint32_t peer_pfree = ptx::map_to_rank(x.bar(B_PFREE), x.peer);
+  const uint32_t peer_lrecv = ptx::map_to_rank(x.bar(B_LRECV), x.peer);
   const uint32_t pswz = (uint32_t)(r & 7);
   const float scale_log2 = prm.scale_log2;
 
@@ -497,126 +553,190 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const bool first = (pg == pb);
       const uint32_t sb = g & 1u;
-
-      // 1. Full scores of page g: own partial (TMEM, once this CTA's score MMA
-      //    is done) + the peer's (received).
-      if (r == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + sb), kRecvBytes);
-      if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
-      if (!wait_warp(x, x.bar(B_RFULL + sb), (g >> 1) & 1u, true)) return false;
-      ptx::tc_fence_after();
-      float s[64];
-      {
-        uint32_t v[32];
-        tmem_load32(x.tmem + lane_base + kColS + sb * 64, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
-        tmem_load32(x.tmem + lane_base + kColS + sb * 64 + 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(v[k]);
-      }
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float4 v = ptx::ld_shared_v4f(recv_row + sb * kRecvBytes + (uint32_t)c * 2048u);
-        s[4 * c] += v.x;   // addition commutes: both CTAs get identical sums
-        s[4 * c + 1] += v.y;
-        s[4 * c + 2] += v.z;
-        s[4 * c + 3] += v.w;
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
-        ptx::mbar_arrive_cluster(peer_rempty + 8u * sb);
-      }
-
-      // 2. Mask, row max (the accum_s -> scores_max reduce), exp2, sums.
-      const int tok0 = pg * kPageTokens;
-      if (__any_sync(0xffffffffu, tok0 + kPageTokens > n_valid)) {
-#pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (tok0 + k >= n_valid) s[k] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
-      const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
-      const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
-
-      // The previous page's P.V must be done: it frees the probability tile
-      // and leaves O holding every page before this one.
-      if (!wait_warp(x, x.bar(B_PEMPTY), (g & 1u) ^ 1u)) return false;
-      if (__any_sync(0xffffffffu, rescale)) {
+      if (owner) {
+        // 1. Full scores of my rows: own partial (TMEM) + the peer's (received).
+        if (lead && warp == 2 * (int)x.rank)
+          ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + sb), kRecvBytes);
+        if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
+        if (!wait_warp(x, x.bar(B_RFULL + sb), (g >> 1) & 1u, true)) return false;
         ptx::tc_fence_after();
-        const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
-#pragma unroll 1
-        for (int ch = 0; ch < 8; ++ch) {
+        float s[64];
+        {
           uint32_t v[32];
-          const uint32_t ta = x.tmem + lane_base + kColO + ch * 32;
-          tmem_load32(ta, v);
+          tmem_load32(x.tmem + lane_base + kColS + sb * 64, v);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-          ptx::tmem_st32(ta, v);
+          for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
+          tmem_load32(x.tmem + lane_base + kColS + sb * 64 + 32, v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(v[k]);
         }
-        ptx::tmem_wait_st();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float4 v =
+              ptx::ld_shared_v4f(recv_row + sb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
+          s[4 * c] += v.x;   // addition commutes: the same sum in either CTA
+          s[4 * c + 1] += v.y;
+          s[4 * c + 2] += v.z;
+          s[4 * c + 3] += v.w;
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+
+        // 2. Mask, row max (the accum_s -> scores_max reduce), exp2, sums.
+        const int tok0 = pg * kPageTokens;
+        if (__any_sync(0xffffffffu, tok0 + kPageTokens > n_valid)) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (tok0 + k >= n_valid) s[k] = -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
+        // Every value read from the receive buffer went into mx: once mx is
+        // computed the reads are complete and the peer may refill the buffer.
+        ptx::consume(mx);
+        __syncwarp();
+        if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_rempty + 8u * sb);
+        const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
+        const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
+        const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
         if (rescale) {
           l_run *= alpha;
           lb_run *= alpha;
-          m_run = m_new;
         }
-      }
-      if (first) m_run = m_new;
-      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-      uint32_t pk[32];
-      float psum = 0.f, pbsum = 0.f;
+        if (rescale || first) m_run = m_new;
+        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+        uint32_t pk[32];
+        float psum = 0.f, pbsum = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float a = ptx::ex2(fmaf(s[2 * j], scale_log2, neg_m));
-        const float c = ptx::ex2(fmaf(s[2 * j + 1], scale_log2, neg_m));
-        psum += a + c;
-        pk[j] = ptx::pack_bf16x2(a, c);
-        pbsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
-      }
-      l_run += psum;
-      lb_run += pbsum;
+        for (int j = 0; j < 32; ++j) {
+          const float a = ptx::ex2(fmaf(s[2 * j], scale_log2, neg_m));
+          const float c = ptx::ex2(fmaf(s[2 * j + 1], scale_log2, neg_m));
+          psum += a + c;
+          pk[j] = ptx::pack_bf16x2(a, c);
+          pbsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
+        }
+        l_run += psum;
+        lb_run += pbsum;
 
-      // Past the end of the sequence the cache slots of the last page hold
-      // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
-      // the P.V MMA, so zero those value rows first.
-      if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
-        const int t0 = L & (kPageTokens - 1);
-        const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
-        const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
-        for (int idx = r; idx < n16; idx += kSoftmaxWarps * 32) {
-          const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
-          ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+        // 3. My P.V of the previous page is done (P buffer free, O stable) and
+        //    the copy of my previous P rows to the peer has read them.
+        if (!wait_warp(x, x.bar(B_PEMPTY), (g & 1u) ^ 1u)) return false;
+        if (!wait_warp(x, x.bar(B_PSENT), (g & 1u) ^ 1u)) return false;
+        if (__any_sync(0xffffffffu, rescale)) {
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t v[32];
+            const uint32_t ta = x.tmem + lane_base + kColO + ch * 32;
+            tmem_load32(ta, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            ptx::tmem_st32(ta, v);
+          }
+          ptx::tmem_wait_st();
+        }
+        // Past the end of the sequence the cache slots of the last page hold
+        // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
+        // the P.V MMA, so zero those value rows first (each CTA zeroes its own
+        // stage, split between its two softmax warps).
+        if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
+          const int t0 = L & (kPageTokens - 1);
+          const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
+          const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
+          for (int idx = hr; idx < n16; idx += kHalfRows) {
+            const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
+            ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
+          }
+        }
+        {
+          // P row r, 128-byte swizzle: 16-byte chunk c at position c ^ (r % 8)
+          const uint32_t prow = x.sbase + kP + (uint32_t)r * 128u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
+                              pk[4 * c + 2], pk[4 * c + 3]);
+          ptx::st_shared_u32(x.sbase + kAlpha + (uint32_t)r * 4u, __float_as_uint(alpha));
         }
         ptx::fence_proxy_async_smem();
-      }
-      {
-        // P row r, 128-byte swizzle: 16-byte chunk c at position c ^ (r % 8)
-        const uint32_t prow = x.sbase + kP + (uint32_t)r * 128u;
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(x.bar(B_PLOCAL));
+          ptx::mbar_arrive(x.bar(B_PFULL));
+        }
+      } else {
+        // Import: once my previous P.V is done, tell the peer it may write
+        // its next P rows into my buffer, then wait for them.
+        if (!wait_warp(x, x.bar(B_PEMPTY), (g & 1u) ^ 1u)) return false;
+        if (warp == 2 * (int)x.peer) {
+          if (lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_PRECV), kPRowsBytes + kAlphaBytes);
+          __syncwarp();
+          // my P.V of page g - 1 has read the peer's rows (its commit was
+          // waited on above): the peer may send page g's
+          if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_pfree);
+        }
+        if (!wait_warp(x, x.bar(B_PRECV), g & 1u, true)) return false;
+        const float alpha =
+            __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + kAlpha + (uint32_t)r * 4u));
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int ch = 0; ch < 8; ++ch) {
+            uint32_t v[32];
+            const uint32_t ta = x.tmem + lane_base + kColO + ch * 32;
+            tmem_load32(ta, v);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
-                            pk[4 * c + 2], pk[4 * c + 3]);
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            ptx::tmem_st32(ta, v);
+          }
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL));
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL));
     }
 
-    // Epilogue: O / l, lse = (m + log2 l) * ln 2.  Split partials go out in a
-    // [slot][dim/4][row][4] layout so a warp's stores are contiguous.
+    // Epilogue: O / l for this CTA's dims of all 128 rows; lse by the row's
+    // owner.  The owners send 1/l of their rows to the peer's importers.
     if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
     ptx::tc_fence_after();
+    const uint32_t par = n_item & 1u;
     const int ns = w.items[b * kItemWords + 1];
     const bool direct = (ns == 1);
-    const float inv_l = lb_run > 0.f ? 1.0f / lb_run : 0.f;
-    const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
     const int sidx = (n_item == 0) ? w.split0 : 0;
     const int64_t slot = (int64_t)w.tile * w.stotal + w.items[b * kItemWords + 2] + sidx;
     const int64_t orow = ((int64_t)b * prm.s_q + i) * prm.h_q + h;
+    float inv_l;
+    if (owner) {
+      inv_l = lb_run > 0.f ? 1.0f / lb_run : 0.f;
+      ptx::st_shared_u32(x.sbase + kInvL + par * 512u + (uint32_t)r * 4u, __float_as_uint(inv_l));
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == kRemoteLane) {
+        // this warp's 32 values of 1/l
+        const uint32_t woff = kInvL + par * 512u + (uint32_t)(warp * 32) * 4u;
+        ptx::bulk_copy_to_peer(ptx::map_to_rank(x.sbase + woff, x.peer), x.sbase + woff, 128u,
+                               peer_lrecv + 8u * par);
+        ptx::bulk_commit();
+        ptx::bulk_wait_read_all();
+      }
+      const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (valid) {
+        if (direct)
+          prm.lse[((int64_t)b * prm.h_q + h) * prm.s_q + i] = lse_v;
+        else
+          prm.ws_lse[slot * kTileRows + r] = lse_v;
+      }
+    } else {
+      if (lead && warp == 2 * (int)x.peer)
+        ptx::mbar_arrive_expect_tx(x.bar(B_LRECV + par), 2u * 128u);
+      if (!wait_warp(x, x.bar(B_LRECV + par), (n_item >> 1) & 1u, true)) return false;
+      inv_l = __uint_as_float(
+          ptx::ld_shared_u32_volatile(x.sbase + kInvL + par * 512u + (uint32_t)r * 4u));
+    }
 #pragma unroll 1
     for (int ch = 0; ch < 8; ++ch) {
       uint32_t v[32];
@@ -652,16 +772,39 @@ __device__ __forceinline__ bool run_softmax(const Ctx& x, const Work& w, const D
         }
       }
     }
-    if (valid && x.rank == 0) {
-      if (direct)
-        prm.lse[((int64_t)b * prm.h_q + h) * prm.s_q + i] = lse_v;
-      else
-        prm.ws_lse[slot * kTileRows + r] = lse_v;
-    }
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(x.bar(B_OEMPTY));
     ++n_item;
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------ P sender
+// One thread: for every page, once this CTA's softmax warps have written
+// their 64 probability rows and rescale factors and the peer's P.V of the
+// previous page is done, copies them into the same place in the peer's shared
+// memory (one TMA bulk copy each, completing on the peer's PRECV barrier).
+__device__ __forceinline__ bool run_psend(const Ctx& x, const Work& w) {
+  const uint32_t poff = kP + x.rank * kPRowsBytes;
+  const uint32_t aoff = kAlpha + x.rank * kAlphaBytes;
+  const uint32_t peer_p = ptx::map_to_rank(x.sbase + poff, x.peer);
+  const uint32_t peer_a = ptx::map_to_rank(x.sbase + aoff, x.peer);
+  const uint32_t peer_precv = ptx::map_to_rank(x.bar(B_PRECV), x.peer);
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0;
+  while (it.next(b, pb, pe)) {
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      if (!wait_bar(x, x.bar(B_PLOCAL), g & 1u)) return false;
+      // phase g of PFREE: the peer's P.V of page g - 1 is done
+      if (!wait_bar(x, x.bar(B_PFREE), g & 1u, true)) return false;
+      ptx::bulk_copy_to_peer(peer_p, x.sbase + poff, kPRowsBytes, peer_precv);
+      ptx::bulk_copy_to_peer(peer_a, x.sbase + aoff, kAlphaBytes, peer_precv);
+      ptx::bulk_commit();
+      ptx::bulk_wait_read_all();
+      ptx::mbar_arrive_relaxed(x.bar(B_PSENT));   // the copies have read the rows
+    }
   }
   return true;
 }
@@ -695,18 +838,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(x.bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(B_SFULL + s), 1);
-      ptx::mbar_init(x.bar(B_SEMPTY + s), 2 * kSoftmaxWarps);   // softmax + exchange warps
+      ptx::mbar_init(x.bar(B_SEMPTY + s), 4);   // 2 softmax + 2 sending warps
+      ptx::mbar_init(x.bar(B_RFULL + s), 1);    // own expect_tx + the peer's bulk-copy bytes
+      ptx::mbar_init(x.bar(B_REMPTY + s), 2);   // the peer's 2 softmax warps (remote)
+      ptx::mbar_init(x.bar(B_LRECV + s), 1);    // own expect_tx + the peer's 1/l bytes
     }
-    ptx::mbar_init(x.bar(B_PFULL), kSoftmaxWarps);
+    ptx::mbar_init(x.bar(B_PFULL), kRowWarps);
     ptx::mbar_init(x.bar(B_PEMPTY), 1);
-    ptx::mbar_init(x.bar(B_XREADY), 4);
+    ptx::mbar_init(x.bar(B_XREADY), 2);
     ptx::mbar_init(x.bar(B_XFREE), 1);
+    ptx::mbar_init(x.bar(B_PRECV), 1);        // own expect_tx + the peer's P bytes
+    ptx::mbar_init(x.bar(B_PFREE), 1);        // the peer's importing warp (remote)
+    ptx::mbar_init(x.bar(B_PLOCAL), 2);
+    ptx::mbar_init(x.bar(B_PSENT), 1);
     ptx::mbar_init(x.bar(B_OFULL), 1);
-    ptx::mbar_init(x.bar(B_OEMPTY), kSoftmaxWarps);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(x.bar(B_RFULL + s), 1);   // own expect_tx + the peer's bulk-copy bytes
-      ptx::mbar_init(x.bar(B_REMPTY + s), kSoftmaxWarps);
-    }
+    ptx::mbar_init(x.bar(B_OEMPTY), kRowWarps);
     ptx::mbar_init(x.bar(B_TEARDOWN), 1);
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
@@ -771,8 +917,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp >= kExchangeWarp0 && warp < kExchangeWarp0 + 4) {
     run_exchange(x, w, prm, warp - kExchangeWarp0, lane);
     __syncwarp();
-  } else if (warp < kSoftmaxWarps) {
-    run_softmax(x, w, prm, warp, lane);
+  } else if (warp == kPSendWarp) {
+    if (lane == 0) run_psend(x, w);
+    __syncwarp();
+  } else if (warp < kRowWarps) {
+    run_rows(x, w, prm, warp, lane);
     __syncwarp();
   }
 

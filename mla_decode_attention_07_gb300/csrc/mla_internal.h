@@ -19,7 +19,7 @@ struct DecodeParams {
   const int32_t* plan;
   void* out;          // bf16 [B, s_q, h_q, 512]
   float* lse;         // fp32 [B, h_q, s_q]
-  float* ws_o;        // fp32 [slots, 128, 512]
+  float* ws_o;        // fp32 [slots][512 / 4][128 rows][4]
   float* ws_lse;      // fp32 [slots, 128]
   int* err;           // device error word
   int batch, s_q, h_q, max_pages, num_pages;

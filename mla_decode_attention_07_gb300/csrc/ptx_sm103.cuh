@@ -81,6 +81,25 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
+// The same without release semantics: it does not wait for this thread's
+// earlier memory operations (remote stores, bulk copies in flight) to become
+// visible across the cluster, which costs a round trip.  Use it only where
+// what the arrive frees was read into registers that are already consumed
+// (so the reads are complete), or was read by the tensor core or a bulk copy
+// whose completion this thread has already waited for.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
+// Local arrive without release semantics, for barriers that only free a
+// buffer whose reads are known to be complete (nothing is published through
+// them).
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Makes the value v an input of an (empty) volatile statement: everything v
+// depends on is computed before any later volatile statement is issued.
+__device__ __forceinline__ void consume(float v) { asm volatile("" ::"f"(v)); }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -101,6 +120,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Blocking test with a time limit: returns when the phase completes (the
+// waiting thread is woken by the barrier) or after about `ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }
@@ -130,6 +162,15 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
   asm volatile(
       "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
       ::"r"(dst), "r"(src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+// Copy `bytes` from global memory into this CTA's shared memory, completing
+// the bytes on a local mbarrier (addresses and size multiples of 16 bytes).
+__device__ __forceinline__ void bulk_load_global(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() {
