@@ -38,10 +38,13 @@
 //    two import the peer's probabilities (and rescale those rows of O).
 //    Warps 4-7 load Q's latent half into TMEM per tile, and the two of them on
 //    the peer's rows ship those rows' partial scores.  Warp 8 is the TMA
-//    producer, warp 9 the MMA issuer and TMEM owner; it polls its barriers
-//    and issues whichever MMA is ready.  One thread of warp 10 ships this
-//    CTA's probability rows to the peer, so the softmax warps go straight on
-//    to the next page.
+//    producer, warp 9 issues the score MMAs and owns TMEM, warp 11 issues
+//    the P.V MMAs.  With two issuing threads a P.V that is ready never waits
+//    behind the issue of a score MMA chain (which stalls while the tensor
+//    pipe's queue is full), and the tensor pipe gets the two kinds
+//    interleaved, which hides much of the per-MMA latency of the dependent
+//    score chain.  One thread of warp 10 ships this CTA's probability rows
+//    to the peer, so the softmax warps go straight on to the next page.
 //  * A thread that has a remote operation in flight (a copy or an arrive on
 //    the peer's barrier) does not also signal the local barriers of the
 //    critical path: a release arrive may wait for that remote operation to
@@ -70,12 +73,13 @@ namespace mla {
 namespace {
 
 // Warp roles (see above).  Warp w reaches TMEM lanes [32 (w % 4), +32).
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kRowWarps = 4;
 constexpr int kExchangeWarp0 = 4;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPSendWarp = 10;
+constexpr int kPvWarp = 11;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after an abort
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
@@ -207,29 +211,6 @@ struct Work {
   const int32_t* items;
 };
 
-// Page-by-page walk of the cluster's work, with the segment (item) index.
-struct Cursor {
-  SegIter it;
-  int b, pb, pe, pg;
-  uint32_t item;
-  bool valid;
-  __device__ __forceinline__ void init(const Work& w) {
-    it = SegIter{w.b0, w.p0, w.b1, w.p1, w.items};
-    item = 0;
-    valid = it.next(b, pb, pe);
-    pg = pb;
-  }
-  __device__ __forceinline__ void advance() {
-    if (++pg >= pe) {
-      valid = it.next(b, pb, pe);
-      pg = pb;
-      ++item;
-    }
-  }
-  __device__ __forceinline__ bool first() const { return pg == pb; }
-  __device__ __forceinline__ bool last() const { return pg == pe - 1; }
-};
-
 // 32 consecutive TMEM columns of this warp's 32 lanes, loaded and waited on
 // in one statement so no use of the registers can be scheduled before the
 // wait.
@@ -325,92 +306,45 @@ __device__ __forceinline__ void issue_pv(const Ctx& x, uint32_t g, bool first) {
   }
 }
 
-__device__ __forceinline__ bool run_mma(const Ctx& x, const Work& w) {
-  Cursor cq, cp;
-  cq.init(w);
-  cp.init(w);
-  uint32_t gq = 0, gp = 0;
-  int q_ok_item = -1, o_ok_item = -1;
-  uint64_t idle_t0 = 0;
-  uint32_t idle = 0;
-  while (cp.valid) {
-    bool progress = false;
-    // The first barrier found not ready, for the idle wait below.
-    uint32_t blk_bar = 0, blk_par = 0;
-    // P.V of the oldest page whose probabilities are ready.
-    if (gp < gq) {
-      bool ok = true;
-      if (cp.first() && (int)cp.item != o_ok_item) {
-        if (ptx::mbar_test_wait(x.bar(B_OEMPTY), (cp.item & 1u) ^ 1u)) {
-          o_ok_item = (int)cp.item;
-        } else {
-          ok = false;
-          blk_bar = x.bar(B_OEMPTY);
-          blk_par = (cp.item & 1u) ^ 1u;
-        }
-      }
-      if (ok && !ptx::mbar_test_wait(x.bar(B_PFULL), gp & 1u)) {
-        ok = false;
-        blk_bar = x.bar(B_PFULL);
-        blk_par = gp & 1u;
-      }
-      if (ok) {
-        ptx::tc_fence_after();
-        issue_pv(x, gp, cp.first());
-        ptx::mma_commit(x.bar(B_EMPTY + gp % kStages));
-        ptx::mma_commit(x.bar(B_PEMPTY));
-        if (cp.last()) ptx::mma_commit(x.bar(B_OFULL));
-        cp.advance();
-        ++gp;
-        progress = true;
-      }
+// Score MMAs, page by page, as soon as the page is loaded, the Q tile is in
+// place and the page's TMEM score tile is free.
+__device__ __forceinline__ bool run_mma_qk(const Ctx& x, const Work& w) {
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0, n_item = 0;
+  while (it.next(b, pb, pe)) {
+    if (!wait_bar(x, x.bar(B_QFULL), n_item & 1u)) return false;
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      if (!wait_bar(x, x.bar(B_FULL + g % kStages), (g / kStages) & 1u)) return false;
+      if (!wait_bar(x, x.bar(B_SEMPTY + (g & 1u)), ((g >> 1) & 1u) ^ 1u)) return false;
+      ptx::tc_fence_after();
+      issue_qk(x, g);
+      ptx::mma_commit(x.bar(B_SFULL + (g & 1u)));
     }
-    // Scores of the next page once it is loaded and its TMEM tile is free.
-    if (cq.valid) {
-      uint32_t bq = 0, pq = 0;
-      if ((int)cq.item != q_ok_item) {
-        if (ptx::mbar_test_wait(x.bar(B_QFULL), cq.item & 1u))
-          q_ok_item = (int)cq.item;
-        else
-          bq = x.bar(B_QFULL), pq = cq.item & 1u;
-      }
-      if (bq == 0u && !ptx::mbar_test_wait(x.bar(B_FULL + gq % kStages), (gq / kStages) & 1u))
-        bq = x.bar(B_FULL + gq % kStages), pq = (gq / kStages) & 1u;
-      if (bq == 0u &&
-          !ptx::mbar_test_wait(x.bar(B_SEMPTY + (gq & 1u)), ((gq >> 1) & 1u) ^ 1u))
-        bq = x.bar(B_SEMPTY + (gq & 1u)), pq = ((gq >> 1) & 1u) ^ 1u;
-      if (bq == 0u) {
-        ptx::tc_fence_after();
-        issue_qk(x, gq);
-        ptx::mma_commit(x.bar(B_SFULL + (gq & 1u)));
-        if (cq.last()) ptx::mma_commit(x.bar(B_QEMPTY));
-        cq.advance();
-        ++gq;
-        progress = true;
-      } else if (blk_bar == 0u) {
-        blk_bar = bq;
-        blk_par = pq;
-      }
+    ptx::mma_commit(x.bar(B_QEMPTY));
+    ++n_item;
+  }
+  return true;
+}
+
+// P.V MMAs, page by page, once the page's probabilities (all 128 rows) are
+// in shared memory; the first page of a tile also waits until the previous
+// tile's output has been read out of TMEM.
+__device__ __forceinline__ bool run_mma_pv(const Ctx& x, const Work& w) {
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0, n_item = 0;
+  while (it.next(b, pb, pe)) {
+    if (!wait_bar(x, x.bar(B_OEMPTY), (n_item & 1u) ^ 1u)) return false;
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      if (!wait_bar(x, x.bar(B_PFULL), g & 1u)) return false;
+      ptx::tc_fence_after();
+      issue_pv(x, g, pg == pb);
+      ptx::mma_commit(x.bar(B_EMPTY + g % kStages));
+      ptx::mma_commit(x.bar(B_PEMPTY));
     }
-    if (progress) {
-      idle = 0;
-      continue;
-    }
-    // Nothing ready: sleep on the first barrier that blocked (the oldest MMA
-    // still to issue comes first).  The thread is woken as soon as that phase
-    // completes, or after a short limit so the other kind is polled too, and
-    // takes no issue slots from the softmax warp on this scheduler meanwhile.
-    // The wait as a whole stays bounded.
-    if (blk_bar != 0u) ptx::mbar_try_wait_for(blk_bar, blk_par, 200u);
-    if ((++idle & 63u) == 0u) {
-      if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) return false;
-      const uint64_t now = ptx::globaltimer();
-      if (idle == 64u) idle_t0 = now;
-      if (now - idle_t0 > kWaitTimeoutNs) {
-        abort_all(x);
-        return false;
-      }
-    }
+    ptx::mma_commit(x.bar(B_OFULL));
+    ++n_item;
   }
   return true;
 }
@@ -853,7 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(x.bar(B_PSENT), 1);
     ptx::mbar_init(x.bar(B_OFULL), 1);
     ptx::mbar_init(x.bar(B_OEMPTY), kRowWarps);
-    ptx::mbar_init(x.bar(B_TEARDOWN), 1);
+    ptx::mbar_init(x.bar(B_TEARDOWN), 2);   // both MMA-issuing threads
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
   }
@@ -912,7 +846,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma(x, w);
+    if (lane == 0) run_mma_qk(x, w);
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    if (lane == 0) run_mma_pv(x, w);
     __syncwarp();
   } else if (warp >= kExchangeWarp0 && warp < kExchangeWarp0 + 4) {
     run_exchange(x, w, prm, warp - kExchangeWarp0, lane);
@@ -928,7 +865,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Teardown.  After an abort, give in-flight copies and MMAs time to land
   // before the shared memory and TMEM are released.
   const bool aborted = ptx::ld_shared_u32_volatile(x.abort_addr) != 0u;
-  if (warp == kMmaWarp && lane == 0) {
+  if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
+    // each issuing thread's MMAs are done
     ptx::mma_commit(x.bar(B_TEARDOWN));
     const uint64_t t0 = ptx::globaltimer();
     while (!ptx::mbar_try_wait(x.bar(B_TEARDOWN), 0u)) {
