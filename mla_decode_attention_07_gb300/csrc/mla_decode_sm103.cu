@@ -101,11 +101,10 @@ constexpr uint32_t kStageBytes = 36864;
 constexpr uint32_t kStageRope = 32768;    // rotary box inside a stage
 constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][64 rows] x 16 B
 constexpr uint32_t kRecvBytes = kHalfRows * 64 * 4;
-constexpr uint32_t kXStage = kRecv + 2 * kRecvBytes;        // [16 chunks][64 rows] x 16 B
-constexpr uint32_t kP = kXStage + kRecvBytes;                // [128 x 64] bf16, 128-byte swizzle
+constexpr uint32_t kP = kRecv + 2 * kRecvBytes;  // 2 x [128 x 64] bf16, 128-byte swizzle
 constexpr uint32_t kPBytes = 128 * 64 * 2;
-constexpr uint32_t kAlpha = kP + kPBytes;                    // float[128] rescale factors
-constexpr uint32_t kInvL = kAlpha + 128 * 4;                 // float[2][128] 1/l per tile parity
+constexpr uint32_t kAlpha = kP + 2 * kPBytes;                // float[2][128] rescale factors
+constexpr uint32_t kInvL = kAlpha + 2 * 128 * 4;             // float[2][128] 1/l per tile parity
 constexpr uint32_t kBar = kInvL + 2 * 128 * 4;
 constexpr uint32_t kMisc = kBar + 8 * 40;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
@@ -118,6 +117,7 @@ constexpr uint32_t kQRopeTx = 8192;
 constexpr uint32_t kPRowsBytes = kHalfRows * 128;    // one CTA's 64 rows of P
 constexpr uint32_t kAlphaBytes = kHalfRows * 4;
 
+// [2] = one per buffer: page g uses score tile, receive buffer and P buffer g % 2.
 enum Bar : uint32_t {
   B_FULL = 0,       // [4] stage loaded (TMA tx)
   B_EMPTY = 4,      // [4] stage consumed (MMA commit)
@@ -125,20 +125,18 @@ enum Bar : uint32_t {
   B_QEMPTY = 9,     // last score MMA of a tile done
   B_SFULL = 10,     // [2] score tile ready (MMA commit)
   B_SEMPTY = 12,    // [2] score tile read (2 softmax warps + 2 sending warps)
-  B_PFULL = 14,     // all 128 rows of P in shared memory and O rescaled (4 row warps)
-  B_PEMPTY = 15,    // P.V done (MMA commit)
-  B_OFULL = 16,
-  B_OEMPTY = 17,    // 4 row warps
-  B_RFULL = 18,     // [2] the peer's partial scores for my rows (bulk-copy tx)
-  B_REMPTY = 20,    // [2] the peer's softmax warps have read what I sent (2 remote arrives)
-  B_XREADY = 22,    // staging written (2 sending warps)
-  B_XFREE = 23,     // staging read by the bulk copy
-  B_PRECV = 24,     // the peer's P rows and rescale factors arrived (bulk-copy tx)
-  B_PFREE = 25,     // the peer's P buffer may take my next rows (peer's P.V done)
-  B_PLOCAL = 26,    // my 2 softmax warps wrote their P rows
-  B_PSENT = 27,     // my P rows have been read by the bulk copy to the peer (P sender)
-  B_LRECV = 28,     // [2] the peer's 1/l for its rows arrived (per tile parity)
-  B_TEARDOWN = 30,
+  B_PFULL = 14,     // [2] all 128 rows of P in shared memory and O rescaled (4 row warps)
+  B_PEMPTY = 16,    // [2] P.V done (MMA commit)
+  B_OFULL = 18,
+  B_OEMPTY = 19,    // 4 row warps
+  B_RFULL = 20,     // [2] the peer's partial scores for my rows (st.async tx)
+  B_REMPTY = 22,    // [2] the peer's softmax warps have read what I sent (2 remote arrives)
+  B_PRECV = 24,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
+  B_PFREE = 26,     // [2] the peer's P buffer may take my next rows (peer's P.V done)
+  B_PLOCAL = 28,    // [2] my 2 softmax warps wrote their P rows
+  B_PSENT = 30,     // [2] my P rows have been read by the bulk copy to the peer (P sender)
+  B_LRECV = 32,     // [2] the peer's 1/l for its rows arrived (per tile parity)
+  B_TEARDOWN = 34,
 };
 
 struct Ctx {
@@ -301,7 +299,8 @@ __device__ __forceinline__ void issue_pv(const Ctx& x, uint32_t g, bool first) {
     // V as the MN-major B operand: 64-dim swizzle atoms 8 KB apart along N,
     // 8-token row groups 1 KB apart along K; 16 tokens per K-step.
     const uint64_t bdesc = ptx::smem_desc(vbase + k * 2048, 8192, 1024, ptx::kLayoutSw128);
-    const uint64_t adesc = ptx::smem_desc(x.sbase + kP + k * 32, 16, 1024, ptx::kLayoutSw128);
+    const uint64_t adesc = ptx::smem_desc(x.sbase + kP + (g & 1u) * kPBytes + k * 32, 16, 1024,
+                                          ptx::kLayoutSw128);
     ptx::mma_ss(x.tmem + kColO, adesc, bdesc, id_pv, (first && k == 0) ? 0u : 1u);
   }
 }
@@ -337,11 +336,11 @@ __device__ __forceinline__ bool run_mma_pv(const Ctx& x, const Work& w) {
   while (it.next(b, pb, pe)) {
     if (!wait_bar(x, x.bar(B_OEMPTY), (n_item & 1u) ^ 1u)) return false;
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      if (!wait_bar(x, x.bar(B_PFULL), g & 1u)) return false;
+      if (!wait_bar(x, x.bar(B_PFULL + (g & 1u)), (g >> 1) & 1u)) return false;
       ptx::tc_fence_after();
       issue_pv(x, g, pg == pb);
       ptx::mma_commit(x.bar(B_EMPTY + g % kStages));
-      ptx::mma_commit(x.bar(B_PEMPTY));
+      ptx::mma_commit(x.bar(B_PEMPTY + (g & 1u)));
     }
     ptx::mma_commit(x.bar(B_OFULL));
     ++n_item;
@@ -353,20 +352,19 @@ __device__ __forceinline__ bool run_mma_pv(const Ctx& x, const Work& w) {
 // Warps 4-7 put the latent half of each Q tile into TMEM (one row per
 // thread).  The two of them whose lanes are the peer's softmax rows then ship
 // those rows' partial scores of every page to the peer, as soon as the score
-// MMA has written them: staged in local shared memory as [16-byte chunk c]
-// [row] and moved by one TMA bulk copy (shared::cta -> shared::cluster) into
-// the peer's receive buffer g % 2, completing the bytes on the peer's
-// barrier; the receiving side posts the expected byte count itself.
+// MMA has written them: copied out of TMEM into registers (which frees the
+// score tile) and stored with st.async straight into the peer's receive
+// buffer g % 2 as [16-byte chunk c][row], so a warp's store covers 512
+// contiguous bytes; each store completes its bytes on the peer's barrier,
+// where the receiving side has posted the expected count.
 __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const DecodeParams& prm,
                                              int e, int lane) {
   const int r = e * 32 + lane;
   const uint32_t lane_base = (uint32_t)(e * 32) << 16;
   const bool sender = (uint32_t)(e >> 1) != x.rank;   // lanes of the peer's rows
-  // The copy is issued by a lane that signals no local barrier.
-  const bool issuer = sender && (e & 1) == 0 && lane == kRemoteLane;
-  const uint32_t peer_recv = ptx::map_to_rank(x.sbase + kRecv, x.peer);
+  const uint32_t peer_row = ptx::map_to_rank(x.sbase + kRecv, x.peer) +
+                            (uint32_t)(r & (kHalfRows - 1)) * 16u;
   const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
-  const uint32_t stage_row = x.sbase + kXStage + (uint32_t)(r & (kHalfRows - 1)) * 16u;
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
@@ -411,38 +409,22 @@ __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const 
       const uint32_t sb = g & 1u;
       if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
       ptx::tc_fence_after();
-      // the peer has read what was sent into this buffer two pages ago, and
-      // the staging buffer is free again
-      if (!wait_warp(x, x.bar(B_REMPTY + sb), ((g >> 1) & 1u) ^ 1u, true)) return false;
-      if (!wait_warp(x, x.bar(B_XFREE), (g & 1u) ^ 1u)) return false;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_load32(x.tmem + lane_base + kColS + sb * 64 + half * 32, v);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          ptx::st_shared_v4(stage_row + (uint32_t)(half * 8 + c) * (kHalfRows * 16), v[4 * c],
-                            v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      }
-      ptx::fence_proxy_async_smem();
+      uint32_t v[2][32];
+      tmem_load32(x.tmem + lane_base + kColS + sb * 64, v[0]);
+      tmem_load32(x.tmem + lane_base + kColS + sb * 64 + 32, v[1]);
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(x.bar(B_XREADY));
-        ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
-      }
-      bool ok = true;
-      if (issuer) {
-        ok = wait_bar(x, x.bar(B_XREADY), g & 1u);
-        if (ok) {
-          ptx::bulk_copy_to_peer(peer_recv + sb * kRecvBytes, x.sbase + kXStage, kRecvBytes,
-                                 peer_rfull + 8u * sb);
-          ptx::bulk_commit();
-          ptx::bulk_wait_read_all();
-          ptx::mbar_arrive_relaxed(x.bar(B_XFREE));   // the copy has read the staging
-        }
-      }
-      if (!__all_sync(0xffffffffu, ok)) return false;
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+      // the peer has read what was sent into this buffer two pages ago
+      if (!wait_warp(x, x.bar(B_REMPTY + sb), ((g >> 1) & 1u) ^ 1u, true)) return false;
+#pragma unroll
+      for (int half = 0; half < 2; ++half)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          ptx::st_async_v4(peer_row + sb * kRecvBytes + (uint32_t)(half * 8 + c) * (kHalfRows * 16),
+                           __uint_as_float(v[half][4 * c]), __uint_as_float(v[half][4 * c + 1]),
+                           __uint_as_float(v[half][4 * c + 2]), __uint_as_float(v[half][4 * c + 3]),
+                           peer_rfull + 8u * sb);
     }
     ++n_item;
   }
@@ -554,11 +536,13 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         l_run += psum;
         lb_run += pbsum;
 
-        // 3. My P.V of the previous page is done (P buffer free, O stable) and
-        //    the copy of my previous P rows to the peer has read them.
-        if (!wait_warp(x, x.bar(B_PEMPTY), (g & 1u) ^ 1u)) return false;
-        if (!wait_warp(x, x.bar(B_PSENT), (g & 1u) ^ 1u)) return false;
+        // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
+        //    of my rows of page g - 2 to the peer has read them.  A rescale
+        //    of O also needs the P.V of page g - 1 done.
+        if (!wait_warp(x, x.bar(B_PEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
+        if (!wait_warp(x, x.bar(B_PSENT + sb), ((g >> 1) & 1u) ^ 1u)) return false;
         if (__any_sync(0xffffffffu, rescale)) {
+          if (!wait_warp(x, x.bar(B_PEMPTY + (sb ^ 1u)), ((g - 1) >> 1) & 1u)) return false;
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 8; ++ch) {
@@ -586,35 +570,39 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         }
         {
           // P row r, 128-byte swizzle: 16-byte chunk c at position c ^ (r % 8)
-          const uint32_t prow = x.sbase + kP + (uint32_t)r * 128u;
+          const uint32_t prow = x.sbase + kP + sb * kPBytes + (uint32_t)r * 128u;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
                               pk[4 * c + 2], pk[4 * c + 3]);
-          ptx::st_shared_u32(x.sbase + kAlpha + (uint32_t)r * 4u, __float_as_uint(alpha));
+          ptx::st_shared_u32(x.sbase + kAlpha + sb * 512u + (uint32_t)r * 4u,
+                             __float_as_uint(alpha));
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive(x.bar(B_PLOCAL));
-          ptx::mbar_arrive(x.bar(B_PFULL));
+          ptx::mbar_arrive(x.bar(B_PLOCAL + sb));
+          ptx::mbar_arrive(x.bar(B_PFULL + sb));
         }
       } else {
-        // Import: once my previous P.V is done, tell the peer it may write
-        // its next P rows into my buffer, then wait for them.
-        if (!wait_warp(x, x.bar(B_PEMPTY), (g & 1u) ^ 1u)) return false;
+        // Import: once my P.V of page g - 2 is done, tell the peer it may
+        // write its rows of page g into my P buffer g % 2, then wait for them.
+        if (!wait_warp(x, x.bar(B_PEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
         if (warp == 2 * (int)x.peer) {
-          if (lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_PRECV), kPRowsBytes + kAlphaBytes);
+          if (lane == 0)
+            ptx::mbar_arrive_expect_tx(x.bar(B_PRECV + sb), kPRowsBytes + kAlphaBytes);
           __syncwarp();
-          // my P.V of page g - 1 has read the peer's rows (its commit was
+          // my P.V of page g - 2 has read the peer's rows (its commit was
           // waited on above): the peer may send page g's
-          if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_pfree);
+          if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_pfree + 8u * sb);
         }
-        if (!wait_warp(x, x.bar(B_PRECV), g & 1u, true)) return false;
-        const float alpha =
-            __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + kAlpha + (uint32_t)r * 4u));
+        if (!wait_warp(x, x.bar(B_PRECV + sb), (g >> 1) & 1u, true)) return false;
+        const float alpha = __uint_as_float(
+            ptx::ld_shared_u32_volatile(x.sbase + kAlpha + sb * 512u + (uint32_t)r * 4u));
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          // a rescale of O needs the P.V of page g - 1 done
+          if (!wait_warp(x, x.bar(B_PEMPTY + (sb ^ 1u)), ((g - 1) >> 1) & 1u)) return false;
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 8; ++ch) {
@@ -629,7 +617,7 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL));
+        if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + sb));
       }
     }
 
@@ -730,14 +718,17 @@ __device__ __forceinline__ bool run_psend(const Ctx& x, const Work& w) {
   uint32_t g = 0;
   while (it.next(b, pb, pe)) {
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      if (!wait_bar(x, x.bar(B_PLOCAL), g & 1u)) return false;
-      // phase g of PFREE: the peer's P.V of page g - 1 is done
-      if (!wait_bar(x, x.bar(B_PFREE), g & 1u, true)) return false;
-      ptx::bulk_copy_to_peer(peer_p, x.sbase + poff, kPRowsBytes, peer_precv);
-      ptx::bulk_copy_to_peer(peer_a, x.sbase + aoff, kAlphaBytes, peer_precv);
+      const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+      if (!wait_bar(x, x.bar(B_PLOCAL + sb), ph)) return false;
+      // the peer's P.V of page g - 2 is done: its buffer g % 2 is free
+      if (!wait_bar(x, x.bar(B_PFREE + sb), ph, true)) return false;
+      ptx::bulk_copy_to_peer(peer_p + sb * kPBytes, x.sbase + poff + sb * kPBytes, kPRowsBytes,
+                             peer_precv + 8u * sb);
+      ptx::bulk_copy_to_peer(peer_a + sb * 512u, x.sbase + aoff + sb * 512u, kAlphaBytes,
+                             peer_precv + 8u * sb);
       ptx::bulk_commit();
       ptx::bulk_wait_read_all();
-      ptx::mbar_arrive_relaxed(x.bar(B_PSENT));   // the copies have read the rows
+      ptx::mbar_arrive_relaxed(x.bar(B_PSENT + sb));   // the copies have read the rows
     }
   }
   return true;
@@ -773,18 +764,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(B_SFULL + s), 1);
       ptx::mbar_init(x.bar(B_SEMPTY + s), 4);   // 2 softmax + 2 sending warps
-      ptx::mbar_init(x.bar(B_RFULL + s), 1);    // own expect_tx + the peer's bulk-copy bytes
+      ptx::mbar_init(x.bar(B_RFULL + s), 1);    // own expect_tx + the peer's st.async bytes
       ptx::mbar_init(x.bar(B_REMPTY + s), 2);   // the peer's 2 softmax warps (remote)
       ptx::mbar_init(x.bar(B_LRECV + s), 1);    // own expect_tx + the peer's 1/l bytes
+      ptx::mbar_init(x.bar(B_PFULL + s), kRowWarps);
+      ptx::mbar_init(x.bar(B_PEMPTY + s), 1);
+      ptx::mbar_init(x.bar(B_PRECV + s), 1);    // own expect_tx + the peer's P bytes
+      ptx::mbar_init(x.bar(B_PFREE + s), 1);    // the peer's importing warp (remote)
+      ptx::mbar_init(x.bar(B_PLOCAL + s), 2);
+      ptx::mbar_init(x.bar(B_PSENT + s), 1);
     }
-    ptx::mbar_init(x.bar(B_PFULL), kRowWarps);
-    ptx::mbar_init(x.bar(B_PEMPTY), 1);
-    ptx::mbar_init(x.bar(B_XREADY), 2);
-    ptx::mbar_init(x.bar(B_XFREE), 1);
-    ptx::mbar_init(x.bar(B_PRECV), 1);        // own expect_tx + the peer's P bytes
-    ptx::mbar_init(x.bar(B_PFREE), 1);        // the peer's importing warp (remote)
-    ptx::mbar_init(x.bar(B_PLOCAL), 2);
-    ptx::mbar_init(x.bar(B_PSENT), 1);
     ptx::mbar_init(x.bar(B_OFULL), 1);
     ptx::mbar_init(x.bar(B_OEMPTY), kRowWarps);
     ptx::mbar_init(x.bar(B_TEARDOWN), 2);   // both MMA-issuing threads
