@@ -488,12 +488,13 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         }
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
+          // addition commutes: the same sums in either CTA
           const float4 v =
               ptx::ld_shared_v4f(recv_row + sb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
-          s[4 * c] += v.x;   // addition commutes: the same sum in either CTA
-          s[4 * c + 1] += v.y;
-          s[4 * c + 2] += v.z;
-          s[4 * c + 3] += v.w;
+          ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(v.x, v.y)),
+                         s[4 * c], s[4 * c + 1]);
+          ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(v.z, v.w)),
+                         s[4 * c + 2], s[4 * c + 3]);
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -506,9 +507,16 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
           for (int k = 0; k < 64; ++k)
             if (tok0 + k >= n_valid) s[k] = -INFINITY;
         }
-        float mx = s[0];
+        // four independent max chains of 3-input maxima
+        float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int k = 1; k < 64; ++k) mx = fmaxf(mx, s[k]);
+        for (int k = 4; k < 64; k += 8) {
+          m4[0] = ptx::max3(m4[0], s[k], s[k + 1]);
+          m4[1] = ptx::max3(m4[1], s[k + 2], s[k + 3]);
+          m4[2] = ptx::max3(m4[2], s[k + 4], s[k + 5]);
+          m4[3] = ptx::max3(m4[3], s[k + 6], s[k + 7]);
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         // Every value read from the receive buffer went into mx: once mx is
         // computed the reads are complete and the peer may refill the buffer.
         ptx::consume(mx);
@@ -523,18 +531,27 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         }
         if (rescale || first) m_run = m_new;
         const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+        // exp2(s * scale - m) on pairs: the fma and the sums are f32x2 ops, and
+        // the sums run as two independent chains
         uint32_t pk[32];
-        float psum = 0.f, pbsum = 0.f;
+        const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
+        const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+        uint64_t ps2[2] = {0ull, 0ull}, pb2[2] = {0ull, 0ull};
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float a = ptx::ex2(fmaf(s[2 * j], scale_log2, neg_m));
-          const float c = ptx::ex2(fmaf(s[2 * j + 1], scale_log2, neg_m));
-          psum += a + c;
+          float xa, xc;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * j], s[2 * j + 1]), sc2, nm2), xa, xc);
+          const float a = ptx::ex2(xa), c = ptx::ex2(xc);
+          ps2[j & 1] = ptx::f2_add(ps2[j & 1], ptx::f2_pack(a, c));
           pk[j] = ptx::pack_bf16x2(a, c);
-          pbsum += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
+          pb2[j & 1] = ptx::f2_add(pb2[j & 1], ptx::f2_pack(__uint_as_float(pk[j] << 16),
+                                                            __uint_as_float(pk[j] & 0xffff0000u)));
         }
-        l_run += psum;
-        lb_run += pbsum;
+        float pa, pc, ba, bc;
+        ptx::f2_unpack(ptx::f2_add(ps2[0], ps2[1]), pa, pc);
+        ptx::f2_unpack(ptx::f2_add(pb2[0], pb2[1]), ba, bc);
+        l_run += pa + pc;
+        lb_run += ba + bc;
 
         // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
         //    of my rows of page g - 2 to the peer has read them.  A rescale
