@@ -229,11 +229,11 @@ void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clus
 // The decode kernel stores partials as [slot][dim/4][row][4] fp32, so the 4
 // dim groups (16 dims) x 128 rows that one CTA merges are 8 KB contiguous per
 // split: one thread moves all of a job's splits into shared memory with TMA
-// bulk copies (up to kCombineChunk splits, 64 KB, in flight at once), then
+// bulk copies (up to kCombineChunk splits, 48 KB, in flight at once), then
 // 256 threads (one per row and pair of dim groups) merge them.  The merge
 // weights come straight from the per-split lse values.
 constexpr int kCombineQuads = 4;                                        // dim groups per job
-constexpr int kCombineChunk = 8;                                        // splits per pass
+constexpr int kCombineChunk = 6;   // splits per pass; 48 KB, so four jobs fit on an SM
 constexpr uint32_t kCombineSplitBytes = kCombineQuads * kTileRows * 16;  // 8 KB
 constexpr uint32_t kCombineSmem = kCombineChunk * kCombineSplitBytes + 64;
 constexpr uint64_t kCombineWaitNs = 2000000000ull;
@@ -677,7 +677,7 @@ cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_
                            cudaStream_t stream) {
   const int tiles = plan_tiles(p.s_q, p.h_q);
   const int64_t jobs = (int64_t)p.batch * tiles * ((kDv / 4) / kCombineQuads);
-  const int64_t cap = (int64_t)num_sms * 3;
+  const int64_t cap = (int64_t)num_sms * 4;
   const int grid = (int)(jobs < cap ? jobs : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
