@@ -95,16 +95,22 @@ constexpr uint32_t kColQ = 384;   // Q's latent half, bf16x2: 128 rows x 256 dim
 
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kStages = 4;
+// Receive buffers for the peer's partial scores and P buffers: page g uses
+// buffer g % k.  Two of each measured no faster than one (the score tiles in
+// TMEM are double buffered, which is what lets the next page's scores run
+// under this page's softmax), so one of each leaves the shared memory free.
+constexpr int kRBufs = 1;
+constexpr int kPBufs = 1;
 constexpr uint32_t kQRope = 0;            // [128 x 32] bf16, 64-byte swizzle
 constexpr uint32_t kStage0 = 8192;        // kStages x 36 KB
 constexpr uint32_t kStageBytes = 36864;
 constexpr uint32_t kStageRope = 32768;    // rotary box inside a stage
 constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][64 rows] x 16 B
 constexpr uint32_t kRecvBytes = kHalfRows * 64 * 4;
-constexpr uint32_t kP = kRecv + 2 * kRecvBytes;  // 2 x [128 x 64] bf16, 128-byte swizzle
+constexpr uint32_t kP = kRecv + kRBufs * kRecvBytes;  // kPBufs x [128 x 64] bf16, 128-byte swizzle
 constexpr uint32_t kPBytes = 128 * 64 * 2;
-constexpr uint32_t kAlpha = kP + 2 * kPBytes;                // float[2][128] rescale factors
-constexpr uint32_t kInvL = kAlpha + 2 * 128 * 4;             // float[2][128] 1/l per tile parity
+constexpr uint32_t kAlpha = kP + kPBufs * kPBytes;           // float[kPBufs][128] rescale factors
+constexpr uint32_t kInvL = kAlpha + kPBufs * 128 * 4;        // float[2][128] 1/l per tile parity
 constexpr uint32_t kBar = kInvL + 2 * 128 * 4;
 constexpr uint32_t kMisc = kBar + 8 * 40;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
@@ -117,27 +123,30 @@ constexpr uint32_t kQRopeTx = 8192;
 constexpr uint32_t kPRowsBytes = kHalfRows * 128;    // one CTA's 64 rows of P
 constexpr uint32_t kAlphaBytes = kHalfRows * 4;
 
-// [2] = one per buffer: page g uses score tile, receive buffer and P buffer g % 2.
+// [2] = one per buffer: page g uses score tile g % 2, receive buffer
+// g % kRBufs and P buffer g % kPBufs.
 enum Bar : uint32_t {
-  B_FULL = 0,       // [4] stage loaded (TMA tx)
-  B_EMPTY = 4,      // [4] stage consumed (MMA commit)
-  B_QFULL = 8,      // Q tile ready: rotary half (TMA) + latent half (4 exchange warps)
-  B_QEMPTY = 9,     // last score MMA of a tile done
-  B_SFULL = 10,     // [2] score tile ready (MMA commit)
-  B_SEMPTY = 12,    // [2] score tile read (2 softmax warps + 2 sending warps)
-  B_PFULL = 14,     // [2] all 128 rows of P in shared memory and O rescaled (4 row warps)
-  B_PEMPTY = 16,    // [2] P.V done (MMA commit)
-  B_OFULL = 18,
-  B_OEMPTY = 19,    // 4 row warps
-  B_RFULL = 20,     // [2] the peer's partial scores for my rows (st.async tx)
-  B_REMPTY = 22,    // [2] the peer's softmax warps have read what I sent (2 remote arrives)
-  B_PRECV = 24,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
-  B_PFREE = 26,     // [2] the peer's P buffer may take my next rows (peer's P.V done)
-  B_PLOCAL = 28,    // [2] my 2 softmax warps wrote their P rows
-  B_PSENT = 30,     // [2] my P rows have been read by the bulk copy to the peer (P sender)
-  B_LRECV = 32,     // [2] the peer's 1/l for its rows arrived (per tile parity)
-  B_TEARDOWN = 34,
+  B_FULL = 0,                 // [kStages] stage loaded (TMA tx)
+  B_EMPTY = kStages,          // [kStages] stage consumed (MMA commit)
+  B_QFULL = 2 * kStages,      // Q tile ready: rotary half (TMA) + latent half (4 exchange warps)
+  B_QEMPTY,                   // last score MMA of a tile done
+  B_SFULL,                    // [2] score tile ready (MMA commit)
+  B_SEMPTY = B_SFULL + 2,     // [2] score tile read (2 softmax warps + 2 sending warps)
+  B_PFULL = B_SEMPTY + 2,     // [2] all 128 rows of P in shared memory and O rescaled (4 row warps)
+  B_PEMPTY = B_PFULL + 2,     // [2] P.V done (MMA commit)
+  B_OFULL = B_PEMPTY + 2,
+  B_OEMPTY,                   // 4 row warps
+  B_RFULL,                    // [2] the peer's partial scores for my rows (st.async tx)
+  B_REMPTY = B_RFULL + 2,     // [2] the peer's softmax warps have read what I sent (2 remote arrives)
+  B_PRECV = B_REMPTY + 2,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
+  B_PFREE = B_PRECV + 2,      // [2] the peer's P buffer may take my next rows (peer's P.V done)
+  B_PLOCAL = B_PFREE + 2,     // [2] my 2 softmax warps wrote their P rows
+  B_PSENT = B_PLOCAL + 2,     // [2] my P rows have been read by the bulk copy to the peer (P sender)
+  B_LRECV = B_PSENT + 2,      // [2] the peer's 1/l for its rows arrived (per tile parity)
+  B_TEARDOWN = B_LRECV + 2,
+  B_COUNT,
 };
+static_assert(B_COUNT <= 40, "barrier space");
 
 struct Ctx {
   uint32_t sbase;       // 1024-aligned shared base
@@ -299,7 +308,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& x, uint32_t g, bool first) {
     // V as the MN-major B operand: 64-dim swizzle atoms 8 KB apart along N,
     // 8-token row groups 1 KB apart along K; 16 tokens per K-step.
     const uint64_t bdesc = ptx::smem_desc(vbase + k * 2048, 8192, 1024, ptx::kLayoutSw128);
-    const uint64_t adesc = ptx::smem_desc(x.sbase + kP + (g & 1u) * kPBytes + k * 32, 16, 1024,
+    const uint64_t adesc = ptx::smem_desc(x.sbase + kP + (g % kPBufs) * kPBytes + k * 32, 16, 1024,
                                           ptx::kLayoutSw128);
     ptx::mma_ss(x.tmem + kColO, adesc, bdesc, id_pv, (first && k == 0) ? 0u : 1u);
   }
@@ -336,11 +345,11 @@ __device__ __forceinline__ bool run_mma_pv(const Ctx& x, const Work& w) {
   while (it.next(b, pb, pe)) {
     if (!wait_bar(x, x.bar(B_OEMPTY), (n_item & 1u) ^ 1u)) return false;
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      if (!wait_bar(x, x.bar(B_PFULL + (g & 1u)), (g >> 1) & 1u)) return false;
+      if (!wait_bar(x, x.bar(B_PFULL + g % kPBufs), (g / kPBufs) & 1u)) return false;
       ptx::tc_fence_after();
       issue_pv(x, g, pg == pb);
       ptx::mma_commit(x.bar(B_EMPTY + g % kStages));
-      ptx::mma_commit(x.bar(B_PEMPTY + (g & 1u)));
+      ptx::mma_commit(x.bar(B_PEMPTY + g % kPBufs));
     }
     ptx::mma_commit(x.bar(B_OFULL));
     ++n_item;
@@ -416,15 +425,16 @@ __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const 
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
       // the peer has read what was sent into this buffer two pages ago
-      if (!wait_warp(x, x.bar(B_REMPTY + sb), ((g >> 1) & 1u) ^ 1u, true)) return false;
+      const uint32_t rb = g % kRBufs;
+      if (!wait_warp(x, x.bar(B_REMPTY + rb), ((g / kRBufs) & 1u) ^ 1u, true)) return false;
 #pragma unroll
       for (int half = 0; half < 2; ++half)
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          ptx::st_async_v4(peer_row + sb * kRecvBytes + (uint32_t)(half * 8 + c) * (kHalfRows * 16),
+          ptx::st_async_v4(peer_row + rb * kRecvBytes + (uint32_t)(half * 8 + c) * (kHalfRows * 16),
                            __uint_as_float(v[half][4 * c]), __uint_as_float(v[half][4 * c + 1]),
                            __uint_as_float(v[half][4 * c + 2]), __uint_as_float(v[half][4 * c + 3]),
-                           peer_rfull + 8u * sb);
+                           peer_rfull + 8u * rb);
     }
     ++n_item;
   }
@@ -468,13 +478,15 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
 
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const bool first = (pg == pb);
-      const uint32_t sb = g & 1u;
+      const uint32_t sb = g & 1u;             // score tile
+      const uint32_t rb = g % kRBufs;         // receive buffer
+      const uint32_t pbuf = g % kPBufs;       // P buffer
       if (owner) {
         // 1. Full scores of my rows: own partial (TMEM) + the peer's (received).
         if (lead && warp == 2 * (int)x.rank)
-          ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + sb), kRecvBytes);
+          ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + rb), kRecvBytes);
         if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
-        if (!wait_warp(x, x.bar(B_RFULL + sb), (g >> 1) & 1u, true)) return false;
+        if (!wait_warp(x, x.bar(B_RFULL + rb), (g / kRBufs) & 1u, true)) return false;
         ptx::tc_fence_after();
         float s[64];
         {
@@ -490,7 +502,7 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         for (int c = 0; c < 16; ++c) {
           // addition commutes: the same sums in either CTA
           const float4 v =
-              ptx::ld_shared_v4f(recv_row + sb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
+              ptx::ld_shared_v4f(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
           ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(v.x, v.y)),
                          s[4 * c], s[4 * c + 1]);
           ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(v.z, v.w)),
@@ -521,7 +533,7 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         // computed the reads are complete and the peer may refill the buffer.
         ptx::consume(mx);
         __syncwarp();
-        if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_rempty + 8u * sb);
+        if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_rempty + 8u * rb);
         const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
         const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
         const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
@@ -556,10 +568,12 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
         //    of my rows of page g - 2 to the peer has read them.  A rescale
         //    of O also needs the P.V of page g - 1 done.
-        if (!wait_warp(x, x.bar(B_PEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
-        if (!wait_warp(x, x.bar(B_PSENT + sb), ((g >> 1) & 1u) ^ 1u)) return false;
+        if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
+        if (!wait_warp(x, x.bar(B_PSENT + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
         if (__any_sync(0xffffffffu, rescale)) {
-          if (!wait_warp(x, x.bar(B_PEMPTY + (sb ^ 1u)), ((g - 1) >> 1) & 1u)) return false;
+          if (kPBufs > 1 &&
+              !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
+            return false;
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 8; ++ch) {
@@ -587,39 +601,41 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         }
         {
           // P row r, 128-byte swizzle: 16-byte chunk c at position c ^ (r % 8)
-          const uint32_t prow = x.sbase + kP + sb * kPBytes + (uint32_t)r * 128u;
+          const uint32_t prow = x.sbase + kP + pbuf * kPBytes + (uint32_t)r * 128u;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
                               pk[4 * c + 2], pk[4 * c + 3]);
-          ptx::st_shared_u32(x.sbase + kAlpha + sb * 512u + (uint32_t)r * 4u,
+          ptx::st_shared_u32(x.sbase + kAlpha + pbuf * 512u + (uint32_t)r * 4u,
                              __float_as_uint(alpha));
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          ptx::mbar_arrive(x.bar(B_PLOCAL + sb));
-          ptx::mbar_arrive(x.bar(B_PFULL + sb));
+          ptx::mbar_arrive(x.bar(B_PLOCAL + pbuf));
+          ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
         }
       } else {
         // Import: once my P.V of page g - 2 is done, tell the peer it may
         // write its rows of page g into my P buffer g % 2, then wait for them.
-        if (!wait_warp(x, x.bar(B_PEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
+        if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
         if (warp == 2 * (int)x.peer) {
           if (lane == 0)
-            ptx::mbar_arrive_expect_tx(x.bar(B_PRECV + sb), kPRowsBytes + kAlphaBytes);
+            ptx::mbar_arrive_expect_tx(x.bar(B_PRECV + pbuf), kPRowsBytes + kAlphaBytes);
           __syncwarp();
           // my P.V of page g - 2 has read the peer's rows (its commit was
           // waited on above): the peer may send page g's
-          if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_pfree + 8u * sb);
+          if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_pfree + 8u * pbuf);
         }
-        if (!wait_warp(x, x.bar(B_PRECV + sb), (g >> 1) & 1u, true)) return false;
+        if (!wait_warp(x, x.bar(B_PRECV + pbuf), (g / kPBufs) & 1u, true)) return false;
         const float alpha = __uint_as_float(
-            ptx::ld_shared_u32_volatile(x.sbase + kAlpha + sb * 512u + (uint32_t)r * 4u));
+            ptx::ld_shared_u32_volatile(x.sbase + kAlpha + pbuf * 512u + (uint32_t)r * 4u));
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
           // a rescale of O needs the P.V of page g - 1 done
-          if (!wait_warp(x, x.bar(B_PEMPTY + (sb ^ 1u)), ((g - 1) >> 1) & 1u)) return false;
+          if (kPBufs > 1 &&
+              !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
+            return false;
           ptx::tc_fence_after();
 #pragma unroll 1
           for (int ch = 0; ch < 8; ++ch) {
@@ -634,7 +650,7 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + sb));
+        if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
       }
     }
 
@@ -735,7 +751,7 @@ __device__ __forceinline__ bool run_psend(const Ctx& x, const Work& w) {
   uint32_t g = 0;
   while (it.next(b, pb, pe)) {
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      const uint32_t sb = g & 1u, ph = (g >> 1) & 1u;
+      const uint32_t sb = g % kPBufs, ph = (g / kPBufs) & 1u;
       if (!wait_bar(x, x.bar(B_PLOCAL + sb), ph)) return false;
       // the peer's P.V of page g - 2 is done: its buffer g % 2 is free
       if (!wait_bar(x, x.bar(B_PFREE + sb), ph, true)) return false;
