@@ -655,9 +655,10 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
     }
 
     // Epilogue: O / l for this CTA's dims of all 128 rows; lse by the row's
-    // owner.  The owners send 1/l of their rows to the peer's importers.
-    if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
-    ptx::tc_fence_after();
+    // owner.  The owners' sums are final after the last page: they send 1/l
+    // of their rows to the peer's importers and write lse before the last
+    // P.V is done, so that draining O (which the next tile's first P.V waits
+    // for) is all that follows it.
     const uint32_t par = n_item & 1u;
     const int ns = w.items[b * kItemWords + 1];
     const bool direct = (ns == 1);
@@ -685,13 +686,16 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
         else
           prm.ws_lse[slot * kTileRows + r] = lse_v;
       }
+      if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
     } else {
       if (lead && warp == 2 * (int)x.peer)
         ptx::mbar_arrive_expect_tx(x.bar(B_LRECV + par), 2u * 128u);
+      if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
       if (!wait_warp(x, x.bar(B_LRECV + par), (n_item >> 1) & 1u, true)) return false;
       inv_l = __uint_as_float(
           ptx::ld_shared_u32_volatile(x.sbase + kInvL + par * 512u + (uint32_t)r * 4u));
     }
+    ptx::tc_fence_after();
 #pragma unroll 1
     for (int ch = 0; ch < 8; ++ch) {
       uint32_t v[32];
