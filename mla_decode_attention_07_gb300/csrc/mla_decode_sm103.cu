@@ -289,14 +289,14 @@ __device__ __forceinline__ void issue_qk(const Ctx& x, uint32_t g) {
   for (int k = 0; k < 16; ++k) {
     const uint64_t bdesc =
         ptx::smem_desc(st + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024, ptx::kLayoutSw128);
-    ptx::mma_ts(d_s, x.tmem + kColQ + k * 8, bdesc, id_qk, k ? 1u : 0u);
+    ptx::mma_ts_elect(d_s, x.tmem + kColQ + k * 8, bdesc, id_qk, k ? 1u : 0u);
   }
   // rotary dims: both operands from shared memory
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const uint64_t adesc = ptx::smem_desc(x.sbase + kQRope + k * 32, 16, 512, ptx::kLayoutSw64);
     const uint64_t bdesc = ptx::smem_desc(st + kStageRope + k * 32, 16, 512, ptx::kLayoutSw64);
-    ptx::mma_ss(d_s, adesc, bdesc, id_qk, 1u);
+    ptx::mma_ss_elect(d_s, adesc, bdesc, id_qk, 1u);
   }
 }
 
@@ -310,7 +310,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& x, uint32_t g, bool first) {
     const uint64_t bdesc = ptx::smem_desc(vbase + k * 2048, 8192, 1024, ptx::kLayoutSw128);
     const uint64_t adesc = ptx::smem_desc(x.sbase + kP + (g % kPBufs) * kPBytes + k * 32, 16, 1024,
                                           ptx::kLayoutSw128);
-    ptx::mma_ss(x.tmem + kColO, adesc, bdesc, id_pv, (first && k == 0) ? 0u : 1u);
+    ptx::mma_ss_elect(x.tmem + kColO, adesc, bdesc, id_pv, (first && k == 0) ? 0u : 1u);
   }
 }
 
@@ -321,15 +321,15 @@ __device__ __forceinline__ bool run_mma_qk(const Ctx& x, const Work& w) {
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
   while (it.next(b, pb, pe)) {
-    if (!wait_bar(x, x.bar(B_QFULL), n_item & 1u)) return false;
+    if (!wait_warp(x, x.bar(B_QFULL), n_item & 1u)) return false;
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      if (!wait_bar(x, x.bar(B_FULL + g % kStages), (g / kStages) & 1u)) return false;
-      if (!wait_bar(x, x.bar(B_SEMPTY + (g & 1u)), ((g >> 1) & 1u) ^ 1u)) return false;
+      if (!wait_warp(x, x.bar(B_FULL + g % kStages), (g / kStages) & 1u)) return false;
+      if (!wait_warp(x, x.bar(B_SEMPTY + (g & 1u)), ((g >> 1) & 1u) ^ 1u)) return false;
       ptx::tc_fence_after();
       issue_qk(x, g);
-      ptx::mma_commit(x.bar(B_SFULL + (g & 1u)));
+      ptx::mma_commit_elect(x.bar(B_SFULL + (g & 1u)));
     }
-    ptx::mma_commit(x.bar(B_QEMPTY));
+    ptx::mma_commit_elect(x.bar(B_QEMPTY));
     ++n_item;
   }
   return true;
@@ -343,15 +343,15 @@ __device__ __forceinline__ bool run_mma_pv(const Ctx& x, const Work& w) {
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
   while (it.next(b, pb, pe)) {
-    if (!wait_bar(x, x.bar(B_OEMPTY), (n_item & 1u) ^ 1u)) return false;
+    if (!wait_warp(x, x.bar(B_OEMPTY), (n_item & 1u) ^ 1u)) return false;
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      if (!wait_bar(x, x.bar(B_PFULL + g % kPBufs), (g / kPBufs) & 1u)) return false;
+      if (!wait_warp(x, x.bar(B_PFULL + g % kPBufs), (g / kPBufs) & 1u)) return false;
       ptx::tc_fence_after();
       issue_pv(x, g, pg == pb);
-      ptx::mma_commit(x.bar(B_EMPTY + g % kStages));
-      ptx::mma_commit(x.bar(B_PEMPTY + g % kPBufs));
+      ptx::mma_commit_elect(x.bar(B_EMPTY + g % kStages));
+      ptx::mma_commit_elect(x.bar(B_PEMPTY + g % kPBufs));
     }
-    ptx::mma_commit(x.bar(B_OFULL));
+    ptx::mma_commit_elect(x.bar(B_OFULL));
     ++n_item;
   }
   return true;
@@ -872,10 +872,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    if (lane == 0) run_mma_qk(x, w);
+    run_mma_qk(x, w);   // whole warp: one elected lane issues
     __syncwarp();
   } else if (warp == kPvWarp) {
-    if (lane == 0) run_mma_pv(x, w);
+    run_mma_pv(x, w);
     __syncwarp();
   } else if (warp >= kExchangeWarp0 && warp < kExchangeWarp0 + 4) {
     run_exchange(x, w, prm, warp - kExchangeWarp0, lane);
@@ -891,13 +891,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Teardown.  After an abort, give in-flight copies and MMAs time to land
   // before the shared memory and TMEM are released.
   const bool aborted = ptx::ld_shared_u32_volatile(x.abort_addr) != 0u;
-  if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
-    // each issuing thread's MMAs are done
-    ptx::mma_commit(x.bar(B_TEARDOWN));
+  if (warp == kMmaWarp || warp == kPvWarp) {
+    // each issuing lane's MMAs are done (the warp is converged here, so the
+    // commit goes out from the lane that issued them)
+    ptx::mma_commit_elect(x.bar(B_TEARDOWN));
     const uint64_t t0 = ptx::globaltimer();
     while (!ptx::mbar_try_wait(x.bar(B_TEARDOWN), 0u)) {
       if (ptx::globaltimer() - t0 > kWaitTimeoutNs) {
-        atomicCAS(x.err, 0, MLA_ERR_DEVICE_TIMEOUT);
+        if (lane == 0) atomicCAS(x.err, 0, MLA_ERR_DEVICE_TIMEOUT);
         break;
       }
     }
