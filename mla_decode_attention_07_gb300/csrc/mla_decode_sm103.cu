@@ -85,6 +85,7 @@ constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after a
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kHalfRows = 64;                        // softmax rows owned by one CTA
+constexpr int kSubRows = 16;                         // of them in each TMEM lane quadrant
 constexpr int kRemoteLane = 31;   // the lane that issues a warp's remote copies and arrives
 
 // TMEM columns (fp32 / packed-bf16x2 32-bit cells, 128 lanes).
@@ -99,8 +100,8 @@ constexpr int kStages = 4;
 // buffer g % k.  Two of each measured no faster than one (the score tiles in
 // TMEM are double buffered, which is what lets the next page's scores run
 // under this page's softmax), so one of each leaves the shared memory free.
-constexpr int kRBufs = 1;
-constexpr int kPBufs = 1;
+constexpr int kRBufs = 2;
+constexpr int kPBufs = 2;
 constexpr uint32_t kQRope = 0;            // [128 x 32] bf16, 64-byte swizzle
 constexpr uint32_t kStage0 = 8192;        // kStages x 36 KB
 constexpr uint32_t kStageBytes = 36864;
@@ -109,8 +110,9 @@ constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][
 constexpr uint32_t kRecvBytes = kHalfRows * 64 * 4;
 constexpr uint32_t kP = kRecv + kRBufs * kRecvBytes;  // kPBufs x [128 x 64] bf16, 128-byte swizzle
 constexpr uint32_t kPBytes = 128 * 64 * 2;
-constexpr uint32_t kAlpha = kP + kPBufs * kPBytes;           // float[kPBufs][128] rescale factors
-constexpr uint32_t kInvL = kAlpha + kPBufs * 128 * 4;        // float[2][128] 1/l per tile parity
+constexpr uint32_t kAlphaBufBytes = 2 * kHalfRows * 4;
+constexpr uint32_t kAlpha = kP + kPBufs * kPBytes;   // float[kPBufs][owner rank][64] rescale factors
+constexpr uint32_t kInvL = kAlpha + kPBufs * kAlphaBufBytes;   // float[2 parities][owner rank][64] 1/l
 constexpr uint32_t kBar = kInvL + 2 * 128 * 4;
 constexpr uint32_t kMisc = kBar + 8 * 40;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
@@ -120,8 +122,8 @@ static_assert(kSmemAlloc <= 232448, "shared memory");
 // Bytes moved per stage / per Q tile by one CTA.
 constexpr uint32_t kStageTx = 4 * 8192 + 4096;   // 4 latent boxes + rotary half
 constexpr uint32_t kQRopeTx = 8192;
-constexpr uint32_t kPRowsBytes = kHalfRows * 128;    // one CTA's 64 rows of P
-constexpr uint32_t kAlphaBytes = kHalfRows * 4;
+constexpr uint32_t kPRecvTx = kHalfRows * 128 + kHalfRows * 4;   // the peer's 64 P rows + factors
+constexpr uint32_t kInvLTx = kHalfRows * 4;                        // the peer's 64 values of 1/l
 
 // [2] = one per buffer: page g uses score tile g % 2, receive buffer
 // g % kRBufs and P buffer g % kPBufs.
@@ -357,24 +359,106 @@ __device__ __forceinline__ bool run_mma_pv(const Ctx& x, const Work& w) {
   return true;
 }
 
+// ------------------------------------------------------------------ half-quadrant TMEM access
+// 16 lanes of one lane quadrant, two threads per lane: thread t reaches lane
+// base + (t & 15) at columns col + (t >> 4) * OFF + j, j < 32 (the tcgen05
+// .16x32bx2 shape; its layout was checked on GB300 against the 32x32b one).
+// The load waits for its data in the same statement, as tmem_load32.
+#define MLA_R32(i) "=r"(r[i])
+template <int OFF>
+__device__ __forceinline__ void tmem_load16x2(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], "
+      "%33;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MLA_R32(0), MLA_R32(1), MLA_R32(2), MLA_R32(3), MLA_R32(4), MLA_R32(5), MLA_R32(6),
+        MLA_R32(7), MLA_R32(8), MLA_R32(9), MLA_R32(10), MLA_R32(11), MLA_R32(12), MLA_R32(13),
+        MLA_R32(14), MLA_R32(15), MLA_R32(16), MLA_R32(17), MLA_R32(18), MLA_R32(19),
+        MLA_R32(20), MLA_R32(21), MLA_R32(22), MLA_R32(23), MLA_R32(24), MLA_R32(25),
+        MLA_R32(26), MLA_R32(27), MLA_R32(28), MLA_R32(29), MLA_R32(30), MLA_R32(31)
+      : "r"(taddr), "n"(OFF)
+      : "memory");
+}
+#undef MLA_R32
+#define MLA_W32(i) "r"(v[i])
+template <int OFF>
+__device__ __forceinline__ void tmem_store16x2(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, "
+      "{%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, "
+      "%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};" ::"r"(
+          taddr),
+      "n"(OFF), MLA_W32(0), MLA_W32(1), MLA_W32(2), MLA_W32(3), MLA_W32(4), MLA_W32(5),
+      MLA_W32(6), MLA_W32(7), MLA_W32(8), MLA_W32(9), MLA_W32(10), MLA_W32(11), MLA_W32(12),
+      MLA_W32(13), MLA_W32(14), MLA_W32(15), MLA_W32(16), MLA_W32(17), MLA_W32(18), MLA_W32(19),
+      MLA_W32(20), MLA_W32(21), MLA_W32(22), MLA_W32(23), MLA_W32(24), MLA_W32(25), MLA_W32(26),
+      MLA_W32(27), MLA_W32(28), MLA_W32(29), MLA_W32(30), MLA_W32(31)
+      : "memory");
+}
+#undef MLA_W32
+
+// This CTA's O columns of the 16 rows at `lanes` (a half quadrant) times each
+// row's alpha (the two threads of a row hold the same alpha): 4 x 32 columns
+// per thread, the 256 in all.
+__device__ __forceinline__ void scale_o_rows(const Ctx& x, uint32_t lanes, float alpha) {
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t v[32];
+    const uint32_t ta = x.tmem + lanes + kColO + ch * 32;
+    tmem_load16x2<128>(ta, v);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+    tmem_store16x2<128>(ta, v);
+  }
+  ptx::tmem_wait_st();
+}
+
 // ------------------------------------------------------------------ exchange warps
-// Warps 4-7 put the latent half of each Q tile into TMEM (one row per
-// thread).  The two of them whose lanes are the peer's softmax rows then ship
-// those rows' partial scores of every page to the peer, as soon as the score
-// MMA has written them: copied out of TMEM into registers (which frees the
-// score tile) and stored with st.async straight into the peer's receive
-// buffer g % 2 as [16-byte chunk c][row], so a warp's store covers 512
-// contiguous bytes; each store completes its bytes on the peer's barrier,
-// where the receiving side has posted the expected count.
+// Warp 4 + q works on TMEM lane quadrant q.  Per tile, the four of them put
+// the latent half of Q into TMEM (one row per thread).  Per page, each ships
+// the peer's 16 rows of its quadrant: their partial scores, copied out of
+// TMEM (which frees the score tile) and stored with st.async into the peer's
+// receive buffer g % 2 as [16-byte chunk][owned row], completing on the
+// peer's barrier where the receiving side posted the byte count.  One page
+// later it imports the same rows' probabilities: once the peer's P rows and
+// rescale factors have landed in this CTA's P buffer, it rescales those rows
+// of O when a factor is not 1 and signals the P.V issuer.  Importing one page
+// behind keeps the next page's scores from waiting on the peer's softmax.
 __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const DecodeParams& prm,
                                              int e, int lane) {
-  const int r = e * 32 + lane;
+  const int r = e * 32 + lane;   // Q row of this thread
   const uint32_t lane_base = (uint32_t)(e * 32) << 16;
-  const bool sender = (uint32_t)(e >> 1) != x.rank;   // lanes of the peer's rows
-  const uint32_t peer_row = ptx::map_to_rank(x.sbase + kRecv, x.peer) +
-                            (uint32_t)(r & (kHalfRows - 1)) * 16u;
+  const uint32_t peer_lanes = (uint32_t)(e * 32 + kSubRows * (int)x.peer) << 16;
+  const int hr = kSubRows * e + (lane & 15);   // the row's index among the peer's owned rows
+  const int half = lane >> 4;                   // score columns [32 half, 32 half + 32)
+  const uint32_t peer_row = ptx::map_to_rank(x.sbase + kRecv, x.peer) + (uint32_t)hr * 16u +
+                            (uint32_t)(8 * half) * (kHalfRows * 16);
   const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
+  const uint32_t alpha_in = x.sbase + kAlpha + (x.peer * kHalfRows + (uint32_t)hr) * 4u;
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
+
+  auto import_page = [&](uint32_t gi) -> bool {
+    const uint32_t pbuf = gi % kPBufs;
+    if (!wait_warp(x, x.bar(B_PRECV + pbuf), (gi / kPBufs) & 1u, true)) return false;
+    const float alpha =
+        __uint_as_float(ptx::ld_shared_u32_volatile(alpha_in + pbuf * kAlphaBufBytes));
+    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      // a rescale of O needs the P.V of page gi - 1 done (never the first
+      // page of a tile, whose factors are all 1)
+      if (kPBufs > 1 &&
+          !wait_warp(x, x.bar(B_PEMPTY + (gi - 1) % kPBufs), ((gi - 1) / kPBufs) & 1u))
+        return false;
+      ptx::tc_fence_after();
+      scale_o_rows(x, peer_lanes, alpha);
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
+    return true;
+  };
+
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
@@ -409,71 +493,71 @@ __device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const 
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(x.bar(B_QFULL));
 
-    if (!sender) {
-      g += (uint32_t)(pe - pb);
-      ++n_item;
-      continue;
-    }
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const uint32_t sb = g & 1u;
       if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
       ptx::tc_fence_after();
-      uint32_t v[2][32];
-      tmem_load32(x.tmem + lane_base + kColS + sb * 64, v[0]);
-      tmem_load32(x.tmem + lane_base + kColS + sb * 64 + 32, v[1]);
+      uint32_t v[32];
+      tmem_load16x2<32>(x.tmem + peer_lanes + kColS + sb * 64, v);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
-      // the peer has read what was sent into this buffer two pages ago
+      // the peer has read what was sent into this buffer kRBufs pages ago
       const uint32_t rb = g % kRBufs;
       if (!wait_warp(x, x.bar(B_REMPTY + rb), ((g / kRBufs) & 1u) ^ 1u, true)) return false;
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          ptx::st_async_v4(peer_row + rb * kRecvBytes + (uint32_t)(half * 8 + c) * (kHalfRows * 16),
-                           __uint_as_float(v[half][4 * c]), __uint_as_float(v[half][4 * c + 1]),
-                           __uint_as_float(v[half][4 * c + 2]), __uint_as_float(v[half][4 * c + 3]),
-                           peer_rfull + 8u * rb);
+      for (int c = 0; c < 8; ++c)
+        ptx::st_async_v4(peer_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16),
+                         __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]),
+                         peer_rfull + 8u * rb);
+      if (pg > pb && !import_page(g - 1)) return false;
     }
+    if (!import_page(g - 1)) return false;   // the tile's last page
     ++n_item;
   }
   return true;
 }
 
 // ------------------------------------------------------------------ row warps
-// Warps 0-3, one thread per query row (= TMEM lane).  In CTA r the warps on
-// rows [64 r, 64 r + 64) own those rows' softmax; the other two import the
-// peer's probability rows.  Both kinds write the epilogue of their rows for
-// this CTA's half of the output dims.
+// Warp q (0-3) owns the softmax of the 16 rows of lane quadrant q that belong
+// to this CTA (lanes 32 q + 16 r + [0, 16) in CTA r), two threads per row
+// with 32 of the page's 64 score columns each, so all four schedulers share
+// the softmax.  Per page: add the peer's partial scores for those rows, mask,
+// row max (the accum_s -> scores_max reduce: over the thread's 32 columns,
+// then with its partner's), exp2, sums, and the bf16 probabilities and
+// rescale factors into P buffer g % 2.  In the epilogue the warp writes O / l
+// for all 32 rows of its quadrant and this CTA's half of the output dims.
 __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const DecodeParams& prm,
                                          int warp, int lane) {
-  const int r = warp * 32 + lane;                   // tile row == TMEM lane
+  const int half = lane >> 4;
+  const int t = lane & 15;
+  const int ro = warp * 32 + kSubRows * (int)x.rank + t;   // owned tile row (TMEM lane)
+  const int hr = kSubRows * warp + t;                      // its owned-row index
+  const uint32_t own_lanes = (uint32_t)(warp * 32 + kSubRows * (int)x.rank) << 16;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const bool owner = (uint32_t)(warp >> 1) == x.rank;
-  const bool lead = (warp & 1) == 0 && lane == 0;   // first lane of the pair of warps
-  const int hr = r & (kHalfRows - 1);               // row inside its half
-  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)hr * 16u;
+  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)hr * 16u +
+                            (uint32_t)(8 * half) * (kHalfRows * 16);
   const uint32_t peer_rempty = ptx::map_to_rank(x.bar(B_REMPTY), x.peer);
-  const uint32_t peer_pfree = ptx::map_to_rank(x.bar(B_PFREE), x.peer);
   const uint32_t peer_lrecv = ptx::map_to_rank(x.bar(B_LRECV), x.peer);
-  const uint32_t pswz = (uint32_t)(r & 7);
+  const uint32_t pswz = (uint32_t)(ro & 7);
   const float scale_log2 = prm.scale_log2;
 
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
   while (it.next(b, pb, pe)) {
-    const int qr = w.tile * kTileRows + r;
-    const bool valid = qr < w.rows;
-    const int i = qr / prm.h_q;
-    const int h = qr - i * prm.h_q;
+    const int qo = w.tile * kTileRows + ro;
+    const bool valid_o = qo < w.rows;
+    const int io = qo / prm.h_q;
+    const int ho = qo - io * prm.h_q;
     const int L = prm.seqlens[b];
-    const int n_valid = valid ? L - prm.s_q + 1 + i : 0;
+    const int n_valid = valid_o ? L - prm.s_q + 1 + io : 0;
     const int P_total = w.items[b * kItemWords + 0];
     // l_run sums the fp32 probabilities (for lse); lb_run sums them after the
     // bf16 rounding the P.V MMA sees, so out = sum(p v) / sum(p) uses one set
-    // of weights and stays a true weighted average of the value rows.
+    // of weights and stays a true weighted average of the value rows.  Each
+    // thread sums its 32 columns; the partners' sums are added at the end.
     float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
 
     for (int pg = pb; pg < pe; ++pg, ++g) {
@@ -481,226 +565,186 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       const uint32_t sb = g & 1u;             // score tile
       const uint32_t rb = g % kRBufs;         // receive buffer
       const uint32_t pbuf = g % kPBufs;       // P buffer
-      if (owner) {
-        // 1. Full scores of my rows: own partial (TMEM) + the peer's (received).
-        if (lead && warp == 2 * (int)x.rank)
-          ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + rb), kRecvBytes);
-        if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
-        if (!wait_warp(x, x.bar(B_RFULL + rb), (g / kRBufs) & 1u, true)) return false;
+      // 1. Full scores of my rows: own partial (TMEM) + the peer's (received).
+      if (warp == 0 && lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + rb), kRecvBytes);
+      if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
+      if (!wait_warp(x, x.bar(B_RFULL + rb), (g / kRBufs) & 1u, true)) return false;
+      ptx::tc_fence_after();
+      float s[32];
+      {
+        uint32_t v[32];
+        tmem_load16x2<32>(x.tmem + own_lanes + kColS + sb * 64, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        // addition commutes: the same sums whichever CTA owns the row
+        const float4 v = ptx::ld_shared_v4f(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(v.x, v.y)),
+                       s[4 * c], s[4 * c + 1]);
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(v.z, v.w)),
+                       s[4 * c + 2], s[4 * c + 3]);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+
+      // 2. Mask, row max (the accum_s -> scores_max reduce), exp2, sums.
+      const int tok0 = pg * kPageTokens + 32 * half;
+      if (__any_sync(0xffffffffu, tok0 + 32 > n_valid)) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (tok0 + k >= n_valid) s[k] = -INFINITY;
+      }
+      // four independent chains of 3-input maxima, then the partner's half
+      float m4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float* sj = s + 8 * j;
+        m4[j] = fmaxf(ptx::max3(ptx::max3(ptx::max3(sj[0], sj[1], sj[2]), sj[3], sj[4]), sj[5], sj[6]),
+                      sj[7]);
+      }
+      float mx = fmaxf(ptx::max3(m4[0], m4[1], m4[2]), m4[3]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      // Every value read from the receive buffer went into mx: once mx is
+      // computed the reads are complete and the peer may refill the buffer.
+      ptx::consume(mx);
+      __syncwarp();
+      if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_rempty + 8u * rb);
+      const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
+      const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
+      const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
+      if (rescale) {
+        l_run *= alpha;
+        lb_run *= alpha;
+      }
+      if (rescale || first) m_run = m_new;
+      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+      // exp2(s * scale - m) on pairs: the fma and the sums are f32x2 ops, and
+      // the sums run as two independent chains
+      uint32_t pk[16];
+      const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
+      const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+      uint64_t ps2[2] = {0ull, 0ull}, pb2[2] = {0ull, 0ull};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float xa, xc;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * j], s[2 * j + 1]), sc2, nm2), xa, xc);
+        const float a = ptx::ex2(xa), c = ptx::ex2(xc);
+        ps2[j & 1] = ptx::f2_add(ps2[j & 1], ptx::f2_pack(a, c));
+        pk[j] = ptx::pack_bf16x2(a, c);
+        pb2[j & 1] = ptx::f2_add(pb2[j & 1], ptx::f2_pack(__uint_as_float(pk[j] << 16),
+                                                          __uint_as_float(pk[j] & 0xffff0000u)));
+      }
+      float pa, pc, ba, bc;
+      ptx::f2_unpack(ptx::f2_add(ps2[0], ps2[1]), pa, pc);
+      ptx::f2_unpack(ptx::f2_add(pb2[0], pb2[1]), ba, bc);
+      l_run += pa + pc;
+      lb_run += ba + bc;
+
+      // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
+      //    of my rows of page g - 2 to the peer has read them.  A rescale of
+      //    O also needs the P.V of page g - 1 done.
+      if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
+      if (!wait_warp(x, x.bar(B_PSENT + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
+      if (__any_sync(0xffffffffu, rescale)) {
+        if (kPBufs > 1 &&
+            !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
+          return false;
         ptx::tc_fence_after();
-        float s[64];
-        {
-          uint32_t v[32];
-          tmem_load32(x.tmem + lane_base + kColS + sb * 64, v);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
-          tmem_load32(x.tmem + lane_base + kColS + sb * 64 + 32, v);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) s[32 + k] = __uint_as_float(v[k]);
+        scale_o_rows(x, own_lanes, alpha);
+      }
+      // Past the end of the sequence the cache slots of the last page hold
+      // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
+      // the P.V MMA, so zero those value rows first (each CTA zeroes its own
+      // stage, split between its four row warps).
+      if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
+        const int t0 = L & (kPageTokens - 1);
+        const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
+        const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
+        for (int idx = warp * 32 + lane; idx < n16; idx += kRowWarps * 32) {
+          const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
+          ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
         }
+      }
+      {
+        // P row ro, 128-byte swizzle: 16-byte chunk c at position c ^ (ro % 8);
+        // this thread's 32 columns are chunks 4 half .. 4 half + 3
+        const uint32_t prow = x.sbase + kP + pbuf * kPBytes + (uint32_t)ro * 128u;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          // addition commutes: the same sums in either CTA
-          const float4 v =
-              ptx::ld_shared_v4f(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
-          ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(v.x, v.y)),
-                         s[4 * c], s[4 * c + 1]);
-          ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(v.z, v.w)),
-                         s[4 * c + 2], s[4 * c + 3]);
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
-
-        // 2. Mask, row max (the accum_s -> scores_max reduce), exp2, sums.
-        const int tok0 = pg * kPageTokens;
-        if (__any_sync(0xffffffffu, tok0 + kPageTokens > n_valid)) {
-#pragma unroll
-          for (int k = 0; k < 64; ++k)
-            if (tok0 + k >= n_valid) s[k] = -INFINITY;
-        }
-        // four independent max chains of 3-input maxima
-        float m4[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-        for (int k = 4; k < 64; k += 8) {
-          m4[0] = ptx::max3(m4[0], s[k], s[k + 1]);
-          m4[1] = ptx::max3(m4[1], s[k + 2], s[k + 3]);
-          m4[2] = ptx::max3(m4[2], s[k + 4], s[k + 5]);
-          m4[3] = ptx::max3(m4[3], s[k + 6], s[k + 7]);
-        }
-        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        // Every value read from the receive buffer went into mx: once mx is
-        // computed the reads are complete and the peer may refill the buffer.
-        ptx::consume(mx);
-        __syncwarp();
-        if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_rempty + 8u * rb);
-        const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
-        const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
-        const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
-        if (rescale) {
-          l_run *= alpha;
-          lb_run *= alpha;
-        }
-        if (rescale || first) m_run = m_new;
-        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-        // exp2(s * scale - m) on pairs: the fma and the sums are f32x2 ops, and
-        // the sums run as two independent chains
-        uint32_t pk[32];
-        const uint64_t sc2 = ptx::f2_pack(scale_log2, scale_log2);
-        const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-        uint64_t ps2[2] = {0ull, 0ull}, pb2[2] = {0ull, 0ull};
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          float xa, xc;
-          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[2 * j], s[2 * j + 1]), sc2, nm2), xa, xc);
-          const float a = ptx::ex2(xa), c = ptx::ex2(xc);
-          ps2[j & 1] = ptx::f2_add(ps2[j & 1], ptx::f2_pack(a, c));
-          pk[j] = ptx::pack_bf16x2(a, c);
-          pb2[j & 1] = ptx::f2_add(pb2[j & 1], ptx::f2_pack(__uint_as_float(pk[j] << 16),
-                                                            __uint_as_float(pk[j] & 0xffff0000u)));
-        }
-        float pa, pc, ba, bc;
-        ptx::f2_unpack(ptx::f2_add(ps2[0], ps2[1]), pa, pc);
-        ptx::f2_unpack(ptx::f2_add(pb2[0], pb2[1]), ba, bc);
-        l_run += pa + pc;
-        lb_run += ba + bc;
-
-        // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
-        //    of my rows of page g - 2 to the peer has read them.  A rescale
-        //    of O also needs the P.V of page g - 1 done.
-        if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
-        if (!wait_warp(x, x.bar(B_PSENT + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
-        if (__any_sync(0xffffffffu, rescale)) {
-          if (kPBufs > 1 &&
-              !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
-            return false;
-          ptx::tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t v[32];
-            const uint32_t ta = x.tmem + lane_base + kColO + ch * 32;
-            tmem_load32(ta, v);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            ptx::tmem_st32(ta, v);
-          }
-          ptx::tmem_wait_st();
-        }
-        // Past the end of the sequence the cache slots of the last page hold
-        // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
-        // the P.V MMA, so zero those value rows first (each CTA zeroes its own
-        // stage, split between its two softmax warps).
-        if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
-          const int t0 = L & (kPageTokens - 1);
-          const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
-          const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
-          for (int idx = hr; idx < n16; idx += kHalfRows) {
-            const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
-            ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
-          }
-        }
-        {
-          // P row r, 128-byte swizzle: 16-byte chunk c at position c ^ (r % 8)
-          const uint32_t prow = x.sbase + kP + pbuf * kPBytes + (uint32_t)r * 128u;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            ptx::st_shared_v4(prow + (((uint32_t)c ^ pswz) << 4), pk[4 * c], pk[4 * c + 1],
-                              pk[4 * c + 2], pk[4 * c + 3]);
-          ptx::st_shared_u32(x.sbase + kAlpha + pbuf * 512u + (uint32_t)r * 4u,
+        for (int j = 0; j < 4; ++j)
+          ptx::st_shared_v4(prow + (((uint32_t)(4 * half + j) ^ pswz) << 4), pk[4 * j],
+                            pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        if (half == 0)
+          ptx::st_shared_u32(x.sbase + kAlpha + pbuf * kAlphaBufBytes +
+                                 (x.rank * kHalfRows + (uint32_t)hr) * 4u,
                              __float_as_uint(alpha));
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(x.bar(B_PLOCAL + pbuf));
-          ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
-        }
-      } else {
-        // Import: once my P.V of page g - 2 is done, tell the peer it may
-        // write its rows of page g into my P buffer g % 2, then wait for them.
-        if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
-        if (warp == 2 * (int)x.peer) {
-          if (lane == 0)
-            ptx::mbar_arrive_expect_tx(x.bar(B_PRECV + pbuf), kPRowsBytes + kAlphaBytes);
-          __syncwarp();
-          // my P.V of page g - 2 has read the peer's rows (its commit was
-          // waited on above): the peer may send page g's
-          if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_pfree + 8u * pbuf);
-        }
-        if (!wait_warp(x, x.bar(B_PRECV + pbuf), (g / kPBufs) & 1u, true)) return false;
-        const float alpha = __uint_as_float(
-            ptx::ld_shared_u32_volatile(x.sbase + kAlpha + pbuf * 512u + (uint32_t)r * 4u));
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-          // a rescale of O needs the P.V of page g - 1 done
-          if (kPBufs > 1 &&
-              !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
-            return false;
-          ptx::tc_fence_after();
-#pragma unroll 1
-          for (int ch = 0; ch < 8; ++ch) {
-            uint32_t v[32];
-            const uint32_t ta = x.tmem + lane_base + kColO + ch * 32;
-            tmem_load32(ta, v);
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            ptx::tmem_st32(ta, v);
-          }
-          ptx::tmem_wait_st();
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(x.bar(B_PLOCAL + pbuf));
+        ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
       }
     }
 
-    // Epilogue: O / l for this CTA's dims of all 128 rows; lse by the row's
-    // owner.  The owners' sums are final after the last page: they send 1/l
-    // of their rows to the peer's importers and write lse before the last
-    // P.V is done, so that draining O (which the next tile's first P.V waits
-    // for) is all that follows it.
+    // Epilogue: O / l for this CTA's dims of the warp's 32 rows; lse by the
+    // row's owner.  The owners' sums are final after the last page: they send
+    // 1/l of their rows to the peer and write lse before the last P.V is
+    // done, so that draining O (which the next tile's first P.V waits for) is
+    // all that follows it.
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+    lb_run += __shfl_xor_sync(0xffffffffu, lb_run, 16);
     const uint32_t par = n_item & 1u;
     const int ns = w.items[b * kItemWords + 1];
     const bool direct = (ns == 1);
     const int sidx = (n_item == 0) ? w.split0 : 0;
     const int64_t slot = (int64_t)w.tile * w.stotal + w.items[b * kItemWords + 2] + sidx;
-    const int64_t orow = ((int64_t)b * prm.s_q + i) * prm.h_q + h;
-    float inv_l;
-    if (owner) {
-      inv_l = lb_run > 0.f ? 1.0f / lb_run : 0.f;
-      ptx::st_shared_u32(x.sbase + kInvL + par * 512u + (uint32_t)r * 4u, __float_as_uint(inv_l));
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == kRemoteLane) {
-        // this warp's 32 values of 1/l
-        const uint32_t woff = kInvL + par * 512u + (uint32_t)(warp * 32) * 4u;
-        ptx::bulk_copy_to_peer(ptx::map_to_rank(x.sbase + woff, x.peer), x.sbase + woff, 128u,
-                               peer_lrecv + 8u * par);
-        ptx::bulk_commit();
-        ptx::bulk_wait_read_all();
-      }
-      const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-      if (valid) {
-        if (direct)
-          prm.lse[((int64_t)b * prm.h_q + h) * prm.s_q + i] = lse_v;
-        else
-          prm.ws_lse[slot * kTileRows + r] = lse_v;
-      }
-      if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
-    } else {
-      if (lead && warp == 2 * (int)x.peer)
-        ptx::mbar_arrive_expect_tx(x.bar(B_LRECV + par), 2u * 128u);
-      if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
-      if (!wait_warp(x, x.bar(B_LRECV + par), (n_item >> 1) & 1u, true)) return false;
-      inv_l = __uint_as_float(
-          ptx::ld_shared_u32_volatile(x.sbase + kInvL + par * 512u + (uint32_t)r * 4u));
+    const float inv_own = lb_run > 0.f ? 1.0f / lb_run : 0.f;
+    if (half == 0)
+      ptx::st_shared_u32(x.sbase + kInvL + par * 512u + (x.rank * kHalfRows + (uint32_t)hr) * 4u,
+                         __float_as_uint(inv_own));
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == kRemoteLane) {
+      // this warp's 16 values of 1/l
+      const uint32_t woff = kInvL + par * 512u + (x.rank * kHalfRows + kSubRows * warp) * 4u;
+      ptx::bulk_copy_to_peer(ptx::map_to_rank(x.sbase + woff, x.peer), x.sbase + woff,
+                             kSubRows * 4u, peer_lrecv + 8u * par);
+      ptx::bulk_commit();
+      ptx::bulk_wait_read_all();
     }
+    if (warp == 0 && lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_LRECV + par), kInvLTx);
+    if (half == 0 && valid_o) {
+      const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (direct)
+        prm.lse[((int64_t)b * prm.h_q + ho) * prm.s_q + io] = lse_v;
+      else
+        prm.ws_lse[slot * kTileRows + ro] = lse_v;
+    }
+    if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
+    if (!wait_warp(x, x.bar(B_LRECV + par), (n_item >> 1) & 1u, true)) return false;
+    // rows of the epilogue: lane -> tile row warp * 32 + lane (mine when its
+    // half quadrant is this CTA's, and then this thread owned it)
+    const int re = warp * 32 + lane;
+    const float inv_l =
+        (half == (int)x.rank)
+            ? inv_own
+            : __uint_as_float(ptx::ld_shared_u32_volatile(
+                  x.sbase + kInvL + par * 512u + (x.peer * kHalfRows + (uint32_t)hr) * 4u));
+    const int qe = w.tile * kTileRows + re;
+    const bool valid_e = qe < w.rows;
+    const int ie = qe / prm.h_q;
+    const int he = qe - ie * prm.h_q;
+    const int64_t orow = ((int64_t)b * prm.s_q + ie) * prm.h_q + he;
     ptx::tc_fence_after();
 #pragma unroll 1
     for (int ch = 0; ch < 8; ++ch) {
       uint32_t v[32];
       tmem_load32(x.tmem + lane_base + kColO + ch * 32, v);
-      if (valid) {
+      if (valid_e) {
         const int d0 = (int)x.rank * 256 + ch * 32;
         if (direct) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
@@ -720,7 +764,7 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
           }
         } else {
           float4* base =
-              reinterpret_cast<float4*>(prm.ws_o) + slot * (kDv / 4) * kTileRows + r;
+              reinterpret_cast<float4*>(prm.ws_o) + slot * (kDv / 4) * kTileRows + re;
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             base[(int64_t)(d0 / 4 + q) * kTileRows] =
@@ -740,29 +784,38 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
 }
 
 // ------------------------------------------------------------------ P sender
-// One thread: for every page, once this CTA's softmax warps have written
-// their 64 probability rows and rescale factors and the peer's P.V of the
-// previous page is done, copies them into the same place in the peer's shared
-// memory (one TMA bulk copy each, completing on the peer's PRECV barrier).
+// One thread.  Per page g: once this CTA's P.V of page g - 2 is done, its P
+// buffer g % 2 may take the peer's rows of page g: post their byte count and
+// tell the peer.  Then, once this CTA's row warps have written their rows and
+// rescale factors and the peer has said the same of its buffer, copy them
+// into the same places in the peer's shared memory (TMA bulk copies,
+// completing on the peer's PRECV barrier).
 __device__ __forceinline__ bool run_psend(const Ctx& x, const Work& w) {
-  const uint32_t poff = kP + x.rank * kPRowsBytes;
-  const uint32_t aoff = kAlpha + x.rank * kAlphaBytes;
-  const uint32_t peer_p = ptx::map_to_rank(x.sbase + poff, x.peer);
+  const uint32_t peer_p = ptx::map_to_rank(x.sbase + kP, x.peer);
+  const uint32_t aoff = kAlpha + x.rank * kHalfRows * 4u;
   const uint32_t peer_a = ptx::map_to_rank(x.sbase + aoff, x.peer);
   const uint32_t peer_precv = ptx::map_to_rank(x.bar(B_PRECV), x.peer);
+  const uint32_t peer_pfree = ptx::map_to_rank(x.bar(B_PFREE), x.peer);
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0;
   while (it.next(b, pb, pe)) {
     for (int pg = pb; pg < pe; ++pg, ++g) {
       const uint32_t sb = g % kPBufs, ph = (g / kPBufs) & 1u;
+      if (!wait_bar(x, x.bar(B_PEMPTY + sb), ph ^ 1u)) return false;
+      ptx::mbar_arrive_expect_tx_relaxed(x.bar(B_PRECV + sb), kPRecvTx);
+      ptx::mbar_arrive_cluster_relaxed(peer_pfree + 8u * sb);
       if (!wait_bar(x, x.bar(B_PLOCAL + sb), ph)) return false;
-      // the peer's P.V of page g - 2 is done: its buffer g % 2 is free
       if (!wait_bar(x, x.bar(B_PFREE + sb), ph, true)) return false;
-      ptx::bulk_copy_to_peer(peer_p + sb * kPBytes, x.sbase + poff + sb * kPBytes, kPRowsBytes,
-                             peer_precv + 8u * sb);
-      ptx::bulk_copy_to_peer(peer_a + sb * 512u, x.sbase + aoff + sb * 512u, kAlphaBytes,
-                             peer_precv + 8u * sb);
+#pragma unroll
+      for (int qd = 0; qd < 4; ++qd) {
+        // rows 32 qd + 16 rank + [0, 16): 2 KB, contiguous in the swizzled buffer
+        const uint32_t off = sb * kPBytes + (uint32_t)(32 * qd + kSubRows * (int)x.rank) * 128u;
+        ptx::bulk_copy_to_peer(peer_p + off, x.sbase + kP + off, kSubRows * 128u,
+                               peer_precv + 8u * sb);
+      }
+      ptx::bulk_copy_to_peer(peer_a + sb * kAlphaBufBytes, x.sbase + aoff + sb * kAlphaBufBytes,
+                             kHalfRows * 4u, peer_precv + 8u * sb);
       ptx::bulk_commit();
       ptx::bulk_wait_read_all();
       ptx::mbar_arrive_relaxed(x.bar(B_PSENT + sb));   // the copies have read the rows
@@ -800,15 +853,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(x.bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(B_SFULL + s), 1);
-      ptx::mbar_init(x.bar(B_SEMPTY + s), 4);   // 2 softmax + 2 sending warps
+      ptx::mbar_init(x.bar(B_SEMPTY + s), 8);   // 4 row + 4 exchange warps
       ptx::mbar_init(x.bar(B_RFULL + s), 1);    // own expect_tx + the peer's st.async bytes
-      ptx::mbar_init(x.bar(B_REMPTY + s), 2);   // the peer's 2 softmax warps (remote)
+      ptx::mbar_init(x.bar(B_REMPTY + s), 4);   // the peer's 4 row warps (remote)
       ptx::mbar_init(x.bar(B_LRECV + s), 1);    // own expect_tx + the peer's 1/l bytes
-      ptx::mbar_init(x.bar(B_PFULL + s), kRowWarps);
+      ptx::mbar_init(x.bar(B_PFULL + s), 8);    // 4 row warps (own rows) + 4 exchange warps (imported)
       ptx::mbar_init(x.bar(B_PEMPTY + s), 1);
       ptx::mbar_init(x.bar(B_PRECV + s), 1);    // own expect_tx + the peer's P bytes
-      ptx::mbar_init(x.bar(B_PFREE + s), 1);    // the peer's importing warp (remote)
-      ptx::mbar_init(x.bar(B_PLOCAL + s), 2);
+      ptx::mbar_init(x.bar(B_PFREE + s), 1);    // the peer's P sender (remote)
+      ptx::mbar_init(x.bar(B_PLOCAL + s), 4);
       ptx::mbar_init(x.bar(B_PSENT + s), 1);
     }
     ptx::mbar_init(x.bar(B_OFULL), 1);
