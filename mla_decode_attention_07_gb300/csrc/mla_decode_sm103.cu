@@ -142,9 +142,7 @@ enum Bar : uint32_t {
   B_REMPTY = B_RFULL + 2,     // [2] the peer's softmax warps have read what I sent (2 remote arrives)
   B_PRECV = B_REMPTY + 2,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
   B_PFREE = B_PRECV + 2,      // [2] the peer's P buffer may take my next rows (peer's P.V done)
-  B_PLOCAL = B_PFREE + 2,     // [2] my 2 softmax warps wrote their P rows
-  B_PSENT = B_PLOCAL + 2,     // [2] my P rows have been read by the bulk copy to the peer (P sender)
-  B_LRECV = B_PSENT + 2,      // [2] the peer's 1/l for its rows arrived (per tile parity)
+  B_LRECV = B_PFREE + 2,      // [2] the peer's 1/l for its rows arrived (per tile parity)
   B_TEARDOWN = B_LRECV + 2,
   B_COUNT,
 };
@@ -540,6 +538,8 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
                             (uint32_t)(8 * half) * (kHalfRows * 16);
   const uint32_t peer_rempty = ptx::map_to_rank(x.bar(B_REMPTY), x.peer);
   const uint32_t peer_lrecv = ptx::map_to_rank(x.bar(B_LRECV), x.peer);
+  const uint32_t peer_precv = ptx::map_to_rank(x.bar(B_PRECV), x.peer);
+  const uint32_t peer_base = ptx::map_to_rank(x.sbase, x.peer);
   const uint32_t pswz = (uint32_t)(ro & 7);
   const float scale_log2 = prm.scale_log2;
 
@@ -644,10 +644,11 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       lb_run += ba + bc;
 
       // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
-      //    of my rows of page g - 2 to the peer has read them.  A rescale of
-      //    O also needs the P.V of page g - 1 done.
+      //    of this warp's rows of page g - 2 to the peer has read them.  A
+      //    rescale of O also needs the P.V of page g - 1 done.
       if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
-      if (!wait_warp(x, x.bar(B_PSENT + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
+      if (lane == kRemoteLane) ptx::bulk_wait_read_but_1();
+      __syncwarp();
       if (__any_sync(0xffffffffu, rescale)) {
         if (kPBufs > 1 &&
             !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
@@ -684,9 +685,18 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       ptx::fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(x.bar(B_PLOCAL + pbuf));
-        ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
+      // 4. This warp's 16 P rows (2 KB, contiguous in the swizzled buffer)
+      //    and their rescale factors into the same places in the peer, once
+      //    the peer's P.V of page g - 2 is done; they complete on the peer's
+      //    PRECV barrier.
+      if (!wait_warp(x, x.bar(B_PFREE + pbuf), (g / kPBufs) & 1u, true)) return false;
+      if (lane == kRemoteLane) {
+        const uint32_t poff = kP + pbuf * kPBytes + (uint32_t)(warp * 32 + kSubRows * (int)x.rank) * 128u;
+        const uint32_t aoff = kAlpha + pbuf * kAlphaBufBytes + (x.rank * kHalfRows + kSubRows * warp) * 4u;
+        ptx::bulk_copy_to_peer(peer_base + poff, x.sbase + poff, kSubRows * 128u, peer_precv + 8u * pbuf);
+        ptx::bulk_copy_to_peer(peer_base + aoff, x.sbase + aoff, kSubRows * 4u, peer_precv + 8u * pbuf);
+        ptx::bulk_commit();
       }
     }
 
@@ -783,18 +793,11 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
   return true;
 }
 
-// ------------------------------------------------------------------ P sender
+// ------------------------------------------------------------------ P notifier
 // One thread.  Per page g: once this CTA's P.V of page g - 2 is done, its P
-// buffer g % 2 may take the peer's rows of page g: post their byte count and
-// tell the peer.  Then, once this CTA's row warps have written their rows and
-// rescale factors and the peer has said the same of its buffer, copy them
-// into the same places in the peer's shared memory (TMA bulk copies,
-// completing on the peer's PRECV barrier).
-__device__ __forceinline__ bool run_psend(const Ctx& x, const Work& w) {
-  const uint32_t peer_p = ptx::map_to_rank(x.sbase + kP, x.peer);
-  const uint32_t aoff = kAlpha + x.rank * kHalfRows * 4u;
-  const uint32_t peer_a = ptx::map_to_rank(x.sbase + aoff, x.peer);
-  const uint32_t peer_precv = ptx::map_to_rank(x.bar(B_PRECV), x.peer);
+// buffer g % 2 may take the peer's rows of page g: post their byte count on
+// PRECV and tell the peer (whose row warps then copy their rows in).
+__device__ __forceinline__ bool run_pnotify(const Ctx& x, const Work& w) {
   const uint32_t peer_pfree = ptx::map_to_rank(x.bar(B_PFREE), x.peer);
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
@@ -805,20 +808,6 @@ __device__ __forceinline__ bool run_psend(const Ctx& x, const Work& w) {
       if (!wait_bar(x, x.bar(B_PEMPTY + sb), ph ^ 1u)) return false;
       ptx::mbar_arrive_expect_tx_relaxed(x.bar(B_PRECV + sb), kPRecvTx);
       ptx::mbar_arrive_cluster_relaxed(peer_pfree + 8u * sb);
-      if (!wait_bar(x, x.bar(B_PLOCAL + sb), ph)) return false;
-      if (!wait_bar(x, x.bar(B_PFREE + sb), ph, true)) return false;
-#pragma unroll
-      for (int qd = 0; qd < 4; ++qd) {
-        // rows 32 qd + 16 rank + [0, 16): 2 KB, contiguous in the swizzled buffer
-        const uint32_t off = sb * kPBytes + (uint32_t)(32 * qd + kSubRows * (int)x.rank) * 128u;
-        ptx::bulk_copy_to_peer(peer_p + off, x.sbase + kP + off, kSubRows * 128u,
-                               peer_precv + 8u * sb);
-      }
-      ptx::bulk_copy_to_peer(peer_a + sb * kAlphaBufBytes, x.sbase + aoff + sb * kAlphaBufBytes,
-                             kHalfRows * 4u, peer_precv + 8u * sb);
-      ptx::bulk_commit();
-      ptx::bulk_wait_read_all();
-      ptx::mbar_arrive_relaxed(x.bar(B_PSENT + sb));   // the copies have read the rows
     }
   }
   return true;
@@ -860,9 +849,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(x.bar(B_PFULL + s), 8);    // 4 row warps (own rows) + 4 exchange warps (imported)
       ptx::mbar_init(x.bar(B_PEMPTY + s), 1);
       ptx::mbar_init(x.bar(B_PRECV + s), 1);    // own expect_tx + the peer's P bytes
-      ptx::mbar_init(x.bar(B_PFREE + s), 1);    // the peer's P sender (remote)
-      ptx::mbar_init(x.bar(B_PLOCAL + s), 4);
-      ptx::mbar_init(x.bar(B_PSENT + s), 1);
+      ptx::mbar_init(x.bar(B_PFREE + s), 1);    // the peer's P notifier (remote)
     }
     ptx::mbar_init(x.bar(B_OFULL), 1);
     ptx::mbar_init(x.bar(B_OEMPTY), kRowWarps);
@@ -934,7 +921,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     run_exchange(x, w, prm, warp - kExchangeWarp0, lane);
     __syncwarp();
   } else if (warp == kPSendWarp) {
-    if (lane == 0) run_psend(x, w);
+    if (lane == 0) run_pnotify(x, w);
     __syncwarp();
   } else if (warp < kRowWarps) {
     run_rows(x, w, prm, warp, lane);

@@ -183,6 +183,11 @@ __device__ __forceinline__ void bulk_load_global(uint32_t dst, const void* src, 
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+// Wait until all but the most recent committed group of bulk copies of this
+// thread have finished reading their sources.
+__device__ __forceinline__ void bulk_wait_read_but_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Wait until every committed bulk copy of this thread has finished reading its source.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
