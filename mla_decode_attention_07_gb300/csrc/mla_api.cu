@@ -226,27 +226,16 @@ void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clus
 // Merges the split partials of every (batch entry, tile) that has two or
 // more splits:  lse = m + ln(sum_j exp(lse_j - m)),  out = sum_j
 // exp(lse_j - lse) * o_j.  Entries without pages get out = 0, lse = -inf.
-// The decode kernel stores partials as [slot][dim/4][row][4] fp32, so the 4
-// dim groups (16 dims) x 128 rows that one CTA merges are 8 KB contiguous per
-// split: one thread moves all of a job's splits into shared memory with TMA
-// bulk copies (up to kCombineChunk splits, 48 KB, in flight at once), then
-// 256 threads (one per row and pair of dim groups) merge them.  The merge
-// weights come straight from the per-split lse values.
-constexpr int kCombineQuads = 4;                                        // dim groups per job
-constexpr int kCombineChunk = 6;   // splits per pass; 48 KB, so four jobs fit on an SM
-constexpr uint32_t kCombineSplitBytes = kCombineQuads * kTileRows * 16;  // 8 KB
-constexpr uint32_t kCombineSmem = kCombineChunk * kCombineSplitBytes + 64;
-constexpr uint64_t kCombineWaitNs = 2000000000ull;
+// The decode kernel stores partials as [slot][dim/4][row][4] fp32, so one
+// job (a batch entry's tile and 16 of its dims) reads, per split, 128 rows x
+// 2 x 16 bytes per half of its threads, every warp access 512 contiguous
+// bytes.  All of a job's loads (the split lse values and partial outputs, up
+// to kCombineBatch splits at a time) are issued before the first use: the
+// job costs about one memory latency after its plan entry is read.
+constexpr int kCombineQuads = 4;    // dim groups (of 4) per job
+constexpr int kCombineBatch = 6;    // splits loaded together
 
-__global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t csmem[];
-  const uint32_t buf = ptx::smem_addr(csmem);
-  const uint32_t bar = buf + kCombineChunk * kCombineSplitBytes;
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
+__global__ void __launch_bounds__(kCombineWarps * 32, 3) mla_combine_kernel(const DecodeParams p) {
   // Launched as a programmatic dependent of the decode kernel: wait for it.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t* plan = p.plan;
@@ -257,10 +246,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const D
   constexpr int kQuadBlocks = (kDv / 4) / kCombineQuads;   // 32
   const int r = threadIdx.x & (kTileRows - 1);             // tile row of this thread
   const int qpair = threadIdx.x >> 7;                      // dim groups 2 qpair, 2 qpair + 1
-  uint32_t phase = 0;
-  bool ok = true;
   const int64_t total = (int64_t)p.batch * tiles * kQuadBlocks;
-  for (int64_t job = blockIdx.x; job < total && ok; job += gridDim.x) {
+  for (int64_t job = blockIdx.x; job < total; job += gridDim.x) {
     const int qb = (int)(job % kQuadBlocks);
     const int64_t item = job / kQuadBlocks;
     const int b = (int)(item % p.batch), t = (int)(item / p.batch);
@@ -274,70 +261,51 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const D
     }
     const int qr = t * kTileRows + r;
     const float* lse_col = p.ws_lse + slot0 * kTileRows + r;
-    // the first kCombineChunk lse values are loaded together (predicated)
-    float lj[kCombineChunk];
-#pragma unroll
-    for (int j = 0; j < kCombineChunk; ++j)
-      lj[j] = j < ns ? lse_col[(int64_t)j * kTileRows] : -INFINITY;
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kCombineChunk; ++j) m = fmaxf(m, lj[j]);
-    for (int j = kCombineChunk; j < ns; ++j) m = fmaxf(m, lse_col[(int64_t)j * kTileRows]);
-    float se = 0.f;
+    const float4* o_col = reinterpret_cast<const float4*>(p.ws_o) + slot0 * (kSlotFloats / 4) +
+                          (int64_t)(qb * kCombineQuads + 2 * qpair) * kTileRows + r;
+    // running merge over batches of splits (one batch in practice)
+    float m = -INFINITY, se = 0.f;
     float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
-    for (int c0 = 0; c0 < ns; c0 += kCombineChunk) {
-      const int nc = ns - c0 < kCombineChunk ? ns - c0 : kCombineChunk;
-      if (threadIdx.x == 0) {
-        ptx::mbar_arrive_expect_tx(bar, (uint32_t)nc * kCombineSplitBytes);
-        for (int j = 0; j < nc; ++j) {
-          const float* src = p.ws_o + (slot0 + c0 + j) * kSlotFloats +
-                             (int64_t)qb * kCombineQuads * kTileRows * 4;
-          ptx::bulk_load_global(buf + j * kCombineSplitBytes, src, kCombineSplitBytes, bar);
-        }
-      }
-      // weights of this chunk while the copies are in flight
-      float wj[kCombineChunk];
+    for (int c0 = 0; c0 < ns; c0 += kCombineBatch) {
+      const int nc = ns - c0 < kCombineBatch ? ns - c0 : kCombineBatch;
+      float lj[kCombineBatch];
+      float4 v0[kCombineBatch], v1[kCombineBatch];
 #pragma unroll
-      for (int j = 0; j < kCombineChunk; ++j) {
-        const float lv = c0 == 0 ? lj[j]
-                         : (j < nc ? lse_col[(int64_t)(c0 + j) * kTileRows] : -INFINITY);
-        wj[j] = (j < nc && m != -INFINITY) ? expf(lv - m) : 0.f;
-        se += wj[j];
-      }
-      // bounded wait for the chunk
-      if (!ptx::mbar_try_wait(bar, phase)) {
-        const uint64_t t0 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(bar, phase)) {
-          if (ptx::globaltimer() - t0 > kCombineWaitNs) {
-            ok = false;
-            break;
-          }
-        }
-      }
-      if (!__syncthreads_and(ok)) {
-        ok = false;
-        break;
-      }
-      phase ^= 1u;
-#pragma unroll
-      for (int j = 0; j < kCombineChunk; ++j) {
+      for (int j = 0; j < kCombineBatch; ++j) {
         if (j < nc) {
-          const uint32_t a = buf + j * kCombineSplitBytes + ((2 * qpair) * kTileRows + r) * 16;
-          const float4 v0 = ptx::ld_shared_v4f(a);
-          const float4 v1 = ptx::ld_shared_v4f(a + kTileRows * 16);
-          acc0.x += wj[j] * v0.x;
-          acc0.y += wj[j] * v0.y;
-          acc0.z += wj[j] * v0.z;
-          acc0.w += wj[j] * v0.w;
-          acc1.x += wj[j] * v1.x;
-          acc1.y += wj[j] * v1.y;
-          acc1.z += wj[j] * v1.z;
-          acc1.w += wj[j] * v1.w;
+          const int64_t s = c0 + j;
+          lj[j] = __ldcs(lse_col + s * kTileRows);
+          v0[j] = __ldcs(o_col + s * (kSlotFloats / 4));
+          v1[j] = __ldcs(o_col + s * (kSlotFloats / 4) + kTileRows);
+        } else {
+          lj[j] = -INFINITY;
+          v0[j] = v1[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
-      __syncthreads();   // the buffer is free for the next chunk or job
+      float mb = m;
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) mb = fmaxf(mb, lj[j]);
+      if (mb == -INFINITY) continue;                          // nothing visible yet
+      // rescale what was merged so far to the new max
+      const float sc = (m == -INFINITY) ? 0.f : expf(m - mb);
+      se *= sc;
+      acc0.x *= sc; acc0.y *= sc; acc0.z *= sc; acc0.w *= sc;
+      acc1.x *= sc; acc1.y *= sc; acc1.z *= sc; acc1.w *= sc;
+      m = mb;
+#pragma unroll
+      for (int j = 0; j < kCombineBatch; ++j) {
+        const float wj = (j < nc) ? expf(lj[j] - m) : 0.f;
+        se += wj;
+        acc0.x += wj * v0[j].x;
+        acc0.y += wj * v0[j].y;
+        acc0.z += wj * v0[j].z;
+        acc0.w += wj * v0[j].w;
+        acc1.x += wj * v1[j].x;
+        acc1.y += wj * v1[j].y;
+        acc1.z += wj * v1[j].z;
+        acc1.w += wj * v1[j].w;
+      }
     }
-    if (!ok) break;
     if (qr >= rows) continue;
     float lse = -INFINITY;
     if (m != -INFINITY) {
@@ -360,13 +328,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32) mla_combine_kernel(const D
                               (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv +
                               (qb * kCombineQuads + 2 * qpair) * 4) = u;
     if (qb == 0 && qpair == 0) p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
-  }
-  if (!ok) {
-    // a copy never completed: record it and let anything in flight land
-    // before the shared memory is released
-    if (threadIdx.x == 0) atomicCAS(p.err, 0, MLA_ERR_DEVICE_TIMEOUT);
-    const uint64_t t0 = ptx::globaltimer();
-    while (ptx::globaltimer() - t0 < 2000000ull) __nanosleep(1000);
   }
 }
 
@@ -397,9 +358,7 @@ int setup_device(int device) {
     } else {
       void* addr = nullptr;
       const int maxc = decode_max_clusters(device);
-      if (maxc <= 0 || cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess ||
-          cudaFuncSetAttribute(mla_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kCombineSmem) != cudaSuccess) {
+      if (maxc <= 0 || cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) {
         d.status = MLA_ERR_CUDA;
       } else {
         d.num_sms = sms;
@@ -682,7 +641,7 @@ cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kCombineWarps * 32);
-  cfg.dynamicSmemBytes = kCombineSmem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
