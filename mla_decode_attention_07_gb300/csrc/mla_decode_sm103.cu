@@ -74,8 +74,7 @@ namespace {
 
 // Warp roles (see above).  Warp w reaches TMEM lanes [32 (w % 4), +32).
 constexpr int kThreads = 384;
-constexpr int kRowWarps = 4;
-constexpr int kExchangeWarp0 = 4;
+constexpr int kQuadWarps = 4;   // page workers per set (one per TMEM lane quadrant)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPSendWarp = 10;
@@ -113,10 +112,15 @@ constexpr uint32_t kPBytes = 128 * 64 * 2;
 constexpr uint32_t kAlphaBufBytes = 2 * kHalfRows * 4;
 constexpr uint32_t kAlpha = kP + kPBufs * kPBytes;   // float[kPBufs][owner rank][64] rescale factors
 constexpr uint32_t kInvL = kAlpha + kPBufs * kAlphaBufBytes;   // float[2 parities][owner rank][64] 1/l
-constexpr uint32_t kBar = kInvL + 2 * 128 * 4;
-constexpr uint32_t kMisc = kBar + 8 * 40;
+constexpr uint32_t kHand = kInvL + 2 * 128 * 4;   // float[2 sets][4 quadrants][16] running max
+constexpr uint32_t kSums = kHand + 2 * 4 * 16 * 4;  // float[2 parities][4][32 lanes][3] set 1's sums
+constexpr uint32_t kBar = kSums + 2 * 4 * 32 * 12;
+constexpr uint32_t kMisc = kBar + 8 * 48;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
 static_assert(kP % 1024 == 0 && kStage0 % 1024 == 0, "swizzled buffers need 1 KB alignment");
+// Page g uses score tile, receive buffer and P buffer g % 2, and its worker
+// set is g % 2: every per-page barrier is then used by one set, in order.
+static_assert(kRBufs == 2 && kPBufs == 2, "buffers are paired with the page worker sets");
 static_assert(kSmemAlloc <= 232448, "shared memory");
 
 // Bytes moved per stage / per Q tile by one CTA.
@@ -143,10 +147,13 @@ enum Bar : uint32_t {
   B_PRECV = B_REMPTY + 2,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
   B_PFREE = B_PRECV + 2,      // [2] the peer's P buffer may take my next rows (peer's P.V done)
   B_LRECV = B_PFREE + 2,      // [2] the peer's 1/l for its rows arrived (per tile parity)
-  B_TEARDOWN = B_LRECV + 2,
+  B_HAND = B_LRECV + 2,       // [2 sets][4 quadrants] running max of the set's page handed on
+  B_SUMS = B_HAND + 8,        // [2] set 1's sums of a tile handed to set 0 (per tile parity)
+  B_SUMSFREE = B_SUMS + 2,    // [2] set 0 has read them
+  B_TEARDOWN = B_SUMSFREE + 2,
   B_COUNT,
 };
-static_assert(B_COUNT <= 40, "barrier space");
+static_assert(B_COUNT <= 48, "barrier space");
 
 struct Ctx {
   uint32_t sbase;       // 1024-aligned shared base
@@ -413,140 +420,91 @@ __device__ __forceinline__ void scale_o_rows(const Ctx& x, uint32_t lanes, float
   ptx::tmem_wait_st();
 }
 
-// ------------------------------------------------------------------ exchange warps
-// Warp 4 + q works on TMEM lane quadrant q.  Per tile, the four of them put
-// the latent half of Q into TMEM (one row per thread).  Per page, each ships
-// the peer's 16 rows of its quadrant: their partial scores, copied out of
-// TMEM (which frees the score tile) and stored with st.async into the peer's
-// receive buffer g % 2 as [16-byte chunk][owned row], completing on the
-// peer's barrier where the receiving side posted the byte count.  One page
-// later it imports the same rows' probabilities: once the peer's P rows and
-// rescale factors have landed in this CTA's P buffer, it rescales those rows
-// of O when a factor is not 1 and signals the P.V issuer.  Importing one page
-// behind keeps the next page's scores from waiting on the peer's softmax.
-__device__ __forceinline__ bool run_exchange(const Ctx& x, const Work& w, const DecodeParams& prm,
-                                             int e, int lane) {
-  const int r = e * 32 + lane;   // Q row of this thread
-  const uint32_t lane_base = (uint32_t)(e * 32) << 16;
-  const uint32_t peer_lanes = (uint32_t)(e * 32 + kSubRows * (int)x.peer) << 16;
-  const int hr = kSubRows * e + (lane & 15);   // the row's index among the peer's owned rows
-  const int half = lane >> 4;                   // score columns [32 half, 32 half + 32)
-  const uint32_t peer_row = ptx::map_to_rank(x.sbase + kRecv, x.peer) + (uint32_t)hr * 16u +
-                            (uint32_t)(8 * half) * (kHalfRows * 16);
-  const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
-  const uint32_t alpha_in = x.sbase + kAlpha + (x.peer * kHalfRows + (uint32_t)hr) * 4u;
-  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
-
-  auto import_page = [&](uint32_t gi) -> bool {
-    const uint32_t pbuf = gi % kPBufs;
-    if (!wait_warp(x, x.bar(B_PRECV + pbuf), (gi / kPBufs) & 1u, true)) return false;
-    const float alpha =
-        __uint_as_float(ptx::ld_shared_u32_volatile(alpha_in + pbuf * kAlphaBufBytes));
-    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-      // a rescale of O needs the P.V of page gi - 1 done (never the first
-      // page of a tile, whose factors are all 1)
-      if (kPBufs > 1 &&
-          !wait_warp(x, x.bar(B_PEMPTY + (gi - 1) % kPBufs), ((gi - 1) / kPBufs) & 1u))
-        return false;
-      ptx::tc_fence_after();
-      scale_o_rows(x, peer_lanes, alpha);
-    }
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
-    return true;
-  };
-
-  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
-  int b, pb, pe;
-  uint32_t g = 0, n_item = 0;
-  while (it.next(b, pb, pe)) {
-    // Q latent half of this tile -> TMEM columns [kColQ, kColQ + 128) once the
-    // previous tile's last score MMA is done.  Rows past the batch entry's
-    // query rows are zero.
-    if (!wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
-    const int qr = w.tile * kTileRows + r;
-    const bool valid = qr < w.rows;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        q + ((int64_t)b * w.rows + (valid ? qr : 0)) * kDqk + 256 * (int)x.rank);
-    // All 32 loads of the row are issued before the first use: the tile's
-    // first score MMA waits on this, so it costs one memory latency, not four.
-    uint4 qv[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) qv[j] = valid ? src[j] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-    for (int ch = 0; ch < 4; ++ch) {
-      uint32_t v[32];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[4 * j] = qv[ch * 8 + j].x;
-        v[4 * j + 1] = qv[ch * 8 + j].y;
-        v[4 * j + 2] = qv[ch * 8 + j].z;
-        v[4 * j + 3] = qv[ch * 8 + j].w;
-      }
-      ptx::tmem_st32(x.tmem + lane_base + kColQ + ch * 32, v);
-    }
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(x.bar(B_QFULL));
-
-    for (int pg = pb; pg < pe; ++pg, ++g) {
-      const uint32_t sb = g & 1u;
-      if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
-      ptx::tc_fence_after();
-      uint32_t v[32];
-      tmem_load16x2<32>(x.tmem + peer_lanes + kColS + sb * 64, v);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
-      // the peer has read what was sent into this buffer kRBufs pages ago
-      const uint32_t rb = g % kRBufs;
-      if (!wait_warp(x, x.bar(B_REMPTY + rb), ((g / kRBufs) & 1u) ^ 1u, true)) return false;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        ptx::st_async_v4(peer_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16),
-                         __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]),
-                         peer_rfull + 8u * rb);
-      if (pg > pb && !import_page(g - 1)) return false;
-    }
-    if (!import_page(g - 1)) return false;   // the tile's last page
-    ++n_item;
-  }
-  return true;
-}
-
-// ------------------------------------------------------------------ row warps
-// Warp q (0-3) owns the softmax of the 16 rows of lane quadrant q that belong
-// to this CTA (lanes 32 q + 16 r + [0, 16) in CTA r), two threads per row
-// with 32 of the page's 64 score columns each, so all four schedulers share
-// the softmax.  Per page: add the peer's partial scores for those rows, mask,
-// row max (the accum_s -> scores_max reduce: over the thread's 32 columns,
-// then with its partner's), exp2, sums, and the bf16 probabilities and
-// rescale factors into P buffer g % 2.  In the epilogue the warp writes O / l
-// for all 32 rows of its quadrant and this CTA's half of the output dims.
-__device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const DecodeParams& prm,
-                                         int warp, int lane) {
+// ------------------------------------------------------------------ page workers
+// Warps 0-3 (set 0) take the even pages of the CTA's work, warps 4-7 (set 1)
+// the odd ones; warp q of a set works on TMEM lane quadrant q, whose 32 rows
+// are 16 of this CTA's (lanes 32 q + 16 r + [0, 16) in CTA r) and 16 of the
+// peer's.  For its page, a worker
+//  A. copies the score tile's partial scores out of TMEM (which frees it for
+//     the page after next) and ships the peer's 16 rows with st.async into
+//     the peer's receive buffer, as [16-byte chunk][owned row];
+//  B. adds the peer's partial for its own 16 rows, two threads per row with
+//     32 of the page's 64 columns each, masks, and takes the row max (the
+//     accum_s -> scores_max reduce: over the thread's 32 columns, then with
+//     its partner's);
+//  C. takes the running max from the worker of the previous page (shared
+//     memory and an mbarrier per quadrant), decides the rescale, and hands
+//     the new running max on, so the online softmax stays sequential while
+//     the rest of two consecutive pages overlaps;
+//  D. writes the bf16 probabilities and rescale factors into P buffer g % 2
+//     and bulk-copies them into the same places in the peer (once the peer's
+//     buffer is free);
+//  E. imports the peer's probabilities for its peer rows (rescaling those rows
+//     of O when a factor is not 1) and signals the P.V issuer.
+// Each worker keeps the probability sums of its own pages, scaled to the
+// running max it last saw; at the end of a tile set 1 hands its sums to set
+// 0, which finishes the tile: O / l for all 32 rows of its quadrant and this
+// CTA's half of the output dims, and lse for its own rows.  Set 1 also puts
+// the latent half of each Q tile into TMEM (one row per thread).
+__device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const DecodeParams& prm,
+                                          int set, int quad, int lane) {
   const int half = lane >> 4;
   const int t = lane & 15;
-  const int ro = warp * 32 + kSubRows * (int)x.rank + t;   // owned tile row (TMEM lane)
-  const int hr = kSubRows * warp + t;                      // its owned-row index
-  const uint32_t own_lanes = (uint32_t)(warp * 32 + kSubRows * (int)x.rank) << 16;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)hr * 16u +
-                            (uint32_t)(8 * half) * (kHalfRows * 16);
+  const int ro = quad * 32 + kSubRows * (int)x.rank + t;   // owned tile row (TMEM lane)
+  const int hr = kSubRows * quad + t;                      // its owned-row index
+  const uint32_t own_lanes = (uint32_t)(quad * 32 + kSubRows * (int)x.rank) << 16;
+  const uint32_t peer_lanes = (uint32_t)(quad * 32 + kSubRows * (int)x.peer) << 16;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  const uint32_t chunk0 = (uint32_t)(8 * half) * (kHalfRows * 16);
+  const uint32_t recv_row = x.sbase + kRecv + (uint32_t)hr * 16u + chunk0;
+  const uint32_t peer_row = ptx::map_to_rank(x.sbase + kRecv, x.peer) + (uint32_t)hr * 16u + chunk0;
+  const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
   const uint32_t peer_rempty = ptx::map_to_rank(x.bar(B_REMPTY), x.peer);
-  const uint32_t peer_lrecv = ptx::map_to_rank(x.bar(B_LRECV), x.peer);
   const uint32_t peer_precv = ptx::map_to_rank(x.bar(B_PRECV), x.peer);
+  const uint32_t peer_lrecv = ptx::map_to_rank(x.bar(B_LRECV), x.peer);
   const uint32_t peer_base = ptx::map_to_rank(x.sbase, x.peer);
+  const uint32_t alpha_in = x.sbase + kAlpha + (x.peer * kHalfRows + (uint32_t)hr) * 4u;
+  const uint32_t hand_out = x.sbase + kHand + ((uint32_t)(set * 4 + quad) * kSubRows + t) * 4u;
+  const uint32_t hand_in = x.sbase + kHand + ((uint32_t)((set ^ 1) * 4 + quad) * kSubRows + t) * 4u;
   const uint32_t pswz = (uint32_t)(ro & 7);
   const float scale_log2 = prm.scale_log2;
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
 
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
   while (it.next(b, pb, pe)) {
+    if (set == 1) {
+      // Q latent half of this tile -> TMEM columns [kColQ, kColQ + 128) once
+      // the previous tile's last score MMA is done.  Rows past the batch
+      // entry's query rows are zero.  All 32 loads of the row are issued
+      // before the first use: the tile's first score MMA waits on this.
+      if (!wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
+      const int qr = w.tile * kTileRows + quad * 32 + lane;
+      const bool valid = qr < w.rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          q + ((int64_t)b * w.rows + (valid ? qr : 0)) * kDqk + 256 * (int)x.rank);
+      uint4 qv[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) qv[j] = valid ? src[j] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[4 * j] = qv[ch * 8 + j].x;
+          v[4 * j + 1] = qv[ch * 8 + j].y;
+          v[4 * j + 2] = qv[ch * 8 + j].z;
+          v[4 * j + 3] = qv[ch * 8 + j].w;
+        }
+        ptx::tmem_st32(x.tmem + lane_base + kColQ + ch * 32, v);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_QFULL));
+    }
+
     const int qo = w.tile * kTileRows + ro;
     const bool valid_o = qo < w.rows;
     const int io = qo / prm.h_q;
@@ -554,50 +512,62 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
     const int L = prm.seqlens[b];
     const int n_valid = valid_o ? L - prm.s_q + 1 + io : 0;
     const int P_total = w.items[b * kItemWords + 0];
-    // l_run sums the fp32 probabilities (for lse); lb_run sums them after the
-    // bf16 rounding the P.V MMA sees, so out = sum(p v) / sum(p) uses one set
-    // of weights and stays a true weighted average of the value rows.  Each
-    // thread sums its 32 columns; the partners' sums are added at the end.
+    // m_run: the running max this worker's sums are scaled to.  l_run sums
+    // the fp32 probabilities (for lse); lb_run sums them after the bf16
+    // rounding the P.V MMA sees, so out = sum(p v) / sum(p) uses one set of
+    // weights and stays a true weighted average of the value rows.  Each
+    // thread sums its 32 columns of this worker's pages.
     float m_run = -INFINITY, l_run = 0.f, lb_run = 0.f;
 
     for (int pg = pb; pg < pe; ++pg, ++g) {
+      if ((int)(g & 1u) != set) continue;
       const bool first = (pg == pb);
       const uint32_t sb = g & 1u;             // score tile
       const uint32_t rb = g % kRBufs;         // receive buffer
       const uint32_t pbuf = g % kPBufs;       // P buffer
-      // 1. Full scores of my rows: own partial (TMEM) + the peer's (received).
-      if (warp == 0 && lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + rb), kRecvBytes);
+
+      // A. Partial scores out of TMEM; the peer's rows to the peer.
+      if (quad == 0 && lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_RFULL + rb), kRecvBytes);
       if (!wait_warp(x, x.bar(B_SFULL + sb), (g >> 1) & 1u)) return false;
-      if (!wait_warp(x, x.bar(B_RFULL + rb), (g / kRBufs) & 1u, true)) return false;
       ptx::tc_fence_after();
+      uint32_t v[32];
       float s[32];
+      tmem_load16x2<32>(x.tmem + peer_lanes + kColS + sb * 64, v);
       {
-        uint32_t v[32];
-        tmem_load16x2<32>(x.tmem + own_lanes + kColS + sb * 64, v);
+        uint32_t u[32];
+        tmem_load16x2<32>(x.tmem + own_lanes + kColS + sb * 64, u);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(v[k]);
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        // addition commutes: the same sums whichever CTA owns the row
-        const float4 v = ptx::ld_shared_v4f(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(v.x, v.y)),
-                       s[4 * c], s[4 * c + 1]);
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(v.z, v.w)),
-                       s[4 * c + 2], s[4 * c + 3]);
+        for (int k = 0; k < 32; ++k) s[k] = __uint_as_float(u[k]);
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
+      // the peer has read what was sent into this buffer kRBufs pages ago
+      if (!wait_warp(x, x.bar(B_REMPTY + rb), ((g / kRBufs) & 1u) ^ 1u, true)) return false;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        ptx::st_async_v4(peer_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16),
+                         __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]),
+                         peer_rfull + 8u * rb);
 
-      // 2. Mask, row max (the accum_s -> scores_max reduce), exp2, sums.
+      // B. Full scores of my rows, mask, row max.
+      if (!wait_warp(x, x.bar(B_RFULL + rb), (g / kRBufs) & 1u, true)) return false;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        // addition commutes: the same sums whichever CTA owns the row
+        const float4 r4 = ptx::ld_shared_v4f(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(r4.x, r4.y)),
+                       s[4 * c], s[4 * c + 1]);
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(r4.z, r4.w)),
+                       s[4 * c + 2], s[4 * c + 3]);
+      }
       const int tok0 = pg * kPageTokens + 32 * half;
       if (__any_sync(0xffffffffu, tok0 + 32 > n_valid)) {
 #pragma unroll
         for (int k = 0; k < 32; ++k)
           if (tok0 + k >= n_valid) s[k] = -INFINITY;
       }
-      // four independent chains of 3-input maxima, then the partner's half
       float m4[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -612,15 +582,30 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       ptx::consume(mx);
       __syncwarp();
       if (lane == kRemoteLane) ptx::mbar_arrive_cluster_relaxed(peer_rempty + 8u * rb);
-      const float m_new = fmaxf(m_run, mx * scale_log2);   // scale_log2 > 0
-      const bool rescale = !first && (m_new > m_run + kRescaleThreshold);
-      const float alpha = rescale ? ptx::ex2(m_run - m_new) : 1.0f;
-      if (rescale) {
-        l_run *= alpha;
-        lb_run *= alpha;
+
+      // C. Running max: from the previous page's worker, to the next one's.
+      float m_ref = -INFINITY;
+      if (g > 0) {
+        if (!wait_warp(x, x.bar(B_HAND + (uint32_t)((set ^ 1) * 4 + quad)), ((g - 1) >> 1) & 1u))
+          return false;
+        if (!first) m_ref = __uint_as_float(ptx::ld_shared_u32_volatile(hand_in));
       }
-      if (rescale || first) m_run = m_new;
-      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+      const float m_cand = fmaxf(m_ref, mx * scale_log2);   // scale_log2 > 0
+      const bool rescale = !first && (m_cand > m_ref + kRescaleThreshold);
+      const float m_new = (first || rescale) ? m_cand : m_ref;
+      const float alpha = rescale ? ptx::ex2(m_ref - m_new) : 1.0f;   // O's factor
+      if (m_new != m_run) {
+        // this worker's sums were taken at an older running max
+        const float f = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m_new);
+        l_run *= f;
+        lb_run *= f;
+        m_run = m_new;
+      }
+      if (half == 0) ptx::st_shared_u32(hand_out, __float_as_uint(m_new));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_HAND + (uint32_t)(set * 4 + quad)));
+
+      const float neg_m = (m_new == -INFINITY) ? 0.f : -m_new;
       // exp2(s * scale - m) on pairs: the fma and the sums are f32x2 ops, and
       // the sums run as two independent chains
       uint32_t pk[16];
@@ -643,11 +628,11 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       l_run += pa + pc;
       lb_run += ba + bc;
 
-      // 3. P buffer g % 2 is free: my P.V of page g - 2 is done and the copy
-      //    of this warp's rows of page g - 2 to the peer has read them.  A
+      // D. P buffer g % 2 is free: my P.V of page g - 2 is done and this
+      //    warp's copy of page g - 2 to the peer has read its rows.  A
       //    rescale of O also needs the P.V of page g - 1 done.
       if (!wait_warp(x, x.bar(B_PEMPTY + pbuf), ((g / kPBufs) & 1u) ^ 1u)) return false;
-      if (lane == kRemoteLane) ptx::bulk_wait_read_but_1();
+      if (lane == kRemoteLane) ptx::bulk_wait_read_all();
       __syncwarp();
       if (__any_sync(0xffffffffu, rescale)) {
         if (kPBufs > 1 &&
@@ -659,12 +644,12 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       // Past the end of the sequence the cache slots of the last page hold
       // stale data; their probabilities are exactly 0 but 0 * NaN is NaN in
       // the P.V MMA, so zero those value rows first (each CTA zeroes its own
-      // stage, split between its four row warps).
+      // stage, split between the page's four workers).
       if (pg == P_total - 1 && (L & (kPageTokens - 1)) != 0) {
         const int t0 = L & (kPageTokens - 1);
         const uint32_t st = x.sbase + kStage0 + (g % kStages) * kStageBytes;
         const int n16 = (kPageTokens - t0) * 4 * 8;   // 16-byte pieces: rows x 4 boxes x 8
-        for (int idx = warp * 32 + lane; idx < n16; idx += kRowWarps * 32) {
+        for (int idx = quad * 32 + lane; idx < n16; idx += 4 * 32) {
           const int row = t0 + (idx >> 5), box = (idx >> 3) & 3, c16 = idx & 7;
           ptx::st_shared_v4(st + box * 8192 + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
         }
@@ -686,20 +671,63 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
-      // 4. This warp's 16 P rows (2 KB, contiguous in the swizzled buffer)
-      //    and their rescale factors into the same places in the peer, once
-      //    the peer's P.V of page g - 2 is done; they complete on the peer's
-      //    PRECV barrier.
+      // this warp's 16 P rows (2 KB, contiguous in the swizzled buffer) and
+      // their factors into the peer once its buffer is free; they complete on
+      // the peer's PRECV barrier
       if (!wait_warp(x, x.bar(B_PFREE + pbuf), (g / kPBufs) & 1u, true)) return false;
       if (lane == kRemoteLane) {
-        const uint32_t poff = kP + pbuf * kPBytes + (uint32_t)(warp * 32 + kSubRows * (int)x.rank) * 128u;
-        const uint32_t aoff = kAlpha + pbuf * kAlphaBufBytes + (x.rank * kHalfRows + kSubRows * warp) * 4u;
+        const uint32_t poff = kP + pbuf * kPBytes + (uint32_t)(quad * 32 + kSubRows * (int)x.rank) * 128u;
+        const uint32_t aoff = kAlpha + pbuf * kAlphaBufBytes + (x.rank * kHalfRows + kSubRows * quad) * 4u;
         ptx::bulk_copy_to_peer(peer_base + poff, x.sbase + poff, kSubRows * 128u, peer_precv + 8u * pbuf);
         ptx::bulk_copy_to_peer(peer_base + aoff, x.sbase + aoff, kSubRows * 4u, peer_precv + 8u * pbuf);
         ptx::bulk_commit();
       }
+
+      // E. The peer's rows of this page.
+      if (!wait_warp(x, x.bar(B_PRECV + pbuf), (g / kPBufs) & 1u, true)) return false;
+      const float alpha_p =
+          __uint_as_float(ptx::ld_shared_u32_volatile(alpha_in + pbuf * kAlphaBufBytes));
+      if (__any_sync(0xffffffffu, alpha_p != 1.0f)) {
+        if (kPBufs > 1 &&
+            !wait_warp(x, x.bar(B_PEMPTY + (g - 1) % kPBufs), ((g - 1) / kPBufs) & 1u))
+          return false;
+        ptx::tc_fence_after();
+        scale_o_rows(x, peer_lanes, alpha_p);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_PFULL + pbuf));
     }
 
+    // End of the tile.
+    const uint32_t par = n_item & 1u;
+    const uint32_t sums = x.sbase + kSums + ((par * 4 + (uint32_t)quad) * 32 + (uint32_t)lane) * 12u;
+    if (set == 1) {
+      // hand this worker's sums (and the max they are scaled to) to set 0,
+      // once set 0 has read those of the tile before last
+      if (!wait_warp(x, x.bar(B_SUMSFREE + par), ((n_item >> 1) & 1u) ^ 1u)) return false;
+      ptx::st_shared_u32(sums, __float_as_uint(m_run));
+      ptx::st_shared_u32(sums + 4, __float_as_uint(l_run));
+      ptx::st_shared_u32(sums + 8, __float_as_uint(lb_run));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_SUMS + par));
+      ++n_item;
+      continue;
+    }
+    if (!wait_warp(x, x.bar(B_SUMS + par), (n_item >> 1) & 1u)) return false;
+    {
+      const float m1 = __uint_as_float(ptx::ld_shared_u32_volatile(sums));
+      const float l1 = __uint_as_float(ptx::ld_shared_u32_volatile(sums + 4));
+      const float lb1 = __uint_as_float(ptx::ld_shared_u32_volatile(sums + 8));
+      const float m = fmaxf(m_run, m1);
+      const float f0 = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m);
+      const float f1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - m);
+      l_run = l_run * f0 + l1 * f1;
+      lb_run = lb_run * f0 + lb1 * f1;
+      m_run = m;
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(x.bar(B_SUMSFREE + par));
     // Epilogue: O / l for this CTA's dims of the warp's 32 rows; lse by the
     // row's owner.  The owners' sums are final after the last page: they send
     // 1/l of their rows to the peer and write lse before the last P.V is
@@ -707,7 +735,6 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
     // all that follows it.
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
     lb_run += __shfl_xor_sync(0xffffffffu, lb_run, 16);
-    const uint32_t par = n_item & 1u;
     const int ns = w.items[b * kItemWords + 1];
     const bool direct = (ns == 1);
     const int sidx = (n_item == 0) ? w.split0 : 0;
@@ -720,13 +747,13 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
     __syncwarp();
     if (lane == kRemoteLane) {
       // this warp's 16 values of 1/l
-      const uint32_t woff = kInvL + par * 512u + (x.rank * kHalfRows + kSubRows * warp) * 4u;
+      const uint32_t woff = kInvL + par * 512u + (x.rank * kHalfRows + kSubRows * quad) * 4u;
       ptx::bulk_copy_to_peer(ptx::map_to_rank(x.sbase + woff, x.peer), x.sbase + woff,
                              kSubRows * 4u, peer_lrecv + 8u * par);
       ptx::bulk_commit();
       ptx::bulk_wait_read_all();
     }
-    if (warp == 0 && lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_LRECV + par), kInvLTx);
+    if (quad == 0 && lane == 0) ptx::mbar_arrive_expect_tx(x.bar(B_LRECV + par), kInvLTx);
     if (half == 0 && valid_o) {
       const float lse_v = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       if (direct)
@@ -736,9 +763,9 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
     }
     if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
     if (!wait_warp(x, x.bar(B_LRECV + par), (n_item >> 1) & 1u, true)) return false;
-    // rows of the epilogue: lane -> tile row warp * 32 + lane (mine when its
+    // rows of the epilogue: lane -> tile row quad * 32 + lane (mine when its
     // half quadrant is this CTA's, and then this thread owned it)
-    const int re = warp * 32 + lane;
+    const int re = quad * 32 + lane;
     const float inv_l =
         (half == (int)x.rank)
             ? inv_own
@@ -752,36 +779,36 @@ __device__ __forceinline__ bool run_rows(const Ctx& x, const Work& w, const Deco
     ptx::tc_fence_after();
 #pragma unroll 1
     for (int ch = 0; ch < 8; ++ch) {
-      uint32_t v[32];
-      tmem_load32(x.tmem + lane_base + kColO + ch * 32, v);
+      uint32_t o[32];
+      tmem_load32(x.tmem + lane_base + kColO + ch * 32, o);
       if (valid_e) {
         const int d0 = (int)x.rank * 256 + ch * 32;
         if (direct) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
                                                 orow * kDv + d0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int qq = 0; qq < 4; ++qq) {
             uint4 u;
-            u.x = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 0]) * inv_l,
-                                   __uint_as_float(v[8 * q + 1]) * inv_l);
-            u.y = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv_l,
-                                   __uint_as_float(v[8 * q + 3]) * inv_l);
-            u.z = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv_l,
-                                   __uint_as_float(v[8 * q + 5]) * inv_l);
-            u.w = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv_l,
-                                   __uint_as_float(v[8 * q + 7]) * inv_l);
-            dst[q] = u;
+            u.x = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 0]) * inv_l,
+                                   __uint_as_float(o[8 * qq + 1]) * inv_l);
+            u.y = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 2]) * inv_l,
+                                   __uint_as_float(o[8 * qq + 3]) * inv_l);
+            u.z = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 4]) * inv_l,
+                                   __uint_as_float(o[8 * qq + 5]) * inv_l);
+            u.w = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 6]) * inv_l,
+                                   __uint_as_float(o[8 * qq + 7]) * inv_l);
+            dst[qq] = u;
           }
         } else {
           float4* base =
               reinterpret_cast<float4*>(prm.ws_o) + slot * (kDv / 4) * kTileRows + re;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            base[(int64_t)(d0 / 4 + q) * kTileRows] =
-                make_float4(__uint_as_float(v[4 * q]) * inv_l,
-                            __uint_as_float(v[4 * q + 1]) * inv_l,
-                            __uint_as_float(v[4 * q + 2]) * inv_l,
-                            __uint_as_float(v[4 * q + 3]) * inv_l);
+          for (int qq = 0; qq < 8; ++qq)
+            base[(int64_t)(d0 / 4 + qq) * kTileRows] =
+                make_float4(__uint_as_float(o[4 * qq]) * inv_l,
+                            __uint_as_float(o[4 * qq + 1]) * inv_l,
+                            __uint_as_float(o[4 * qq + 2]) * inv_l,
+                            __uint_as_float(o[4 * qq + 3]) * inv_l);
         }
       }
     }
@@ -842,17 +869,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(x.bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(B_SFULL + s), 1);
-      ptx::mbar_init(x.bar(B_SEMPTY + s), 8);   // 4 row + 4 exchange warps
+      ptx::mbar_init(x.bar(B_SEMPTY + s), 4);   // the page's 4 workers
       ptx::mbar_init(x.bar(B_RFULL + s), 1);    // own expect_tx + the peer's st.async bytes
-      ptx::mbar_init(x.bar(B_REMPTY + s), 4);   // the peer's 4 row warps (remote)
+      ptx::mbar_init(x.bar(B_REMPTY + s), 4);   // the peer's 4 workers of the page (remote)
       ptx::mbar_init(x.bar(B_LRECV + s), 1);    // own expect_tx + the peer's 1/l bytes
-      ptx::mbar_init(x.bar(B_PFULL + s), 8);    // 4 row warps (own rows) + 4 exchange warps (imported)
+      ptx::mbar_init(x.bar(B_PFULL + s), 8);    // the page's 4 workers: own rows, then imported rows
+      ptx::mbar_init(x.bar(B_SUMS + s), kQuadWarps);
+      ptx::mbar_init(x.bar(B_SUMSFREE + s), kQuadWarps);
       ptx::mbar_init(x.bar(B_PEMPTY + s), 1);
       ptx::mbar_init(x.bar(B_PRECV + s), 1);    // own expect_tx + the peer's P bytes
       ptx::mbar_init(x.bar(B_PFREE + s), 1);    // the peer's P notifier (remote)
     }
     ptx::mbar_init(x.bar(B_OFULL), 1);
-    ptx::mbar_init(x.bar(B_OEMPTY), kRowWarps);
+    for (int h = 0; h < 8; ++h) ptx::mbar_init(x.bar(B_HAND + h), 1);
+    ptx::mbar_init(x.bar(B_OEMPTY), kQuadWarps);
     ptx::mbar_init(x.bar(B_TEARDOWN), 2);   // both MMA-issuing threads
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
@@ -917,14 +947,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kPvWarp) {
     run_mma_pv(x, w);
     __syncwarp();
-  } else if (warp >= kExchangeWarp0 && warp < kExchangeWarp0 + 4) {
-    run_exchange(x, w, prm, warp - kExchangeWarp0, lane);
-    __syncwarp();
   } else if (warp == kPSendWarp) {
     if (lane == 0) run_pnotify(x, w);
     __syncwarp();
-  } else if (warp < kRowWarps) {
-    run_rows(x, w, prm, warp, lane);
+  } else if (warp < 2 * kQuadWarps) {
+    run_pages(x, w, prm, warp / kQuadWarps, warp % kQuadWarps, lane);
     __syncwarp();
   }
 
