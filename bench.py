@@ -91,16 +91,26 @@ def roofline_times(w: W.Workload, peaks):
     return t_mem, t_flop
 
 
-def traffic_per_launch():
-    """DRAM bytes per attend launch from the committed ncu summary, if the
-    kernel source is unchanged since it was captured."""
+def kernel_code_sha(path: str) -> str:
+    """sha256 of a CUDA source with its // comments and blank lines removed:
+    the code the counters were taken on, independent of comment edits."""
+    lines = []
+    for line in open(path, encoding="utf-8").read().splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code.strip():
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
+def traffic_per_launch(workload: str):
+    """DRAM bytes per attend launch from the committed ncu summary, if it was
+    taken on this workload and the kernel code is unchanged since."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
-        sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
-        if rec.get("source_sha256") != sha:
+        if rec.get("workload") != workload or rec.get("code_sha256") != kernel_code_sha(DECODE_SRC):
             return None
         return float(rec["dram_bytes_per_launch_full_workload"])
     except Exception:
@@ -368,7 +378,7 @@ def run_ours(args):
     else:
         achieved = w.flops() / attend_s / 1e12
         peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-    traffic = traffic_per_launch()
+    traffic = traffic_per_launch(w.name)
 
     result = {
         "metric": METRIC,

@@ -23,28 +23,28 @@
 //    rotary dims ([512 + 32 r, 512 + 32 r + 32)).  Each CTA therefore loads
 //    exactly 36 KB of every 72 KB page: the pair reads each page once, with
 //    no duplicated tensor work.
-//  * The softmax is split by rows: CTA r owns query rows [64 r, 64 r + 64).
-//    For every page it sends the peer the 64 x 64 fp32 partial scores of the
-//    peer's rows (16 KB), adds the peer's partial for its own rows, runs the
-//    online softmax for them and sends back their bf16 probabilities (8 KB)
-//    and rescale factors, so both CTAs hold P for all 128 rows for their
-//    halves of O.  All cross-SM traffic is TMA bulk copies between the two
-//    CTAs' shared memories, completed on mbarriers.  Distributed shared
-//    memory moves about 37 GB/s per SM on GB300, so the 24 KB per page this
-//    costs is close to the HBM time of a page; sending the whole 32 KB
-//    partial tile both ways would not be.
-//  * Warp roles: warps 0-3 own TMEM lanes 32w..32w+31 (= query rows); in
-//    CTA r the two warps on rows [64 r, 64 r + 64) run the softmax, the other
-//    two import the peer's probabilities (and rescale those rows of O).
-//    Warps 4-7 load Q's latent half into TMEM per tile, and the two of them on
-//    the peer's rows ship those rows' partial scores.  Warp 8 is the TMA
-//    producer, warp 9 issues the score MMAs and owns TMEM, warp 11 issues
-//    the P.V MMAs.  With two issuing threads a P.V that is ready never waits
-//    behind the issue of a score MMA chain (which stalls while the tensor
-//    pipe's queue is full), and the tensor pipe gets the two kinds
-//    interleaved, which hides much of the per-MMA latency of the dependent
-//    score chain.  One thread of warp 10 ships this CTA's probability rows
-//    to the peer, so the softmax warps go straight on to the next page.
+//  * The softmax is split by rows: CTA r owns 16 rows of every TMEM lane
+//    quadrant (lanes 32 q + 16 r + [0, 16)), 64 in all.  For every page it
+//    sends the peer the 64 x 64 fp32 partial scores of the peer's rows
+//    (16 KB, st.async), adds the peer's partial for its own rows, runs the
+//    online softmax for them and sends back their bf16 probabilities and
+//    rescale factors (8 KB, TMA bulk copies), so both CTAs hold P for all 128
+//    rows for their halves of O.  All cross-SM traffic goes into the peer's
+//    shared memory and completes on its mbarriers.  Distributed shared memory
+//    moves only a few tens of GB/s per SM on GB300, and these 48 KB in and
+//    out of each SM per page are what bounds the page rate; sending the whole
+//    32 KB partial tile both ways would be worse.
+//  * Page workers: warps 0-3 take the even pages of the CTA's work and warps
+//    4-7 the odd ones, warp q of a set working on lane quadrant q (its 16
+//    owned rows, two threads per row through the 16x32bx2 TMEM access shape,
+//    and its 16 peer rows).  A worker ships its page's partial scores, runs
+//    the softmax, copies out its probabilities and imports the peer's; the
+//    running row max passes from one page's worker to the next through
+//    shared memory and an mbarrier, so the online softmax stays sequential
+//    while two pages' chains of waits overlap.  Warp 8 is the TMA producer,
+//    warp 9 issues the score MMAs and owns TMEM, warp 11 issues the P.V MMAs
+//    (each from one elected lane of a converged warp), and one thread of
+//    warp 10 tells the peer when a P buffer is free.
 //  * A thread that has a remote operation in flight (a copy or an arrive on
 //    the peer's barrier) does not also signal the local barriers of the
 //    critical path: a release arrive may wait for that remote operation to
@@ -96,16 +96,14 @@ constexpr uint32_t kColQ = 384;   // Q's latent half, bf16x2: 128 rows x 256 dim
 // Shared memory (offsets from a 1024-byte aligned base).
 constexpr int kStages = 4;
 // Receive buffers for the peer's partial scores and P buffers: page g uses
-// buffer g % k.  Two of each measured no faster than one (the score tiles in
-// TMEM are double buffered, which is what lets the next page's scores run
-// under this page's softmax), so one of each leaves the shared memory free.
+// buffer g % 2, like its score tile and its worker set.
 constexpr int kRBufs = 2;
 constexpr int kPBufs = 2;
 constexpr uint32_t kQRope = 0;            // [128 x 32] bf16, 64-byte swizzle
 constexpr uint32_t kStage0 = 8192;        // kStages x 36 KB
 constexpr uint32_t kStageBytes = 36864;
 constexpr uint32_t kStageRope = 32768;    // rotary box inside a stage
-constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][64 rows] x 16 B
+constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][64 owned rows] x 16 B
 constexpr uint32_t kRecvBytes = kHalfRows * 64 * 4;
 constexpr uint32_t kP = kRecv + kRBufs * kRecvBytes;  // kPBufs x [128 x 64] bf16, 128-byte swizzle
 constexpr uint32_t kPBytes = 128 * 64 * 2;
@@ -129,21 +127,21 @@ constexpr uint32_t kQRopeTx = 8192;
 constexpr uint32_t kPRecvTx = kHalfRows * 128 + kHalfRows * 4;   // the peer's 64 P rows + factors
 constexpr uint32_t kInvLTx = kHalfRows * 4;                        // the peer's 64 values of 1/l
 
-// [2] = one per buffer: page g uses score tile g % 2, receive buffer
-// g % kRBufs and P buffer g % kPBufs.
+// [2] = one per buffer: page g uses score tile, receive buffer and P buffer
+// g % 2.  "Workers" are the page's four workers (the set g % 2).
 enum Bar : uint32_t {
   B_FULL = 0,                 // [kStages] stage loaded (TMA tx)
   B_EMPTY = kStages,          // [kStages] stage consumed (MMA commit)
-  B_QFULL = 2 * kStages,      // Q tile ready: rotary half (TMA) + latent half (4 exchange warps)
+  B_QFULL = 2 * kStages,      // Q tile ready: rotary half (TMA) + latent half (set 1's 4 warps)
   B_QEMPTY,                   // last score MMA of a tile done
   B_SFULL,                    // [2] score tile ready (MMA commit)
-  B_SEMPTY = B_SFULL + 2,     // [2] score tile read (2 softmax warps + 2 sending warps)
-  B_PFULL = B_SEMPTY + 2,     // [2] all 128 rows of P in shared memory and O rescaled (4 row warps)
+  B_SEMPTY = B_SFULL + 2,     // [2] score tile read (the page's 4 workers)
+  B_PFULL = B_SEMPTY + 2,     // [2] all 128 rows of P in shared memory and O rescaled (4 workers x 2)
   B_PEMPTY = B_PFULL + 2,     // [2] P.V done (MMA commit)
   B_OFULL = B_PEMPTY + 2,
-  B_OEMPTY,                   // 4 row warps
+  B_OEMPTY,                   // set 0's 4 warps have drained O
   B_RFULL,                    // [2] the peer's partial scores for my rows (st.async tx)
-  B_REMPTY = B_RFULL + 2,     // [2] the peer's softmax warps have read what I sent (2 remote arrives)
+  B_REMPTY = B_RFULL + 2,     // [2] the peer's workers have read what I sent (4 remote arrives)
   B_PRECV = B_REMPTY + 2,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
   B_PFREE = B_PRECV + 2,      // [2] the peer's P buffer may take my next rows (peer's P.V done)
   B_LRECV = B_PFREE + 2,      // [2] the peer's 1/l for its rows arrived (per tile parity)
