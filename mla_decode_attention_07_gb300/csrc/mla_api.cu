@@ -65,6 +65,11 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const int32_t* s
   // The decode kernel may launch now: it reads the plan only after waiting
   // for this grid to complete.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // This grid is itself launched as a programmatic dependent of whatever
+  // precedes it on the stream (typically the previous step's combine, which
+  // still reads the plan buffer): wait for it to complete before reading the
+  // lengths or writing the plan.  Being launched early hides the launch.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tiles = plan_tiles(s_q, h_q);
   const int gt = plan_group_clusters(num_clusters, tiles);
   int64_t* starts_g = reinterpret_cast<int64_t*>(reinterpret_cast<char*>(plan) +
@@ -470,9 +475,21 @@ int mla_decode_plan(const int32_t* cache_seqlens, int batch, int s_q, int h_q, v
   const size_t smem = batch <= kPlanSmemBatch
                           ? sizeof(int64_t) * (size_t)(batch + 1) + sizeof(int32_t) * (size_t)batch
                           : 0;
-  mla_plan_kernel<<<1, kPlanThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      cache_seqlens, batch, s_q, h_q, d.num_clusters, static_cast<int32_t*>(tile_meta), d.err);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_plan_kernel, cache_seqlens, batch, s_q, h_q,
+                            d.num_clusters, static_cast<int32_t*>(tile_meta), d.err) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // extern "C"
