@@ -30,7 +30,7 @@ namespace mla {
 
 constexpr int kPageTokens = 64;
 constexpr int kTileRows = 128;
-constexpr int kSplitOverhead = 4;   // virtual units charged per batch entry (measured: ~4 pages)
+constexpr int kSplitOverhead = 6;   // virtual units charged per batch entry (best of 2/4/6/8 measured)
 constexpr int kMinUnitsPerCluster = 4;
 constexpr int kPlanMagic = 0x4D4C4131;  // "MLA1"
 

@@ -75,7 +75,38 @@ SMALL = [
     (109, 1, 1, 8, [77], 0),
     (110, 3, 2, 100, [333, 90, 1], 1),
     (111, 16, 1, 128, [640] * 16, 0),
+    # many one-page entries: every cluster gets several tiles whose pages
+    # alternate between the two page-worker sets (a tile can have no page of
+    # one set), which exercises the running-max and sums hand-offs
+    (112, 300, 1, 128, list(W.uniform_int(112, W.TENSOR_SEQLENS, 300, 1, 64)), 0),
+    (113, 200, 2, 64, list(W.uniform_int(113, W.TENSOR_SEQLENS, 200, 0, 256)), 1),
 ]
+
+
+# Cases whose rows see only a handful of keys: the probabilities reach the
+# P.V product rounded to bf16 (relative error <= 2^-9 each), so the output,
+# a weighted average of value rows, is off by at most 2^-8 * max|v - out|,
+# plus the bf16 rounding of out itself (2^-9 |out|).  With one to 64 keys per
+# row a single weight can carry most of the mass and that bound exceeds the
+# workloads' fixed 1e-2 (a CPU model of exactly this rounding reproduces the
+# GPU's largest error on case 112); these cases are held to the bound.
+SHORT_ROWS = {112}
+
+
+def bf16_rounding_bound(inp, ref_o):
+    """Elementwise bound on |out - exact| from bf16 P and bf16 out."""
+    v = (inp.kv_cache.view(np.uint16).astype(np.uint32) << 16).view(np.float32)[:, :, 0, :512]
+    bound = np.zeros_like(ref_o)
+    for b in range(inp.batch):
+        L = int(inp.cache_seqlens[b])
+        pages = [int(inp.block_table[b, p]) for p in range((L + 63) // 64)]
+        if not pages:
+            continue
+        rows = np.concatenate([v[p] for p in pages])[:L]
+        vmax = np.abs(rows).max(axis=0).astype(np.float64)          # [512]
+        o = np.abs(ref_o[b])
+        bound[b] = 2.0 ** -8 * (vmax + o) + 2.0 ** -9 * o + 1e-5
+    return bound
 
 
 @pytest.mark.parametrize("case", SMALL, ids=lambda c: f"s{c[0]}_b{c[1]}_sq{c[2]}_h{c[3]}")
@@ -84,6 +115,15 @@ def test_small_parity(torch_cuda, case, oracle_mod):
     inp = W.make_inputs(seed, B, s_q, h_q, seqlens, extra_pages=extra)
     out, lse, _ = run_gpu(torch_cuda, inp)
     ref_o, ref_l = oracle_mod.mla_decode(inp)
+    if seed in SHORT_ROWS:
+        assert not np.isnan(out).any() and not np.isnan(lse).any()
+        assert np.array_equal(np.isneginf(lse), np.isneginf(ref_l))
+        err = np.abs(out.astype(np.float64) - ref_o)
+        bound = bf16_rounding_bound(inp, ref_o)
+        assert (err <= bound).all(), f"case {seed}: max err/bound {float((err / bound).max()):.3f}"
+        fin = ~np.isneginf(ref_l)
+        assert np.abs(lse[fin] - ref_l[fin]).max() <= LSE_TOL
+        return
     assert_parity(out, lse, ref_o, ref_l, f"case {seed}")
 
 

@@ -28,6 +28,7 @@ CASES = [
     (list(W.uniform_int(7, 9, 300, 0, 3000)), 1, 128, 75),
     ([5000, 3, 70000, 64], 1, 128, 5),
     ([100] * 20, 3, 100, 74),
+    (list(W.uniform_int(112, W.TENSOR_SEQLENS, 300, 1, 64)), 1, 128, 76),
 ]
 
 
