@@ -238,9 +238,13 @@ void plan_host(const int32_t* seqlens, int batch, int s_q, int h_q, int num_clus
 // to kCombineBatch splits at a time) are issued before the first use: the
 // job costs about one memory latency after its plan entry is read.
 constexpr int kCombineQuads = 4;    // dim groups (of 4) per job
-constexpr int kCombineBatch = 6;    // splits loaded together
 
-__global__ void __launch_bounds__(kCombineWarps * 32, 3) mla_combine_kernel(const DecodeParams p) {
+// BATCH splits loaded together; MINB CTAs per SM (the register budget that
+// allows).  Six splits at three CTAs per SM, or four at four: the launch picks
+// the form that runs its jobs in fewer waves.
+template <int BATCH, int MINB>
+__global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(const DecodeParams p) {
+  constexpr int kCombineBatch = BATCH;
   // Launched as a programmatic dependent of the decode kernel: wait for it.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int32_t* plan = p.plan;
@@ -653,7 +657,9 @@ cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_
                            cudaStream_t stream) {
   const int tiles = plan_tiles(p.s_q, p.h_q);
   const int64_t jobs = (int64_t)p.batch * tiles * ((kDv / 4) / kCombineQuads);
-  const int64_t cap = (int64_t)num_sms * 4;
+  // four CTAs per SM only when three would need another wave
+  const bool four = jobs > (int64_t)num_sms * 3;
+  const int64_t cap = (int64_t)num_sms * (four ? 4 : 3);
   const int grid = (int)(jobs < cap ? jobs : cap);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -665,6 +671,7 @@ cudaError_t launch_combine(const DecodeParams& p, int /*num_clusters*/, int num_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
+  return four ? cudaLaunchKernelEx(&cfg, mla_combine_kernel<4, 4>, p)
+              : cudaLaunchKernelEx(&cfg, mla_combine_kernel<6, 3>, p);
 }
 }  // namespace mla
