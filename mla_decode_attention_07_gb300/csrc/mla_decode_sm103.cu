@@ -25,15 +25,17 @@
 //    no duplicated tensor work.
 //  * The softmax is split by rows: CTA r owns 16 rows of every TMEM lane
 //    quadrant (lanes 32 q + 16 r + [0, 16)), 64 in all.  For every page it
-//    sends the peer the 64 x 64 fp32 partial scores of the peer's rows
-//    (16 KB, st.async), adds the peer's partial for its own rows, runs the
+//    sends the peer the 64 x 64 partial scores of the peer's rows (12 KB:
+//    fp32 rounded to 24-bit floats, relative error <= 2^-16, within what the
+//    fp32 accumulation of the 288 products already allows; st.async), adds
+//    the peer's partial for its own rows, runs the
 //    online softmax for them and sends back their bf16 probabilities and
 //    rescale factors (8 KB, TMA bulk copies), so both CTAs hold P for all 128
 //    rows for their halves of O.  All cross-SM traffic goes into the peer's
 //    shared memory and completes on its mbarriers.  Distributed shared memory
-//    moves only a few tens of GB/s per SM on GB300, and these 48 KB in and
-//    out of each SM per page are what bounds the page rate; sending the whole
-//    32 KB partial tile both ways would be worse.
+//    moves only about 40 GB/s out of each SM on GB300, and these transfers
+//    (about 20 KB each way per page) are what bounds the page rate; sending
+//    the whole 32 KB partial tile both ways would be worse.
 //  * Page workers: warps 0-3 take the even pages of the CTA's work and warps
 //    4-7 the odd ones, warp q of a set working on lane quadrant q (its 16
 //    owned rows, two threads per row through the 16x32bx2 TMEM access shape,
@@ -103,8 +105,11 @@ constexpr uint32_t kQRope = 0;            // [128 x 32] bf16, 64-byte swizzle
 constexpr uint32_t kStage0 = 8192;        // kStages x 36 KB
 constexpr uint32_t kStageBytes = 36864;
 constexpr uint32_t kStageRope = 32768;    // rotary box inside a stage
-constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [16 chunks][64 owned rows] x 16 B
-constexpr uint32_t kRecvBytes = kHalfRows * 64 * 4;
+// The peer's partial scores of my rows arrive as 24-bit floats, 64 columns =
+// 192 bytes = 12 chunks of 16 bytes per row: [12 chunks][64 owned rows].
+constexpr uint32_t kRecvChunks = 12;
+constexpr uint32_t kRecv = kStage0 + kStages * kStageBytes;  // 2 x [12 chunks][64 owned rows] x 16 B
+constexpr uint32_t kRecvBytes = kHalfRows * kRecvChunks * 16;
 constexpr uint32_t kP = kRecv + kRBufs * kRecvBytes;  // kPBufs x [128 x 64] bf16, 128-byte swizzle
 constexpr uint32_t kPBytes = 128 * 64 * 2;
 constexpr uint32_t kAlphaBufBytes = 2 * kHalfRows * 4;
@@ -453,7 +458,7 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
   const uint32_t own_lanes = (uint32_t)(quad * 32 + kSubRows * (int)x.rank) << 16;
   const uint32_t peer_lanes = (uint32_t)(quad * 32 + kSubRows * (int)x.peer) << 16;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-  const uint32_t chunk0 = (uint32_t)(8 * half) * (kHalfRows * 16);
+  const uint32_t chunk0 = (uint32_t)(6 * half) * (kHalfRows * 16);
   const uint32_t recv_row = x.sbase + kRecv + (uint32_t)hr * 16u + chunk0;
   const uint32_t peer_row = ptx::map_to_rank(x.sbase + kRecv, x.peer) + (uint32_t)hr * 16u + chunk0;
   const uint32_t peer_rfull = ptx::map_to_rank(x.bar(B_RFULL), x.peer);
@@ -542,23 +547,42 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
       if (lane == 0) ptx::mbar_arrive(x.bar(B_SEMPTY + sb));
       // the peer has read what was sent into this buffer kRBufs pages ago
       if (!wait_warp(x, x.bar(B_REMPTY + rb), ((g / kRBufs) & 1u) ^ 1u, true)) return false;
+      // 24-bit floats: the rounding (<= 2^-16 relative) is within what the
+      // fp32 accumulation of these 288 products already allows (288 x 2^-24
+      // of the sum of their magnitudes), and the transfer, which bounds the
+      // page rate, shrinks by a quarter
+      uint32_t w24[24];
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        ptx::st_async_v4(peer_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16),
-                         __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]),
-                         peer_rfull + 8u * rb);
+      for (int j = 0; j < 8; ++j)
+        ptx::pack24x4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3], w24[3 * j],
+                      w24[3 * j + 1], w24[3 * j + 2]);
+#pragma unroll
+      for (int c = 0; c < 6; ++c)
+        ptx::st_async_v4_b32(peer_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16),
+                             w24[4 * c], w24[4 * c + 1], w24[4 * c + 2], w24[4 * c + 3],
+                             peer_rfull + 8u * rb);
 
       // B. Full scores of my rows, mask, row max.
       if (!wait_warp(x, x.bar(B_RFULL + rb), (g / kRBufs) & 1u, true)) return false;
+      {
+        uint32_t w24[24];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        // addition commutes: the same sums whichever CTA owns the row
-        const float4 r4 = ptx::ld_shared_v4f(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c], s[4 * c + 1]), ptx::f2_pack(r4.x, r4.y)),
-                       s[4 * c], s[4 * c + 1]);
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * c + 2], s[4 * c + 3]), ptx::f2_pack(r4.z, r4.w)),
-                       s[4 * c + 2], s[4 * c + 3]);
+        for (int c = 0; c < 6; ++c) {
+          const uint4 r4 = ptx::ld_shared_v4u(recv_row + rb * kRecvBytes + (uint32_t)c * (kHalfRows * 16));
+          w24[4 * c] = r4.x;
+          w24[4 * c + 1] = r4.y;
+          w24[4 * c + 2] = r4.z;
+          w24[4 * c + 3] = r4.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float a, bq, c2, d;
+          ptx::unpack24x4(w24[3 * j], w24[3 * j + 1], w24[3 * j + 2], a, bq, c2, d);
+          ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * j], s[4 * j + 1]), ptx::f2_pack(a, bq)),
+                         s[4 * j], s[4 * j + 1]);
+          ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(s[4 * j + 2], s[4 * j + 3]), ptx::f2_pack(c2, d)),
+                         s[4 * j + 2], s[4 * j + 3]);
+        }
       }
       const int tok0 = pg * kPageTokens + 32 * half;
       if (__any_sync(0xffffffffu, tok0 + 32 > n_valid)) {

@@ -61,6 +61,36 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
       : "memory");
 }
 
+// The same for four 32-bit words.
+__device__ __forceinline__ void st_async_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                                uint32_t d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+      : "memory");
+}
+
+// Four fp32 values as 24-bit floats (sign, exponent and the top 15 mantissa
+// bits, rounded to nearest with ties away from zero: relative error at most
+// 2^-16; zero stays zero) packed into three words, and back.
+__device__ __forceinline__ void pack24x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                         uint32_t& w0, uint32_t& w1, uint32_t& w2) {
+  a += 0x80u;
+  b += 0x80u;
+  c += 0x80u;
+  d += 0x80u;
+  w0 = __byte_perm(a, b, 0x5321);   // a1 a2 a3 b1
+  w1 = __byte_perm(b, c, 0x6532);   // b2 b3 c1 c2
+  w2 = __byte_perm(c, d, 0x7653);   // c3 d1 d2 d3
+}
+__device__ __forceinline__ void unpack24x4(uint32_t w0, uint32_t w1, uint32_t w2, float& a,
+                                           float& b, float& c, float& d) {
+  a = __uint_as_float(__byte_perm(w0, 0u, 0x2104));
+  b = __uint_as_float(__byte_perm(w0, w1, 0x5433) & 0xFFFFFF00u);
+  c = __uint_as_float(__byte_perm(w1, w2, 0x4322) & 0xFFFFFF00u);
+  d = __uint_as_float(__byte_perm(w2, 0u, 0x3214));
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -407,6 +437,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4u(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
   float4 v;
