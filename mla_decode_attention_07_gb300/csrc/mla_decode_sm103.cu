@@ -79,7 +79,7 @@ constexpr int kThreads = 384;
 constexpr int kQuadWarps = 4;   // page workers per set (one per TMEM lane quadrant)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kPSendWarp = 10;
+constexpr int kPSendWarp = 10;   // the P notifier thread
 constexpr int kPvWarp = 11;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after an abort
@@ -845,7 +845,7 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
 // ------------------------------------------------------------------ P notifier
 // One thread.  Per page g: once this CTA's P.V of page g - 2 is done, its P
 // buffer g % 2 may take the peer's rows of page g: post their byte count on
-// PRECV and tell the peer (whose row warps then copy their rows in).
+// PRECV and tell the peer (whose page workers then copy their rows in).
 __device__ __forceinline__ bool run_pnotify(const Ctx& x, const Work& w) {
   const uint32_t peer_pfree = ptx::map_to_rank(x.bar(B_PFREE), x.peer);
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
@@ -887,7 +887,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(x.bar(B_FULL + s), 1);
       ptx::mbar_init(x.bar(B_EMPTY + s), 1);
     }
-    ptx::mbar_init(x.bar(B_QFULL), 1 + 4);   // rotary TMA + 4 exchange warps
+    ptx::mbar_init(x.bar(B_QFULL), 1 + 4);   // rotary TMA + set 1's 4 warps
     ptx::mbar_init(x.bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(B_SFULL + s), 1);
