@@ -30,6 +30,14 @@
  *   out          bf16  [batch, s_q, h_q, 512]        device
  *   lse          fp32  [batch, h_q, s_q]             device
  *
+ * Arithmetic: bf16 inputs; q.k and P.V products accumulate in fp32 on the
+ * tensor cores.  The 576-wide q.k of a row is summed in two halves on the
+ * two SMs of a cluster; the half that crosses to the row's owner is rounded
+ * to a 24-bit float (relative error <= 2^-16, within the fp32 accumulation's
+ * own bound for those 288 products).  Probabilities enter P.V as bf16; out is
+ * normalised by the sum of those bf16 probabilities and rounded to bf16; lse
+ * comes from the fp32 sums.
+ *
  * Ownership: the caller owns every buffer; the library allocates nothing on
  * any call.  Asynchrony: every call that takes a stream only enqueues work on
  * it and returns; errors found on the host are returned before anything is
