@@ -245,12 +245,29 @@ constexpr int kCombineQuads = 4;    // dim groups (of 4) per job
 template <int BATCH, int MINB>
 __global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(const DecodeParams p) {
   constexpr int kCombineBatch = BATCH;
-  // Launched as a programmatic dependent of the decode kernel: wait for it.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Launched as a programmatic dependent of the decode kernel, whose blocks
+  // let this grid launch only after their own wait on the planner had
+  // returned: the plan is complete and visible here, so it is read (past L1)
+  // before the wait.  The partials are not, and no output is written before
+  // the wait; every block waits once, so that this grid completes only after
+  // the decode kernel has.  One thread per block reads the plan words into
+  // shared memory: every block reads the same few words, and one L2 request
+  // per block instead of one per warp keeps that line from becoming a hot
+  // spot.
   const int32_t* plan = p.plan;
-  const int tiles = plan[H_TILES], gt = plan[H_GT], stotal = plan[H_STOTAL];
+  __shared__ int s_hdr[4];
+  __shared__ int s_item[2];
+  if (threadIdx.x == 0) {
+    s_hdr[0] = __ldcg(plan + H_TILES);
+    s_hdr[1] = __ldcg(plan + H_GT);
+    s_hdr[2] = __ldcg(plan + H_STOTAL);
+    s_hdr[3] = __ldcg(plan + H_NCLUSTERS);
+  }
+  __syncthreads();
+  const int tiles = s_hdr[0], gt = s_hdr[1], stotal = s_hdr[2];
   const int32_t* items = plan + plan_off_items(gt) / 4;
-  const int64_t max_slots = workspace_slots(plan[H_NCLUSTERS]);
+  const int64_t max_slots = workspace_slots(s_hdr[3]);
+  bool waited = false;
   const int rows = p.s_q * p.h_q;
   constexpr int kQuadBlocks = (kDv / 4) / kCombineQuads;   // 32
   const int r = threadIdx.x & (kTileRows - 1);             // tile row of this thread
@@ -260,13 +277,23 @@ __global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(c
     const int qb = (int)(job % kQuadBlocks);
     const int64_t item = job / kQuadBlocks;
     const int b = (int)(item % p.batch), t = (int)(item / p.batch);
-    const int ns = items[b * kItemWords + 1];
+    __syncthreads();                                         // the last job's s_item is read
+    if (threadIdx.x == 0) {
+      s_item[0] = __ldcg(items + b * kItemWords + 1);
+      s_item[1] = __ldcg(items + b * kItemWords + 2);
+    }
+    __syncthreads();
+    const int ns = s_item[0];
     if (ns == 1) continue;                                   // written by the main kernel
     if (t * kTileRows >= rows) continue;                      // padding tile
-    const int64_t slot0 = (int64_t)t * stotal + items[b * kItemWords + 2];
+    const int64_t slot0 = (int64_t)t * stotal + s_item[1];
     if (ns > 1 && (slot0 < 0 || slot0 + ns > max_slots)) {
       if (threadIdx.x == 0) atomicCAS(p.err, 0, MLA_ERR_PLAN);
       continue;
+    }
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      waited = true;
     }
     const int qr = t * kTileRows + r;
     const float* lse_col = p.ws_lse + slot0 * kTileRows + r;
@@ -338,6 +365,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(c
                               (qb * kCombineQuads + 2 * qpair) * 4) = u;
     if (qb == 0 && qpair == 0) p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
   }
+  if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ device state
