@@ -17,6 +17,9 @@ Shapes (DeepSeek-style MLA decode over a paged latent cache):
   kv_cache     [num_pages, 64, 1, 576] bf16 (uint16 bits)
   block_table  [B, max_pages]          int32
   cache_seqlens[B]                     int32
+Sparse decode adds, with s_q = 1:
+  indices      [B, topk]               int32 token positions, -1 past counts[b]
+  counts       [B]                     int32 selected positions per entry
 """
 from __future__ import annotations
 
@@ -38,6 +41,8 @@ TENSOR_Q = 0x51
 TENSOR_KV = 0x4B56
 TENSOR_SEQLENS = 0x5345
 TENSOR_PERM = 0x5045
+TENSOR_IDX = 0x4958        # sparse: token positions selected per batch entry
+TENSOR_POOL = 0x504C       # sparse: block-table draws into a shared page pool
 
 BF16_NAN = np.uint16(0x7FC0)
 
@@ -237,4 +242,108 @@ WORKLOADS = {
                                          seqlen=8192, seed=3),
     "long_b8_h16_l65536": Workload("long_b8_h16_l65536", batch=8, s_q=1, h_q=16, seqlen=65536,
                                    seed=4),
+}
+
+
+@dataclasses.dataclass
+class SparseInputs:
+    """Sparse decode inputs: a paged cache (``base``, s_q = 1) plus, per batch
+    entry, the list of token positions its query attends to."""
+    base: DecodeInputs
+    indices: np.ndarray      # int32 [B, topk]; entries past counts[b] are -1
+    counts: np.ndarray       # int32 [B]
+
+    @property
+    def topk(self) -> int:
+        return int(self.indices.shape[1])
+
+
+def draw_indices(seed: int, seqlens, topk: int, counts=None, *,
+                 repeats: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Per entry b, ``counts[b]`` token positions in [0, L_b) (default
+    min(topk, L_b)) in random order: distinct (a random subset), or with
+    ``repeats`` drawn independently.  Slots past counts[b] hold -1."""
+    seqlens = np.asarray(seqlens, dtype=np.int64)
+    B = seqlens.shape[0]
+    if counts is None:
+        counts = np.minimum(seqlens, topk)
+    counts = np.asarray(counts, dtype=np.int32).reshape(B)
+    idx = np.full((B, topk), -1, dtype=np.int32)
+    for b in range(B):
+        L, c = int(seqlens[b]), int(counts[b])
+        if c == 0:
+            continue
+        if c > topk or (c > L and not repeats) or L == 0:
+            raise ValueError("count out of range")
+        sb = (seed * 1000003 + b) & 0xFFFFFFFFFFFFFFFF
+        if repeats:
+            z = splitmix64(sb ^ TENSOR_IDX, 0, c)
+            idx[b, :c] = (z % np.uint64(L)).astype(np.int64)
+        else:
+            z = splitmix64(sb ^ TENSOR_IDX, 0, L)
+            idx[b, :c] = np.argsort(z, kind="stable")[:c]
+    return idx, counts
+
+
+def make_sparse_inputs(seed: int, batch: int, h_q: int, seqlens, topk: int, counts=None, *,
+                       repeats: bool = False, pool_pages: int | None = None,
+                       poison: bool = True) -> SparseInputs:
+    """Seeded sparse decode inputs (one query token per entry).
+
+    Without ``pool_pages`` the cache is ``make_inputs``' (every live page
+    once, NaN-poisoned tails and decoys).  With it, the cache is a shared
+    pool of that many pages and every block-table entry is a uniform draw
+    from the pool, so long contexts need not be stored in full (pages repeat
+    across and within entries, as with a shared prefix)."""
+    seqlens = np.asarray(seqlens, dtype=np.int32).reshape(batch)
+    if pool_pages is None:
+        base = make_inputs(seed, batch, 1, h_q, seqlens, extra_pages=2, poison=poison)
+    else:
+        max_pages = max(1, max((int(L) + PAGE - 1) // PAGE for L in seqlens))
+        bt = uniform_int(seed, TENSOR_POOL, batch * max_pages, 0, pool_pages - 1)
+        kv = normal_bf16(seed, TENSOR_KV, pool_pages * PAGE * D_QK).reshape(pool_pages, PAGE, 1,
+                                                                           D_QK)
+        q = normal_bf16(seed, TENSOR_Q, batch * h_q * D_QK).reshape(batch, 1, h_q, D_QK)
+        base = DecodeInputs(q=q, kv_cache=kv, block_table=bt.reshape(batch, max_pages),
+                            cache_seqlens=seqlens, s_q=1, h_q=h_q)
+    idx, cnt = draw_indices(seed, seqlens, topk, counts, repeats=repeats)
+    return SparseInputs(base=base, indices=idx, counts=cnt)
+
+
+@dataclasses.dataclass(frozen=True)
+class SparseWorkload:
+    """One named sparse decode workload (s_q = 1)."""
+    name: str
+    batch: int
+    h_q: int
+    seqlen: int
+    topk: int
+    pool_pages: int
+    seed: int = 0
+
+    def make(self) -> SparseInputs:
+        return make_sparse_inputs(self.seed, self.batch, self.h_q,
+                                  np.full(self.batch, self.seqlen, dtype=np.int32), self.topk,
+                                  pool_pages=self.pool_pages)
+
+    def keys(self) -> int:
+        return self.batch * min(self.topk, self.seqlen)
+
+    def flops(self) -> float:
+        """2 * (576 + 512) per (head, selected key)."""
+        return 2.0 * (D_QK + D_V) * self.h_q * self.keys()
+
+    def bytes(self) -> float:
+        """Each selected cache row once, plus q, out, lse and the indices."""
+        rows = self.batch * self.h_q
+        return float(self.keys() * (D_QK * 2 + 4) + rows * D_QK * 2 + rows * D_V * 2 + rows * 4)
+
+
+# Sparse decode at 128K context: 2048 selected positions per entry, 128
+# heads; the cache is a 604 MB pool of 8192 pages shared by the 64 entries'
+# block tables.
+SPARSE_WORKLOADS = {
+    "sparse_b64_h128_l131072_k2048": SparseWorkload("sparse_b64_h128_l131072_k2048", batch=64,
+                                                    h_q=128, seqlen=131072, topk=2048,
+                                                    pool_pages=8192, seed=5),
 }

@@ -8,8 +8,9 @@ marshals numpy arrays into it.
 Definition followed: scaled-dot-product attention of every query row over
 the latent cache rows it may see (bottom-right causal inside the ``s_q`` query
 tokens), values = the first 512 dims of the same row, lse = natural log of
-the softmax denominator of the scaled logits.  The header of ``mla_oracle.c``
-states it in full.
+the softmax denominator of the scaled logits.  Sparse decode (one query
+token per entry) is the same attention over the cache rows at a listed set of
+token positions.  The header of ``mla_oracle.c`` states both in full.
 """
 from __future__ import annotations
 
@@ -64,6 +65,9 @@ class Oracle:
         lib.oracle_mla_decode_rows.restype = I
         lib.oracle_mla_decode.argtypes = [P, P, I, P, I, P, I, I, I, ctypes.c_double, P, P, I]
         lib.oracle_mla_decode.restype = I
+        lib.oracle_mla_decode_sparse_rows.argtypes = [P, P, I, P, I, P, P, I, P, I, I,
+                                                      ctypes.c_double, I, P, I, I, P, P, I]
+        lib.oracle_mla_decode_sparse_rows.restype = I
         lib.oracle_lse_combine.argtypes = [I, P, P, P, P]
         lib.oracle_lse_combine.restype = None
         self.lib = lib
@@ -106,6 +110,37 @@ class Oracle:
             raise ValueError("oracle: index out of range")
         return out, lse
 
+    def mla_decode_sparse_rows(self, si, rows_bh, key_begin: int = 0, key_end: int = 2**31 - 1,
+                               nthreads: int | None = None, scale: float | None = None):
+        """Sparse decode of selected (b, h) rows: returns (out [n,512], lse [n]).
+        key_begin/key_end restrict the positions in each entry's index list."""
+        inp = si.base
+        rows_a, rp = _c(np.asarray(rows_bh, dtype=np.int32).reshape(-1, 2), np.int32)
+        n = rows_a.shape[0]
+        _q, qp = _c(inp.q, np.uint16)
+        _kv, kvp = _c(inp.kv_cache, np.uint16)
+        _bt, btp = _c(inp.block_table, np.int32)
+        _sl, slp = _c(inp.cache_seqlens, np.int32)
+        _ix, ixp = _c(si.indices, np.int32)
+        _ct, ctp = _c(si.counts, np.int32)
+        out = np.zeros((n, D_V), dtype=np.float64)
+        lse = np.zeros((n,), dtype=np.float64)
+        rc = self.lib.oracle_mla_decode_sparse_rows(
+            qp, kvp, inp.num_pages, btp, inp.max_pages, slp, ixp, si.indices.shape[1], ctp,
+            inp.batch, inp.h_q, float(inp.softmax_scale if scale is None else scale), n, rp,
+            int(key_begin), int(key_end), out.ctypes.data_as(ctypes.c_void_p),
+            lse.ctypes.data_as(ctypes.c_void_p), nthreads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle: index or count out of range")
+        return out, lse
+
+    def mla_decode_sparse(self, si, nthreads: int | None = None, scale: float | None = None):
+        """Sparse decode, every row: returns (out [B,1,h_q,512], lse [B,h_q,1])."""
+        B, h_q = si.base.batch, si.base.h_q
+        rows = np.array([(b, h) for b in range(B) for h in range(h_q)], dtype=np.int32)
+        out, lse = self.mla_decode_sparse_rows(si, rows, nthreads=nthreads, scale=scale)
+        return out.reshape(B, 1, h_q, D_V), lse.reshape(B, h_q, 1)
+
     def lse_combine(self, lse_parts, o_parts):
         """Merge results over disjoint key sets: returns (lse, out[512])."""
         _l, lp = _c(np.asarray(lse_parts, dtype=np.float64).reshape(-1), np.float64)
@@ -137,6 +172,15 @@ def mla_decode_rows(inp, rows, key_begin=0, key_end=2**31 - 1, nthreads=None, sc
 
 def lse_combine(lse_parts, o_parts):
     return default().lse_combine(lse_parts, o_parts)
+
+
+def mla_decode_sparse(si, nthreads=None, scale=None):
+    return default().mla_decode_sparse(si, nthreads, scale)
+
+
+def mla_decode_sparse_rows(si, rows_bh, key_begin=0, key_end=2**31 - 1, nthreads=None,
+                           scale=None):
+    return default().mla_decode_sparse_rows(si, rows_bh, key_begin, key_end, nthreads, scale)
 
 
 if __name__ == "__main__":  # pragma: no cover

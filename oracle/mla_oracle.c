@@ -27,6 +27,16 @@
  * oracle_lse_combine writes out the merge of attention results computed over
  * disjoint key sets: lse = log(sum_j exp(lse_j)), out = sum_j
  * exp(lse_j - lse) * out_j.
+ *
+ * oracle_mla_decode_sparse is the same attention over a selected subset of
+ * the cache.  The FlagTree talk write-up ("FlagTree: Triton-TLE 言語拡張、
+ * タイルIRバックエンド、およびコンパイラ最適化手法", section 性能テスト)
+ * names SparseMLA decode at 128K context but no mechanism; the reading taken
+ * is DeepSeek's sparse MLA decode: one query token per batch entry, whose
+ * keys are the cache rows at the token positions indices[b][j], j <
+ * counts[b] (a list, so a repeated position counts twice), every position
+ * in [0, L_b).  With indices[b][j] = j and counts[b] = L_b it is the dense
+ * definition above.
  */
 #include <math.h>
 #include <pthread.h>
@@ -58,12 +68,33 @@ typedef struct {
     int n_rows;
     const int32_t* rows; /* n_rows x (b, i, h) */
     int key_begin, key_end;
+    const int32_t* indices; /* sparse: [batch][topk] token positions, else NULL */
+    int topk;
+    const int32_t* counts;  /* sparse: keys of each entry */
     double* out;         /* n_rows x 512 */
     double* lse;         /* n_rows */
     int next;            /* shared work counter */
     pthread_mutex_t mu;
     int bad;             /* set when an index is out of range */
 } job_t;
+
+/* Cache row of key j of entry b: token j (dense) or indices[b][j] (sparse).
+ * NULL when an index is out of range. */
+static const uint16_t* key_row(const job_t* J, int b, int j)
+{
+    int t = j;
+    if (J->indices) {
+        t = J->indices[(size_t)b * J->topk + j];
+        if (t < 0 || t >= J->seqlens[b])
+            return NULL;
+    }
+    if (t / PAGE >= J->max_pages)
+        return NULL;
+    const int page = J->block_table[(size_t)b * J->max_pages + t / PAGE];
+    if (page < 0 || page >= J->num_pages)
+        return NULL;
+    return J->kv + ((size_t)page * PAGE + (t % PAGE)) * D_QK;
+}
 
 /* Attention of one query row over its visible keys restricted to
  * [key_begin, key_end). */
@@ -77,8 +108,16 @@ static void one_row(job_t* J, int r, double* s)
         J->bad = 1;
         return;
     }
-    const int L = J->seqlens[b];
-    const int n = L - J->s_q + 1 + i;
+    int n;
+    if (J->indices) {
+        n = J->counts[b];
+        if (n < 0 || n > J->topk) {
+            J->bad = 1;
+            return;
+        }
+    } else {
+        n = J->seqlens[b] - J->s_q + 1 + i;
+    }
     int t0 = J->key_begin > 0 ? J->key_begin : 0;
     int t1 = J->key_end < n ? J->key_end : n;
     if (t1 <= t0)
@@ -91,12 +130,11 @@ static void one_row(job_t* J, int r, double* s)
 
     double m = -INFINITY;
     for (int t = t0; t < t1; ++t) {
-        int page = J->block_table[(size_t)b * J->max_pages + t / PAGE];
-        if (page < 0 || page >= J->num_pages) {
+        const uint16_t* krow = key_row(J, b, t);
+        if (!krow) {
             J->bad = 1;
             return;
         }
-        const uint16_t* krow = J->kv + ((size_t)page * PAGE + (t % PAGE)) * D_QK;
         double dot = 0.0;
         for (int d = 0; d < D_QK; ++d)
             dot += qd[d] * bf16_to_double(krow[d]);
@@ -110,8 +148,7 @@ static void one_row(job_t* J, int r, double* s)
     const double lse = m + log(sum);
     for (int t = t0; t < t1; ++t) {
         const double w = exp(s[t - t0] - lse);
-        int page = J->block_table[(size_t)b * J->max_pages + t / PAGE];
-        const uint16_t* vrow = J->kv + ((size_t)page * PAGE + (t % PAGE)) * D_QK;
+        const uint16_t* vrow = key_row(J, b, t);
         for (int d = 0; d < D_V; ++d)
             o[d] += w * bf16_to_double(vrow[d]);
     }
@@ -121,8 +158,8 @@ static void one_row(job_t* J, int r, double* s)
 static void* worker(void* arg)
 {
     job_t* J = (job_t*)arg;
-    int max_n = 0;
-    for (int b = 0; b < J->batch; ++b)
+    int max_n = J->indices ? J->topk : 0;
+    for (int b = 0; b < J->batch && !J->indices; ++b)
         if (J->seqlens[b] > max_n)
             max_n = J->seqlens[b];
     double* s = (double*)malloc(sizeof(double) * (size_t)(max_n > 0 ? max_n : 1));
@@ -222,6 +259,64 @@ int oracle_mla_decode(const uint16_t* q, const uint16_t* kv, int num_pages,
     free(rows);
     free(l);
     return rc;
+}
+
+/* Sparse decode, one query token per entry (s_q = 1), selected rows: rows =
+ * n_rows pairs (b, h); key_begin/key_end restrict j (the list position).
+ * out [n_rows][512], lse [n_rows].  Returns 0, or -1 on an out-of-range
+ * index or count. */
+int oracle_mla_decode_sparse_rows(const uint16_t* q, const uint16_t* kv, int num_pages,
+                                  const int32_t* block_table, int max_pages,
+                                  const int32_t* cache_seqlens, const int32_t* indices, int topk,
+                                  const int32_t* counts, int batch, int h_q, double softmax_scale,
+                                  int n_rows, const int32_t* rows_bh, int key_begin, int key_end,
+                                  double* out, double* lse, int nthreads)
+{
+    int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * 3 * (size_t)(n_rows > 0 ? n_rows : 1));
+    if (!rows)
+        return -1;
+    for (int r = 0; r < n_rows; ++r) {
+        rows[3 * r] = rows_bh[2 * r];
+        rows[3 * r + 1] = 0;
+        rows[3 * r + 2] = rows_bh[2 * r + 1];
+    }
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q;
+    J.kv = kv;
+    J.num_pages = num_pages;
+    J.block_table = block_table;
+    J.max_pages = max_pages;
+    J.seqlens = cache_seqlens;
+    J.batch = batch;
+    J.s_q = 1;
+    J.h_q = h_q;
+    J.scale = softmax_scale;
+    J.n_rows = n_rows;
+    J.rows = rows;
+    J.key_begin = key_begin;
+    J.key_end = key_end;
+    J.indices = indices;
+    J.topk = topk;
+    J.counts = counts;
+    J.out = out;
+    J.lse = lse;
+    pthread_mutex_init(&J.mu, NULL);
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > 256)
+        nthreads = 256;
+    pthread_t th[256];
+    int started = 0;
+    for (int k = 1; k < nthreads; ++k)
+        if (pthread_create(&th[started], NULL, worker, &J) == 0)
+            ++started;
+    worker(&J);
+    for (int k = 0; k < started; ++k)
+        pthread_join(th[k], NULL);
+    pthread_mutex_destroy(&J.mu);
+    free(rows);
+    return J.bad ? -1 : 0;
 }
 
 /* Merge n results over disjoint key sets. lse_parts [n], o_parts [n][512]. */

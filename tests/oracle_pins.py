@@ -23,6 +23,13 @@ What pins what:
                    changes nothing, bit for bit
   two_token      - closed form with two keys, hand-chosen exact values
   empty          - no visible key: out = 0, lse = -inf
+  sparse_dense   - sparse decode: a dense numpy evaluation over the rows at
+                   the listed token positions (distinct, repeated, partial
+                   counts, and the identity list, which is the dense case)
+  sparse_twice   - every position listed twice: out unchanged, lse + ln 2
+  sparse_order   - the order of the list does not matter
+  sparse_edges   - count 0 gives out = 0, lse = -inf; a position past L_b
+                   is rejected
 """
 from __future__ import annotations
 
@@ -227,6 +234,102 @@ def check_empty(orc):
     assert np.all(np.isfinite(l[2])), "L=3 rows finite"
 
 
+def _sparse(orc, si, nthreads=2):
+    """The oracle on valid sparse inputs; refusing them is a failed pin."""
+    try:
+        return orc.mla_decode_sparse(si, nthreads=nthreads)
+    except ValueError as e:
+        raise AssertionError(f"oracle rejected valid sparse inputs: {e}") from e
+
+
+def sparse_reference(si):
+    """softmax(q K_sel^T * scale) V_sel per (b, h), K_sel the cache rows at
+    the listed positions, evaluated with numpy matmuls."""
+    inp = si.base
+    B, h_q = inp.batch, inp.h_q
+    out = np.zeros((B, 1, h_q, W.D_V))
+    lse = np.zeros((B, h_q, 1))
+    for b in range(B):
+        c = int(si.counts[b])
+        if c == 0:
+            lse[b] = -np.inf
+            continue
+        ts = [int(t) for t in si.indices[b, :c]]
+        K = f64(np.stack([inp.kv_cache[inp.block_table[b, t // W.PAGE], t % W.PAGE, 0] for t in ts]))
+        S = (f64(inp.q[b, 0]) @ K.T) * inp.softmax_scale
+        m = S.max(axis=1, keepdims=True)
+        P = np.exp(S - m)
+        l = P.sum(axis=1)
+        out[b, 0] = (P @ K[:, : W.D_V]) / l[:, None]
+        lse[b, :, 0] = m[:, 0] + np.log(l)
+    return out, lse
+
+
+def check_sparse_dense(orc):
+    cases = [
+        dict(seed=31, seqlens=[300, 64, 1], topk=128, counts=None, repeats=False),
+        dict(seed=32, seqlens=[500, 200], topk=70, counts=[70, 13], repeats=False),
+        dict(seed=33, seqlens=[90, 40], topk=64, counts=[64, 30], repeats=True),
+    ]
+    for c in cases:
+        si = W.make_sparse_inputs(c["seed"], len(c["seqlens"]), 3, c["seqlens"], c["topk"],
+                                  c["counts"], repeats=c["repeats"])
+        o, l = _sparse(orc, si)
+        ro, rl = sparse_reference(si)
+        _close(o, ro, 1e-12, f"sparse out {c}")
+        _close(l, rl, 1e-12, f"sparse lse {c}")
+    # the identity list over the whole sequence is the dense case
+    inp = W.make_inputs(34, 2, 1, 2, [130, 65], extra_pages=1)
+    idx = np.full((2, 130), -1, dtype=np.int32)
+    idx[0, :130] = np.arange(130)
+    idx[1, :65] = np.arange(65)
+    si = W.SparseInputs(base=inp, indices=idx, counts=np.array([130, 65], dtype=np.int32))
+    o, l = _sparse(orc, si)
+    ro, rl = dense_reference(inp)
+    _close(o, ro, 1e-12, "sparse identity out")
+    _close(l, rl, 1e-12, "sparse identity lse")
+
+
+def check_sparse_twice(orc):
+    si = W.make_sparse_inputs(35, 2, 2, [200, 77], 40)
+    o1, l1 = _sparse(orc, si)
+    idx2 = np.concatenate([si.indices[:, :40], si.indices[:, :40]], axis=1)
+    two = W.SparseInputs(base=si.base, indices=idx2, counts=(2 * si.counts).astype(np.int32))
+    o2, l2 = _sparse(orc, two)
+    _close(o2, o1, 1e-12, "listed twice out")
+    _close(l2 - l1, np.full_like(l1, math.log(2.0)), 1e-12, "listed twice lse")
+
+
+def check_sparse_order(orc):
+    si = W.make_sparse_inputs(36, 2, 3, [256, 100], 64)
+    o1, l1 = _sparse(orc, si)
+    idx = si.indices.copy()
+    for b in range(2):
+        c = int(si.counts[b])
+        idx[b, :c] = idx[b, :c][W.permutation(37 + b, 1, c)]
+    o2, l2 = _sparse(orc, W.SparseInputs(base=si.base, indices=idx, counts=si.counts))
+    assert not np.array_equal(idx, si.indices), "order check did not reorder"
+    _close(o2, o1, 1e-12, "reordered out")
+    _close(l2, l1, 1e-12, "reordered lse")
+
+
+def check_sparse_edges(orc):
+    si = W.make_sparse_inputs(38, 2, 2, [100, 50], 16, counts=[0, 16])
+    o, l = _sparse(orc, si, nthreads=1)
+    assert np.all(o[0] == 0.0) and np.all(np.isneginf(l[0])), "count 0 not empty"
+    assert np.all(np.isfinite(l[1])), "count 16 finite"
+    bad = si.indices.copy()
+    bad[1, 3] = 50                              # == L_1: past the sequence
+    try:
+        orc.mla_decode_sparse(W.SparseInputs(base=si.base, indices=bad, counts=si.counts),
+                              nthreads=1)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a position past L_b was accepted")
+
+
 ALL_CHECKS = [check_dense, check_seqlen_one, check_constant_v, check_shift, check_q_zero,
               check_split_combine, check_causal, check_permutation, check_two_token,
-              check_empty]
+              check_empty, check_sparse_dense, check_sparse_twice, check_sparse_order,
+              check_sparse_edges]

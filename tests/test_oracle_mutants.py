@@ -11,7 +11,7 @@ import oracle_pins
 
 MUTANTS = {
     "no_scale": ("s[t - t0] = J->scale * dot;", "s[t - t0] = dot;"),
-    "causal_off_by_one": ("const int n = L - J->s_q + 1 + i;", "const int n = L - J->s_q + i;"),
+    "causal_off_by_one": ("n = J->seqlens[b] - J->s_q + 1 + i;", "n = J->seqlens[b] - J->s_q + i;"),
     "lse_log2": ("const double lse = m + log(sum);", "const double lse = m + log2(sum);"),
     "value_offset": ("o[d] += w * bf16_to_double(vrow[d]);",
                      "o[d] += w * bf16_to_double(vrow[d + 64]);"),
@@ -20,8 +20,12 @@ MUTANTS = {
     "no_max_in_sum": ("sum += exp(s[t - t0] - m);", "sum += exp(s[t - t0]);"),
     "q_transposed": ("(((size_t)b * J->s_q + i) * J->h_q + h) * D_QK",
                      "(((size_t)b * J->h_q + h) * J->s_q + i) * D_QK"),
-    "slot_shift": ("((size_t)page * PAGE + (t % PAGE)) * D_QK;\n        double dot",
-                   "((size_t)page * PAGE + ((t + 1) % PAGE)) * D_QK;\n        double dot"),
+    "slot_shift": ("return J->kv + ((size_t)page * PAGE + (t % PAGE)) * D_QK;",
+                   "return J->kv + ((size_t)page * PAGE + ((t + 1) % PAGE)) * D_QK;"),
+    "sparse_ignores_list": ("t = J->indices[(size_t)b * J->topk + j];", "t = j;"),
+    "sparse_first_entry_list": ("t = J->indices[(size_t)b * J->topk + j];",
+                                "t = J->indices[j];"),
+    "sparse_count_short": ("n = J->counts[b];", "n = J->counts[b] > 0 ? J->counts[b] - 1 : 0;"),
     "combine_weight": ("const double w = exp(lse_parts[j] - *lse);",
                        "const double w = exp(lse_parts[j] - m);"),
     "dot_short": ("for (int d = 0; d < D_QK; ++d)\n            dot +=",
