@@ -130,6 +130,36 @@ int mla_decode_attend(const void* q, const void* kv_cache, int num_pages,
 int mla_decode_combine(int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/* Sparse decode: one query token per batch entry (s_q = 1) attending to a
+ * listed subset of its cache rows instead of all of them.  The FlagTree
+ * talk write-up ("FlagTree: Triton-TLE 言語拡張、タイルIRバックエンド、
+ * およびコンパイラ最適化手法", section 性能テスト) reports SparseMLA decode
+ * at 128K context without a mechanism; this is DeepSeek's form of it:
+ *
+ *   keys of entry b: the cache rows at token positions indices[b][j],
+ *   j < counts[b] (a list: a repeated position counts twice); each
+ *   position t in [0, cache_seqlens[b]) sits at
+ *   kv_cache[block_table[b][t/64]][t%64]
+ *   out, lse: as mla_decode over those keys (no causal mask)
+ *
+ *   indices  int32 [batch, topk]  device, positions past counts[b] ignored
+ *   counts   int32 [batch]        device, 0 <= counts[b] <= topk
+ *   q        bf16 [batch, 1, h_q, 576]; out bf16 [batch, 1, h_q, 512];
+ *   lse      fp32 [batch, h_q, 1]
+ *
+ * tile_meta comes from mla_decode_plan(counts, batch, 1, h_q, ...): the plan
+ * splits each entry's list into chunks of 64 positions the way it splits a
+ * sequence into pages.  The kernel gathers each chunk's rows with 16-byte
+ * asynchronous copies (the rows are scattered, so there is no page to load
+ * whole).  A position outside [0, cache_seqlens[b]), a block-table entry
+ * outside the pool or counts[b] > topk is flagged as MLA_ERR_DEVICE_BOUNDS
+ * and its row read as zeros.  Other rules as mla_decode. */
+int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
+                      const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                      const int32_t* indices, int topk, const int32_t* counts, int batch, int h_q,
+                      const void* tile_meta, void* out, float* lse, float softmax_scale,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* mla_decode for callers that cannot allocate device memory: the same
  * arguments minus the workspace.  The paper has no counterpart; this entry
  * point exists for host frameworks whose allocator owns all device memory

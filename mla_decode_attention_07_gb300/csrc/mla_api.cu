@@ -552,8 +552,12 @@ int prepare_decode(const void* q, const void* kv_cache, int num_pages, const int
   if (!workspace || (int64_t)workspace_bytes < need) return MLA_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MLA_ERR_INVALID_ARG;
   p->q = q;
+  p->kv = kv_cache;
   p->block_table = block_table;
   p->seqlens = cache_seqlens;
+  p->indices = nullptr;
+  p->cache_len = nullptr;
+  p->topk = 0;
   p->plan = static_cast<const int32_t*>(tile_meta);
   p->out = out;
   p->lse = lse;
@@ -641,6 +645,32 @@ int mla_decode(const void* q, const void* kv_cache, int num_pages, const int32_t
                                 batch, s_q, h_q, tile_meta, out, lse, softmax_scale, workspace,
                                 workspace_bytes, &p, &nc, &sms);
   if (rc != MLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int a = attend(q, kv_cache, p, nc, s);
+  if (a != MLA_OK) return a;
+  return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
+                      const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                      const int32_t* indices, int topk, const int32_t* counts, int batch, int h_q,
+                      const void* tile_meta, void* out, float* lse, float softmax_scale,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!indices || !counts || !cache_seqlens || topk < 1 || !aligned(indices, 4) ||
+      !aligned(counts, 4) || (int64_t)batch * topk >= ((int64_t)1 << 31))
+    return MLA_ERR_INVALID_ARG;
+  DecodeParams p;
+  int nc = 0, sms = 0;
+  // the counts take the place of the sequence lengths: the plan splits them
+  // into chunks of 64 listed positions, and the kernel masks past them
+  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, counts, batch,
+                                1, h_q, tile_meta, out, lse, softmax_scale, workspace,
+                                workspace_bytes, &p, &nc, &sms);
+  if (rc != MLA_OK) return rc;
+  if (!aligned(cache_seqlens, 4)) return MLA_ERR_INVALID_ARG;
+  p.indices = indices;
+  p.cache_len = cache_seqlens;
+  p.topk = topk;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int a = attend(q, kv_cache, p, nc, s);
   if (a != MLA_OK) return a;

@@ -287,6 +287,101 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
   return true;
 }
 
+// Sparse decode (one query token per entry): step g's "page" is the chunk
+// of listed positions [64 pg, 64 pg + 64) of entry b, whose cache rows are
+// scattered.  The whole producer warp gathers a chunk's rows (this CTA's 256
+// latent and 32 rotary dims of each, lanes taking rows lane and lane + 32)
+// with 16-byte cp.async copies, straight into the layout the tiled loads give
+// a stage: latent box k (dims 64 k ..) row r, 16-byte chunk c at
+// k * 8192 + r * 128 + ((c ^ (r % 8)) << 4) (128-byte swizzle); the rotary box
+// row r, chunk c at kStageRope + r * 64 + ((c ^ ((r / 2) % 4)) << 4) (64-byte
+// swizzle).  Rows past the entry's count are zero-filled.  Step g's copies
+// are waited for once step g + kGatherLag is issued (all of them at the end
+// of a tile, so that the next tile's Q wait cannot hold back the last score
+// MMAs), then fenced to the async proxy and announced on the stage's FULL
+// barrier.  kGatherLag < kStages: a stage the warp waits to refill was
+// announced before.
+constexpr uint32_t kGatherLag = 2;
+
+__device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
+                                                    const DecodeParams& prm,
+                                                    const CUtensorMap* tm_q_rope, int lane) {
+  SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
+  int b, pb, pe;
+  uint32_t g = 0, announced = 0, n_item = 0;
+  const char* kv = static_cast<const char*>(prm.kv);
+  const int32_t xq_rope = 512 + 32 * (int32_t)x.rank;
+  while (it.next(b, pb, pe)) {
+    if (!wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) {
+      ptx::cp_async_wait<0>();
+      return false;
+    }
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(x.bar(B_QFULL), kQRopeTx);
+      const int32_t row0 = b * w.rows + w.tile * kTileRows;
+      ptx::tma_load_2d(x.sbase + kQRope, tm_q_rope, xq_rope, row0, x.bar(B_QFULL));
+    }
+    const int count = prm.seqlens[b];
+    const int cap = prm.cache_len[b];
+    const int32_t* list = prm.indices + (size_t)b * prm.topk;
+    const int32_t* bt = prm.block_table + (size_t)b * prm.max_pages;
+    if (count > prm.topk && lane == 0) atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+    for (int pg = pb; pg < pe; ++pg, ++g) {
+      const uint32_t s = g % kStages, k = g / kStages;
+      if (!wait_warp(x, x.bar(B_EMPTY + s), (k & 1u) ^ 1u)) {
+        ptx::cp_async_wait<0>();
+        return false;
+      }
+      const uint32_t st = x.sbase + kStage0 + s * kStageBytes;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int r = lane + 32 * h;
+        const int j = pg * kPageTokens + r;
+        const char* src = kv;   // any valid address when nothing is read
+        uint32_t n = 0;
+        if (j < count && j < prm.topk) {
+          const int t = list[j];
+          int page = -1;
+          if (t >= 0 && t < cap && t / kPageTokens < prm.max_pages) page = bt[t / kPageTokens];
+          if ((unsigned)page < (unsigned)prm.num_pages) {
+            src = kv + ((size_t)page * kPageTokens + (size_t)(t % kPageTokens)) * (kDqk * 2);
+            n = 16;
+          } else {
+            atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+          }
+        }
+        const char* lat = src + 512 * x.rank;
+        const char* rope = src + 1024 + 64 * x.rank;
+        const uint32_t rsw = (uint32_t)(r & 7), rsw64 = (uint32_t)((r >> 1) & 3);
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          ptx::cp_async16(st + (uint32_t)(q >> 3) * 8192u + (uint32_t)r * 128u +
+                              ((((uint32_t)q & 7u) ^ rsw) << 4),
+                          lat + q * 16, n);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          ptx::cp_async16(st + kStageRope + (uint32_t)r * 64u + ((((uint32_t)c) ^ rsw64) << 4),
+                          rope + c * 16, n);
+      }
+      ptx::cp_async_commit();
+      if (g >= announced + kGatherLag) {
+        ptx::cp_async_wait<kGatherLag>();
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(x.bar(B_FULL + announced % kStages));
+        ++announced;
+      }
+    }
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    for (; announced < g; ++announced)
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_FULL + announced % kStages));
+    ++n_item;
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ MMA issuer
 // Issues S = Q K^T for page gq and O += P V for page gp (gp < gq), each as
 // soon as its inputs are ready, in page order within each kind.
@@ -961,7 +1056,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (!has_work) {
     // nothing to do: fall through to the teardown
   } else if (warp == kProducerWarp) {
-    if (lane == 0) run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
+    if (prm.indices != nullptr)
+      run_producer_sparse(x, w, prm, &tm_q_rope, lane);
+    else if (lane == 0)
+      run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     run_mma_qk(x, w);   // whole warp: one elected lane issues

@@ -14,8 +14,12 @@ constexpr int kDv = 512;   // value dims = the first 512 dims of the row
 // Everything the decode kernel needs besides its four tensor maps.
 struct DecodeParams {
   const void* q;      // bf16 [B, s_q, h_q, 576]
+  const void* kv;     // bf16 [num_pages, 64, 1, 576]
   const int32_t* block_table;
-  const int32_t* seqlens;
+  const int32_t* seqlens;      // keys per entry: cache lengths, or the sparse counts
+  const int32_t* indices;      // sparse: [B, topk] token positions; null for dense
+  const int32_t* cache_len;    // sparse: cache lengths (bounds of the positions)
+  int topk;
   const int32_t* plan;
   void* out;          // bf16 [B, s_q, h_q, 512]
   float* lse;         // fp32 [B, h_q, s_q]

@@ -29,7 +29,7 @@ MLA_ERR_PLAN = -7
 
 EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_workspace_size", "mla_decode_plan", "mla_decode_plan_host", "mla_decode",
-            "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc",
+            "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc", "mla_decode_sparse",
             "mla_check_device_error", "mla_strerror"]
 
 _lib = None
@@ -70,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_decode_combine.restype = I
     lib.mla_decode_noalloc.argtypes = [V, V, I, V, I, V, I, I, I, V, V, V, F, V]
     lib.mla_decode_noalloc.restype = I
+    lib.mla_decode_sparse.argtypes = [V, V, I, V, I, V, V, I, V, I, I, V, V, V, F, V, Z, V]
+    lib.mla_decode_sparse.restype = I
     lib.mla_check_device_error.argtypes = [V]
     lib.mla_check_device_error.restype = I
     lib.mla_strerror.argtypes = [I]
@@ -162,6 +164,24 @@ def mla_decode(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
                            _ptr(workspace), int(workspace.numel() * workspace.element_size()),
                            _stream(stream))
     _check(rc, "mla_decode")
+
+
+def mla_decode_sparse(q, kv_cache, block_table, cache_seqlens, indices, counts, tile_meta, out,
+                      lse, softmax_scale: float, workspace, stream=None) -> None:
+    """Sparse decode: q [B, 1, h_q, 576]; indices [B, topk] int32 token
+    positions; counts [B] int32; tile_meta from mla_decode_plan(counts, 1,
+    h_q, ...); out [B, 1, h_q, 512] bf16; lse [B, h_q, 1] fp32."""
+    B, h_q = int(q.shape[0]), int(q.shape[2])
+    if int(q.shape[1]) != 1:
+        raise MlaError(MLA_ERR_INVALID_ARG, "mla_decode_sparse (s_q must be 1)")
+    rc = load().mla_decode_sparse(_ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]),
+                                  _ptr(block_table), int(block_table.shape[1]),
+                                  _ptr(cache_seqlens), _ptr(indices), int(indices.shape[1]),
+                                  _ptr(counts), B, h_q, _ptr(tile_meta), _ptr(out), _ptr(lse),
+                                  float(softmax_scale), _ptr(workspace),
+                                  int(workspace.numel() * workspace.element_size()),
+                                  _stream(stream))
+    _check(rc, "mla_decode_sparse")
 
 
 def mla_decode_attend(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
