@@ -16,6 +16,10 @@ recorded between the three launches of each timed step.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (the
 only other arm there is: the pages ship no implementation).
+
+--workload sparse_b64_h128_l131072_k2048 measures sparse decode instead
+(mla_decode_plan over the counts + mla_decode_sparse: 2048 listed positions
+per entry of a 128K-token context), with rotating query/position sets.
 """
 from __future__ import annotations
 
@@ -49,7 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(W.WORKLOADS) + sorted(W.SPARSE_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the oracle baseline leg")
@@ -552,9 +557,174 @@ def run_reference(args):
     }), flush=True)
 
 
+SPARSE_METRIC = "MLA sparse decode TFLOP/s, gathered KV GB/s and % of GB300 roofline per call"
+
+
+def sparse_sets(w, si, n):
+    """Rotating (q, positions) sets over one cache pool: set 0 is the
+    workload's own, the others redraw q and the positions."""
+    seqlens = si.base.cache_seqlens
+    out = [(si.base.q, si.indices, si.counts)]
+    for k in range(1, n):
+        sd = w.seed + 7919 * k
+        q = W.normal_bf16(sd, W.TENSOR_Q, w.batch * w.h_q * W.D_QK).reshape(w.batch, 1, w.h_q,
+                                                                           W.D_QK)
+        idx, cnt = W.draw_indices(sd, seqlens, w.topk)
+        out.append((q, idx, cnt))
+    return out
+
+
+def sparse_cpu_baseline(si, budget_s):
+    """The oracle over a seeded row sample of the sparse workload."""
+    import oracle
+    threads = oracle.default_threads()
+    B, h_q = si.base.batch, si.base.h_q
+    rows_all = np.array([(b, h) for b in range(B) for h in range(h_q)], dtype=np.int32)
+    per_row = 2.0 * (W.D_QK + W.D_V)
+    fl = lambda rows: sum(per_row * int(si.counts[b]) for b, _h in rows)
+    cal = rows_all[:16]
+    t0 = time.perf_counter()
+    oracle.mla_decode_sparse_rows(si, cal, nthreads=threads)
+    rate = fl(cal) / max(1e-6, time.perf_counter() - t0)
+    n = int(min(len(rows_all), max(16, budget_s * rate / per_row / max(1, si.topk) / 1.2)))
+    rng = np.random.default_rng(0)
+    sample = rows_all[np.sort(rng.choice(len(rows_all), size=n, replace=False))]
+    passes, spent = 0, 0.0
+    while spent < 0.5 * budget_s and passes < 50:
+        t0 = time.perf_counter()
+        oracle.mla_decode_sparse_rows(si, sample, nthreads=threads)
+        spent += time.perf_counter() - t0
+        passes += 1
+    return {"value": fl(sample) * passes / spent / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} of {len(rows_all)} query rows, seeded random, {passes} pass(es), "
+                      f"{spent:.1f} s, fp64 C oracle"}
+
+
+def run_sparse(args):
+    """Sparse decode on one GPU (or N replicas): plan over the counts plus
+    mla_decode_sparse per step, inputs resident, rotating position sets."""
+    import torch
+    from mla_decode_attention_07_gb300 import libmla
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    libmla.load()
+    w = W.SPARSE_WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    si = w.make()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    kv = t(si.base.kv_cache.view(np.int16)).view(torch.bfloat16)
+    bt, sl = t(si.base.block_table), t(si.base.cache_seqlens)
+    sets = [dict(q=t(q.view(np.int16)).view(torch.bfloat16), idx=t(idx), cnt=t(cnt))
+            for q, idx, cnt in sparse_sets(w, si, 4)]
+    B, h_q = w.batch, w.h_q
+    out = torch.empty((B, 1, h_q, W.D_V), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, h_q, 1), dtype=torch.float32, device=dev)
+    meta, ws = libmla.alloc_plan_and_workspace(B, 1, h_q, dev.index)
+    stream = torch.cuda.current_stream(dev)
+    scale = W.SOFTMAX_SCALE
+
+    def step(k, ev=None):
+        st = sets[k % len(sets)]
+        if ev:
+            ev[0].record(stream)
+        libmla.mla_decode_plan(st["cnt"], 1, h_q, meta, stream)
+        if ev:
+            ev[1].record(stream)
+        libmla.mla_decode_sparse(st["q"], kv, bt, sl, st["idx"], st["cnt"], meta, out, lse,
+                                 scale, ws, stream)
+        if ev:
+            ev[2].record(stream)
+
+    for k in range(max(3, args.warmup)):
+        step(k)
+    torch.cuda.synchronize()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error during warm-up: {libmla.mla_strerror(rc)}")
+    sampler = ClockSampler(physical_gpu_index(dev.index))
+    sampler.start()
+    t_end = time.perf_counter() + 1.5
+    k = 0
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            step(k)
+            k += 1
+        torch.cuda.synchronize()
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for i in range(K):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_step = aggregate_max(e0.elapsed_time(e1), world) / K
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        step(i, evs[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error in timed region: {libmla.mla_strerror(rc)}")
+    plan_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    call_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) * 1e3
+    gbytes = w.bytes()
+    achieved = gbytes / (call_us * 1e-6) / 1e9
+    result = {
+        "metric": SPARSE_METRIC,
+        "value": round(w.flops() * world / (ms_step * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64 normals rounded to bf16; uniform random "
+                "distinct positions; shared 8192-page pool)",
+        "config": {"workload": w.name, "batch": B, "s_q": 1, "h_q": h_q, "seqlen": w.seqlen,
+                   "topk": w.topk, "pool_pages": w.pool_pages,
+                   "l2": "4 rotating query/position sets; each step gathers "
+                         f"{w.keys() * W.D_QK * 2 / 1e6:.0f} MB of scattered rows from a "
+                         f"{w.pool_pages * 64 * W.D_QK * 2 / 1e6:.0f} MB pool",
+                   "parallelism": "single GPU" if world == 1 else f"{world} replicas"},
+        "us_per_call": round(ms_step * 1e3, 3),
+        "kv_gbs": round(w.keys() * W.D_QK * 2 / (ms_step * 1e-3) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "mla_decode_sparse call (decode kernel + combine)",
+                     "peak_source": peak_src},
+        "kernels_us": {"plan": round(plan_us, 3), "decode_call": round(call_us, 3)},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = sparse_cpu_baseline(si, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.workload in W.SPARSE_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm is timed on the dense workloads; the sparse "
+                              "line carries its own cpu_baseline"}), flush=True)
+        else:
+            run_sparse(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

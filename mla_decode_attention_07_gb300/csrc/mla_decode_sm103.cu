@@ -64,6 +64,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -290,18 +291,25 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
 // Sparse decode (one query token per entry): step g's "page" is the chunk
 // of listed positions [64 pg, 64 pg + 64) of entry b, whose cache rows are
 // scattered.  The whole producer warp gathers a chunk's rows (this CTA's 256
-// latent and 32 rotary dims of each, lanes taking rows lane and lane + 32)
-// with 16-byte cp.async copies, straight into the layout the tiled loads give
-// a stage: latent box k (dims 64 k ..) row r, 16-byte chunk c at
-// k * 8192 + r * 128 + ((c ^ (r % 8)) << 4) (128-byte swizzle); the rotary box
-// row r, chunk c at kStageRope + r * 64 + ((c ^ ((r / 2) % 4)) << 4) (64-byte
-// swizzle).  Rows past the entry's count are zero-filled.  Step g's copies
-// are waited for once step g + kGatherLag is issued (all of them at the end
-// of a tile, so that the next tile's Q wait cannot hold back the last score
-// MMAs), then fenced to the async proxy and announced on the stage's FULL
-// barrier.  kGatherLag < kStages: a stage the warp waits to refill was
-// announced before.
+// latent and 32 rotary dims of each) with 16-byte cp.async copies, straight
+// into the layout the tiled loads give a stage: latent box k (dims 64 k ..)
+// row r, 16-byte chunk c at k * 8192 + r * 128 + ((c ^ (r % 8)) << 4)
+// (128-byte swizzle); the rotary box row r, chunk c at kStageRope + r * 64 +
+// ((c ^ ((r / 2) % 4)) << 4) (64-byte swizzle).  One instruction copies one
+// row's 512 latent bytes (lane = chunk), so each is four whole 128-byte
+// lines; eight more copy the rotary parts of eight rows each.  Rows past the
+// entry's count are zero-filled.
+//
+// The row each lane resolves (rows lane and lane + 32: list position, then
+// block-table entry) is ready one chunk ahead, and the list positions two
+// chunks ahead, so no dependent global load sits between two chunks' copies.
+// Step g's copies are waited for once step g + kGatherLag is issued (all of
+// them at the end of a tile, so that the next tile's Q wait cannot hold back
+// the last score MMAs), then fenced to the async proxy and announced on the
+// stage's FULL barrier.  kGatherLag < kStages: a stage the warp waits to
+// refill was announced before.
 constexpr uint32_t kGatherLag = 2;
+constexpr int kNotListed = INT_MIN;   // slot past the entry's count
 
 __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
                                                     const DecodeParams& prm,
@@ -311,6 +319,8 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
   uint32_t g = 0, announced = 0, n_item = 0;
   const char* kv = static_cast<const char*>(prm.kv);
   const int32_t xq_rope = 512 + 32 * (int32_t)x.rank;
+  const uint32_t lat_off = 512u * x.rank + 16u * (uint32_t)lane;
+  const uint32_t rope_off = 1024u + 64u * x.rank + 16u * (uint32_t)(lane & 3);
   while (it.next(b, pb, pe)) {
     if (!wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) {
       ptx::cp_async_wait<0>();
@@ -323,45 +333,68 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
     }
     const int count = prm.seqlens[b];
     const int cap = prm.cache_len[b];
+    const int lim = count < prm.topk ? count : prm.topk;
     const int32_t* list = prm.indices + (size_t)b * prm.topk;
     const int32_t* bt = prm.block_table + (size_t)b * prm.max_pages;
     if (count > prm.topk && lane == 0) atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+    // list position of row r of chunk pg (kNotListed past the count)
+    auto position = [&](int pg, int r) -> int {
+      const int j = pg * kPageTokens + r;
+      return (pg < pe && j < lim) ? list[j] : kNotListed;
+    };
+    // block-table entry of a position (the load is only issued here; the
+    // value is looked at by `resolve`, a chunk later)
+    auto page_of = [&](int t) -> int {
+      return (t != kNotListed && t >= 0 && t < cap && t / kPageTokens < prm.max_pages)
+                 ? bt[t / kPageTokens]
+                 : -1;
+    };
+    // cache row (page * 64 + slot) of a position; -1 reads zeros
+    auto resolve = [&](int t, int page) -> int {
+      if (t == kNotListed) return -1;
+      if ((unsigned)page >= (unsigned)prm.num_pages) {
+        atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+        return -1;
+      }
+      return page * kPageTokens + t % kPageTokens;
+    };
+    int t_cur0 = position(pb, lane), t_cur1 = position(pb, lane + 32);
+    int p_cur0 = page_of(t_cur0), p_cur1 = page_of(t_cur1);
+    int t_next0 = position(pb + 1, lane), t_next1 = position(pb + 1, lane + 32);
     for (int pg = pb; pg < pe; ++pg, ++g) {
+      const int row0 = resolve(t_cur0, p_cur0), row1 = resolve(t_cur1, p_cur1);
+      // one chunk ahead: the block-table entries of pg + 1; two ahead: the
+      // positions of pg + 2
+      t_cur0 = t_next0;
+      t_cur1 = t_next1;
+      p_cur0 = page_of(t_cur0);
+      p_cur1 = page_of(t_cur1);
+      t_next0 = position(pg + 2, lane);
+      t_next1 = position(pg + 2, lane + 32);
       const uint32_t s = g % kStages, k = g / kStages;
       if (!wait_warp(x, x.bar(B_EMPTY + s), (k & 1u) ^ 1u)) {
         ptx::cp_async_wait<0>();
         return false;
       }
       const uint32_t st = x.sbase + kStage0 + s * kStageBytes;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int r = lane + 32 * h;
-        const int j = pg * kPageTokens + r;
-        const char* src = kv;   // any valid address when nothing is read
-        uint32_t n = 0;
-        if (j < count && j < prm.topk) {
-          const int t = list[j];
-          int page = -1;
-          if (t >= 0 && t < cap && t / kPageTokens < prm.max_pages) page = bt[t / kPageTokens];
-          if ((unsigned)page < (unsigned)prm.num_pages) {
-            src = kv + ((size_t)page * kPageTokens + (size_t)(t % kPageTokens)) * (kDqk * 2);
-            n = 16;
-          } else {
-            atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
-          }
-        }
-        const char* lat = src + 512 * x.rank;
-        const char* rope = src + 1024 + 64 * x.rank;
-        const uint32_t rsw = (uint32_t)(r & 7), rsw64 = (uint32_t)((r >> 1) & 3);
+      const uint32_t box = st + (uint32_t)(lane >> 3) * 8192u;
+#pragma unroll 4
+      for (int r = 0; r < kPageTokens; ++r) {
+        const int rr = __shfl_sync(0xffffffffu, r < 32 ? row0 : row1, r & 31);
+        const char* src = rr >= 0 ? kv + (size_t)rr * (kDqk * 2) + lat_off : kv;
+        ptx::cp_async16(box + (uint32_t)r * 128u + ((((uint32_t)lane & 7u) ^ ((uint32_t)r & 7u)) << 4),
+                        src, rr >= 0 ? 16u : 0u);
+      }
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          ptx::cp_async16(st + (uint32_t)(q >> 3) * 8192u + (uint32_t)r * 128u +
-                              ((((uint32_t)q & 7u) ^ rsw) << 4),
-                          lat + q * 16, n);
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          ptx::cp_async16(st + kStageRope + (uint32_t)r * 64u + ((((uint32_t)c) ^ rsw64) << 4),
-                          rope + c * 16, n);
+      for (int i = 0; i < 8; ++i) {
+        const int r = 8 * i + (lane >> 2);
+        const int rr0 = __shfl_sync(0xffffffffu, row0, r & 31);
+        const int rr1 = __shfl_sync(0xffffffffu, row1, r & 31);
+        const int rr = r < 32 ? rr0 : rr1;
+        const char* src = rr >= 0 ? kv + (size_t)rr * (kDqk * 2) + rope_off : kv;
+        ptx::cp_async16(st + kStageRope + (uint32_t)r * 64u +
+                            ((((uint32_t)lane & 3u) ^ (((uint32_t)r >> 1) & 3u)) << 4),
+                        src, rr >= 0 ? 16u : 0u);
       }
       ptx::cp_async_commit();
       if (g >= announced + kGatherLag) {
