@@ -44,6 +44,7 @@ METRIC = "MLA decode TFLOP/s, KV GB/s and % of GB300 roofline per call (1 GPU)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DEFAULT_WORKLOAD = "b16_h128_l4096"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_traffic.json")
+SPARSE_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sparse_traffic.json")
 DECODE_SRC = os.path.join(ROOT, "mla_decode_attention_07_gb300", "csrc", "mla_decode_sm103.cu")
 
 
@@ -107,13 +108,13 @@ def kernel_code_sha(path: str) -> str:
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
-def traffic_per_launch(workload: str):
+def traffic_per_launch(workload: str, path: str = TRAFFIC_FILE):
     """DRAM bytes per attend launch from the committed ncu summary, if it was
     taken on this workload and the kernel code is unchanged since."""
-    if not os.path.exists(TRAFFIC_FILE):
+    if not os.path.exists(path):
         return None
     try:
-        with open(TRAFFIC_FILE) as f:
+        with open(path) as f:
             rec = json.load(f)
         if rec.get("workload") != workload or rec.get("code_sha256") != kernel_code_sha(DECODE_SRC):
             return None
@@ -700,8 +701,10 @@ def run_sparse(args):
         "kv_gbs": round(w.keys() * W.D_QK * 2 / (ms_step * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "mla_decode_sparse call (decode kernel + combine)",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic_per_launch(w.name, SPARSE_TRAFFIC_FILE),
+                     "kernel": "mla_decode_sparse call (decode kernel + combine); traffic: "
+                               "the decode kernel's DRAM bytes per launch",
                      "peak_source": peak_src},
         "kernels_us": {"plan": round(plan_us, 3), "decode_call": round(call_us, 3)},
         "gpu_launches": 3 * K,
