@@ -58,6 +58,26 @@ def test_decode_rejects_bad_args_on_host(lib, kw):
     assert _decode(lib, **kw) == libmla.MLA_ERR_INVALID_ARG
 
 
+def _sparse(lib, **kw):
+    a = dict(q=0x1000, kv=0x2000, num_pages=4, bt=0x3000, max_pages=4, sl=0x4000, idx=0x9000,
+             topk=64, cnt=0xA000, batch=1, h_q=16, meta=0x5000, out=0x6000, lse=0x7000,
+             scale=0.07, ws=0x8000, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.mla_decode_sparse(a["q"], a["kv"], a["num_pages"], a["bt"], a["max_pages"],
+                                 a["sl"], a["idx"], a["topk"], a["cnt"], a["batch"], a["h_q"],
+                                 a["meta"], a["out"], a["lse"], ctypes.c_float(a["scale"]),
+                                 a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(idx=None), dict(cnt=None), dict(sl=None), dict(topk=0), dict(idx=0x9002),
+    dict(cnt=0xA001), dict(batch=1 << 16, topk=1 << 16), dict(q=None), dict(h_q=0),
+    dict(out=0x6002), dict(scale=float("inf")),
+])
+def test_sparse_rejects_bad_args_on_host(lib, kw):
+    assert _sparse(lib, **kw) == libmla.MLA_ERR_INVALID_ARG
+
+
 def test_plan_rejects_bad_args_on_host(lib):
     assert lib.mla_decode_plan(None, 1, 1, 16, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_plan(0x4000, 1, 1, 0, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
@@ -78,5 +98,6 @@ def test_no_gpu_means_error_not_fallback(lib):
         pytest.skip("a GPU is present")
     # Valid-looking arguments: the only thing missing is the device.
     assert _decode(lib) in (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
+    assert _sparse(lib) in (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
     assert lib.mla_num_clusters(0) < 0
     assert lib.mla_plan_size(1, 1, 16, 0) == 0

@@ -67,3 +67,35 @@ def test_workload_accounting():
     assert s.visible_keys() == 132 * (8192 + 8191)
     r = W.WORKLOADS["ragged_b64_h128"].seqlens()
     assert r.min() >= 1 and r.max() <= 8192 and len(r) == 64
+
+
+def test_sparse_positions_are_a_seeded_subset():
+    idx, cnt = W.draw_indices(9, [300, 64, 5, 0], 128)
+    assert list(cnt) == [128, 64, 5, 0]
+    for b, (L, c) in enumerate([(300, 128), (64, 64), (5, 5), (0, 0)]):
+        sel = idx[b, :c]
+        assert len(set(sel.tolist())) == c                  # distinct
+        assert ((sel >= 0) & (sel < max(L, 1))).all()
+        assert (idx[b, c:] == -1).all()
+    assert sorted(idx[1, :64].tolist()) == list(range(64))  # count == L: a permutation
+    again, _ = W.draw_indices(9, [300, 64, 5, 0], 128)
+    assert np.array_equal(idx, again)                       # seeded
+    other, _ = W.draw_indices(10, [300, 64, 5, 0], 128)
+    assert not np.array_equal(idx, other)
+
+
+def test_sparse_repeats_and_bad_counts():
+    idx, cnt = W.draw_indices(3, [10], 40, counts=[40], repeats=True)
+    assert cnt[0] == 40 and ((idx[0] >= 0) & (idx[0] < 10)).all()
+    with pytest.raises(ValueError):
+        W.draw_indices(3, [10], 40, counts=[20])            # 20 distinct of 10
+    with pytest.raises(ValueError):
+        W.draw_indices(3, [100], 8, counts=[9])             # more than top-k
+
+
+def test_sparse_pool_block_tables_stay_in_the_pool():
+    si = W.make_sparse_inputs(4, 3, 16, [1000, 65, 64], 32, pool_pages=7)
+    assert si.base.kv_cache.shape == (7, W.PAGE, 1, W.D_QK)
+    assert si.base.block_table.shape == (3, 16)
+    assert ((si.base.block_table >= 0) & (si.base.block_table < 7)).all()
+    assert si.base.q.shape == (3, 1, 16, W.D_QK)
