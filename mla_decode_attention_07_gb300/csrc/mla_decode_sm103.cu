@@ -76,12 +76,18 @@ namespace mla {
 namespace {
 
 // Warp roles (see above).  Warp w reaches TMEM lanes [32 (w % 4), +32).
-constexpr int kThreads = 384;
+constexpr int kThreads = 480;         // launched for sparse decode
+constexpr int kDenseThreads = 384;    // dense decode: warps 0-11 only
 constexpr int kQuadWarps = 4;   // page workers per set (one per TMEM lane quadrant)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kPSendWarp = 10;   // the P notifier thread
 constexpr int kPvWarp = 11;
+constexpr int kGatherWarp = 12;   // sparse decode: warps 12-14 gather with warp 8 (idle when dense)
+constexpr int kGatherWarps = 4;   // sparse decode: each gathers 64 / kGatherWarps rows of a chunk
+constexpr int kGatherRows = 64 / kGatherWarps;
+static_assert(kThreads == 32 * (kGatherWarp + kGatherWarps - 1), "gather warps end the block");
+static_assert(kGatherRows % 8 == 0 && kGatherRows <= 32, "rotary copies take 8 rows at a time");
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainNs = 2000000ull;            // 2 ms settle time after an abort
 constexpr float kRescaleThreshold = 8.0f;           // log2 units
@@ -313,7 +319,8 @@ constexpr int kNotListed = INT_MIN;   // slot past the entry's count
 
 __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
                                                     const DecodeParams& prm,
-                                                    const CUtensorMap* tm_q_rope, int lane) {
+                                                    const CUtensorMap* tm_q_rope, int lane,
+                                                    int half) {
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, announced = 0, n_item = 0;
@@ -322,11 +329,11 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
   const uint32_t lat_off = 512u * x.rank + 16u * (uint32_t)lane;
   const uint32_t rope_off = 1024u + 64u * x.rank + 16u * (uint32_t)(lane & 3);
   while (it.next(b, pb, pe)) {
-    if (!wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) {
+    if (half == 0 && !wait_warp(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) {
       ptx::cp_async_wait<0>();
       return false;
     }
-    if (lane == 0) {
+    if (half == 0 && lane == 0) {
       ptx::mbar_arrive_expect_tx(x.bar(B_QFULL), kQRopeTx);
       const int32_t row0 = b * w.rows + w.tile * kTileRows;
       ptx::tma_load_2d(x.sbase + kQRope, tm_q_rope, xq_rope, row0, x.bar(B_QFULL));
@@ -336,7 +343,9 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
     const int lim = count < prm.topk ? count : prm.topk;
     const int32_t* list = prm.indices + (size_t)b * prm.topk;
     const int32_t* bt = prm.block_table + (size_t)b * prm.max_pages;
-    if (count > prm.topk && lane == 0) atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+    if (count > prm.topk && lane == 0 && half == 0) atomicCAS(x.err, 0, MLA_ERR_DEVICE_BOUNDS);
+    // this lane's row of every chunk (lanes past kGatherRows repeat the first ones)
+    const int myr = kGatherRows * half + (lane & (kGatherRows - 1));
     // list position of row r of chunk pg (kNotListed past the count)
     auto position = [&](int pg, int r) -> int {
       const int j = pg * kPageTokens + r;
@@ -358,19 +367,16 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
       }
       return page * kPageTokens + t % kPageTokens;
     };
-    int t_cur0 = position(pb, lane), t_cur1 = position(pb, lane + 32);
-    int p_cur0 = page_of(t_cur0), p_cur1 = page_of(t_cur1);
-    int t_next0 = position(pb + 1, lane), t_next1 = position(pb + 1, lane + 32);
+    int t_cur = position(pb, myr);
+    int p_cur = page_of(t_cur);
+    int t_next = position(pb + 1, myr);
     for (int pg = pb; pg < pe; ++pg, ++g) {
-      const int row0 = resolve(t_cur0, p_cur0), row1 = resolve(t_cur1, p_cur1);
+      const int row = resolve(t_cur, p_cur);
       // one chunk ahead: the block-table entries of pg + 1; two ahead: the
       // positions of pg + 2
-      t_cur0 = t_next0;
-      t_cur1 = t_next1;
-      p_cur0 = page_of(t_cur0);
-      p_cur1 = page_of(t_cur1);
-      t_next0 = position(pg + 2, lane);
-      t_next1 = position(pg + 2, lane + 32);
+      t_cur = t_next;
+      p_cur = page_of(t_cur);
+      t_next = position(pg + 2, myr);
       const uint32_t s = g % kStages, k = g / kStages;
       if (!wait_warp(x, x.bar(B_EMPTY + s), (k & 1u) ^ 1u)) {
         ptx::cp_async_wait<0>();
@@ -379,18 +385,16 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
       const uint32_t st = x.sbase + kStage0 + s * kStageBytes;
       const uint32_t box = st + (uint32_t)(lane >> 3) * 8192u;
 #pragma unroll 4
-      for (int r = 0; r < kPageTokens; ++r) {
-        const int rr = __shfl_sync(0xffffffffu, r < 32 ? row0 : row1, r & 31);
+      for (int r = kGatherRows * half; r < kGatherRows * (half + 1); ++r) {
+        const int rr = __shfl_sync(0xffffffffu, row, r & (kGatherRows - 1));
         const char* src = rr >= 0 ? kv + (size_t)rr * (kDqk * 2) + lat_off : kv;
         ptx::cp_async16(box + (uint32_t)r * 128u + ((((uint32_t)lane & 7u) ^ ((uint32_t)r & 7u)) << 4),
                         src, rr >= 0 ? 16u : 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = 8 * i + (lane >> 2);
-        const int rr0 = __shfl_sync(0xffffffffu, row0, r & 31);
-        const int rr1 = __shfl_sync(0xffffffffu, row1, r & 31);
-        const int rr = r < 32 ? rr0 : rr1;
+      for (int i = 0; i < kGatherRows / 8; ++i) {
+        const int r = kGatherRows * half + 8 * i + (lane >> 2);
+        const int rr = __shfl_sync(0xffffffffu, row, r & (kGatherRows - 1));
         const char* src = rr >= 0 ? kv + (size_t)rr * (kDqk * 2) + rope_off : kv;
         ptx::cp_async16(st + kStageRope + (uint32_t)r * 64u +
                             ((((uint32_t)lane & 3u) ^ (((uint32_t)r >> 1) & 3u)) << 4),
@@ -990,7 +994,10 @@ __device__ __forceinline__ bool run_pnotify(const Ctx& x, const Work& w) {
   return true;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// Two instantiations: dense (kDenseThreads, the register budget of 384
+// threads) and sparse (kThreads, with the extra gather warps).
+template <bool kSparse>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreads : kDenseThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_q_rope,
                       const __grid_constant__ CUtensorMap tm_kv_lat,
                       const __grid_constant__ CUtensorMap tm_kv_rope, const DecodeParams prm) {
@@ -1012,7 +1019,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // dependent launch it overlaps the planner's tail.
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(x.bar(B_FULL + s), 1);
+      ptx::mbar_init(x.bar(B_FULL + s), kSparse ? kGatherWarps : 1);   // gather warps, or the TMA
       ptx::mbar_init(x.bar(B_EMPTY + s), 1);
     }
     ptx::mbar_init(x.bar(B_QFULL), 1 + 4);   // rotary TMA + set 1's 4 warps
@@ -1088,10 +1095,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (!has_work) {
     // nothing to do: fall through to the teardown
-  } else if (warp == kProducerWarp) {
-    if (prm.indices != nullptr)
-      run_producer_sparse(x, w, prm, &tm_q_rope, lane);
-    else if (lane == 0)
+  } else if (warp == kProducerWarp || warp >= kGatherWarp) {
+    if constexpr (kSparse)
+      run_producer_sparse(x, w, prm, &tm_q_rope, lane,
+                          warp == kProducerWarp ? 0 : warp - kGatherWarp + 1);
+    else if (warp == kProducerWarp && lane == 0)
       run_producer(x, w, prm, &tm_q_rope, &tm_kv_lat, &tm_kv_rope);
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -1141,7 +1149,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 int decode_smem_bytes() { return (int)kSmemAlloc; }
 
 cudaError_t decode_kernel_setup(int /*device*/) {
-  return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(
+      mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)kSmemAlloc);
 }
 
@@ -1156,7 +1167,8 @@ int decode_max_clusters(int device) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)kSmemAlloc;
     int m = 0;
-    if (cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel, &cfg) == cudaSuccess) n = m;
+    // the sparse instantiation (more threads) bounds both
+    if (cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel<true>, &cfg) == cudaSuccess) n = m;
   }
   if (prev != device) cudaSetDevice(prev);
   return n;
@@ -1166,7 +1178,7 @@ cudaError_t launch_decode(const TensorMaps& m, const DecodeParams& p, int num_cl
                           cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_clusters);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(p.indices != nullptr ? kThreads : kDenseThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1174,7 +1186,9 @@ cudaError_t launch_decode(const TensorMaps& m, const DecodeParams& p, int num_cl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_decode_kernel, m.q_rope, m.kv_lat, m.kv_rope, p);
+  if (p.indices != nullptr)
+    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, m.q_rope, m.kv_lat, m.kv_rope, p);
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, m.q_rope, m.kv_lat, m.kv_rope, p);
 }
 
 }  // namespace mla
