@@ -160,6 +160,13 @@ int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
                       const void* tile_meta, void* out, float* lse, float softmax_scale,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* Failure-path self-test: enqueues a two-CTA kernel whose only wait, on a
+ * barrier nothing completes, runs through the same bounded wait as the
+ * decode kernel.  After about 2 s it gives up, records
+ * MLA_ERR_DEVICE_TIMEOUT (read and cleared by mla_check_device_error) and
+ * returns; the context stays usable.  For tests of the failure path only. */
+int mla_selftest_wait_timeout(void* stream);
+
 /* mla_decode for callers that cannot allocate device memory: the same
  * arguments minus the workspace.  The paper has no counterpart; this entry
  * point exists for host frameworks whose allocator owns all device memory

@@ -677,6 +677,17 @@ int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
   return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+int mla_selftest_wait_timeout(void* stream) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = setup_device(device);
+  if (st != MLA_OK) return st;
+  return launch_wait_selftest(g_dev[device].err, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
 int mla_check_device_error(void* stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;

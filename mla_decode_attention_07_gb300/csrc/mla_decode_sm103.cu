@@ -1144,7 +1144,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreads :
   }
 }
 
+// Self-test of the failure path: a two-CTA cluster whose only wait, on an
+// mbarrier nothing arrives on, goes through wait_bar.  The first CTA to give
+// up (after kWaitTimeoutNs) records MLA_ERR_DEVICE_TIMEOUT and raises both
+// CTAs' abort flags, the other sees its flag and gives up too, and both
+// leave through a cluster barrier, as the decode kernel's teardown does.
+__global__ void __cluster_dims__(2, 1, 1) mla_wait_selftest_kernel(int* err) {
+  __shared__ __align__(8) uint64_t never;
+  __shared__ uint32_t abort_flag;
+  const uint32_t rank = ptx::cluster_ctarank();
+  Ctx x = {};
+  x.rank = rank;
+  x.peer = rank ^ 1u;
+  x.abort_addr = ptx::smem_addr(&abort_flag);
+  x.peer_abort_addr = ptx::map_to_rank(x.abort_addr, x.peer);
+  x.err = err;
+  const uint32_t bar = ptx::smem_addr(&never);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::st_shared_u32(x.abort_addr, 0u);
+    ptx::fence_mbarrier_init();
+  }
+  ptx::cluster_sync();
+  if (threadIdx.x == 0) wait_bar(x, bar, 0u);
+  __syncwarp();
+  ptx::cluster_sync();   // no remote store into either CTA after this point
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int* err, cudaStream_t stream) {
+  mla_wait_selftest_kernel<<<2, 32, 0, stream>>>(err);
+  return cudaGetLastError();
+}
 
 int decode_smem_bytes() { return (int)kSmemAlloc; }
 

@@ -46,6 +46,7 @@ MLA_HD int64_t workspace_slots(int num_clusters) { return 2 * (int64_t)num_clust
 int decode_smem_bytes();
 cudaError_t decode_kernel_setup(int device);
 int decode_max_clusters(int device);  // co-resident 2-CTA clusters, or < 0
+cudaError_t launch_wait_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_decode(const TensorMaps& maps, const DecodeParams& p, int num_clusters,
                           cudaStream_t stream);
 

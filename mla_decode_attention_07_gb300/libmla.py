@@ -29,7 +29,7 @@ MLA_ERR_PLAN = -7
 
 EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_workspace_size", "mla_decode_plan", "mla_decode_plan_host", "mla_decode",
-            "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc", "mla_decode_sparse",
+            "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc", "mla_decode_sparse", "mla_selftest_wait_timeout",
             "mla_check_device_error", "mla_strerror"]
 
 _lib = None
@@ -72,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_decode_noalloc.restype = I
     lib.mla_decode_sparse.argtypes = [V, V, I, V, I, V, V, I, V, I, I, V, V, V, F, V, Z, V]
     lib.mla_decode_sparse.restype = I
+    lib.mla_selftest_wait_timeout.argtypes = [V]
+    lib.mla_selftest_wait_timeout.restype = I
     lib.mla_check_device_error.argtypes = [V]
     lib.mla_check_device_error.restype = I
     lib.mla_strerror.argtypes = [I]
@@ -218,6 +220,12 @@ def mla_decode_noalloc(q, kv_cache, block_table, cache_seqlens, tile_meta, out, 
                                    _ptr(cache_seqlens), B, s_q, h_q, _ptr(tile_meta), _ptr(out),
                                    _ptr(lse), float(softmax_scale), _stream(stream))
     _check(rc, "mla_decode_noalloc")
+
+
+def mla_selftest_wait_timeout(stream=None) -> None:
+    """Failure-path self-test: a wait that nothing satisfies gives up after
+    about 2 s and records MLA_ERR_DEVICE_TIMEOUT (see mla_check_device_error)."""
+    _check(load().mla_selftest_wait_timeout(_stream(stream)), "mla_selftest_wait_timeout")
 
 
 def mla_check_device_error(stream=None) -> int:

@@ -240,3 +240,16 @@ def test_plan_covers_all_pages_on_device(torch_cuda):
                 assert (b, p) not in seen
                 seen.add((b, p))
     assert len(seen) == sum((int(L) + 63) // 64 for L in sl)
+
+
+def test_bounded_wait_times_out_and_context_survives(torch_cuda, oracle_mod):
+    """A wait nothing satisfies gives up (about 2 s), reports
+    MLA_ERR_DEVICE_TIMEOUT, and the next decode on the same context is
+    correct."""
+    libmla.mla_selftest_wait_timeout()
+    assert libmla.mla_check_device_error() == libmla.MLA_ERR_DEVICE_TIMEOUT
+    assert libmla.mla_check_device_error() == 0          # read and cleared
+    inp = W.make_inputs(121, 2, 1, 128, [200, 64], extra_pages=1)
+    out, lse, _ = run_gpu(torch_cuda, inp)
+    ref_o, ref_l = oracle_mod.mla_decode(inp)
+    assert_parity(out, lse, ref_o, ref_l, "after timeout")
