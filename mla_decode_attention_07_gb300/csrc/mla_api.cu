@@ -351,6 +351,15 @@ __global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(c
       lse = m + logf(se);
     }
     const int i = qr / p.h_q, h = qr - i * p.h_q;
+    const int64_t oidx = (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv +
+                         (qb * kCombineQuads + 2 * qpair) * 4;
+    if (qb == 0 && qpair == 0) p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
+    if (p.out_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oidx);
+      dst[0] = acc0;
+      dst[1] = acc1;
+      continue;
+    }
     uint4 u;
     const __nv_bfloat162 a0 = __floats2bfloat162_rn(acc0.x, acc0.y);
     const __nv_bfloat162 a1 = __floats2bfloat162_rn(acc0.z, acc0.w);
@@ -360,10 +369,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(c
     memcpy(&u.y, &a1, 4);
     memcpy(&u.z, &a2, 4);
     memcpy(&u.w, &a3, 4);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                              (((int64_t)b * p.s_q + i) * p.h_q + h) * kDv +
-                              (qb * kCombineQuads + 2 * qpair) * 4) = u;
-    if (qb == 0 && qpair == 0) p.lse[((int64_t)b * p.h_q + h) * p.s_q + i] = lse;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oidx) = u;
   }
   if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
@@ -561,6 +567,7 @@ int prepare_decode(const void* q, const void* kv_cache, int num_pages, const int
   p->plan = static_cast<const int32_t*>(tile_meta);
   p->out = out;
   p->lse = lse;
+  p->out_f32 = 0;
   const int64_t slots = workspace_slots(d.num_clusters);
   p->ws_o = static_cast<float*>(workspace);
   p->ws_lse = static_cast<float*>(workspace) + slots * kSlotFloats;
@@ -586,6 +593,53 @@ int attend(const void* q, const void* kv_cache, const DecodeParams& p, int num_c
       !make_map(&maps.kv_rope, kv_cache, kv_rows, 32, kPageTokens, CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
   return launch_decode(maps, p, num_clusters, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+
+// mla_decode and mla_decode_f32: the main kernel, then the combine; out_f32
+// selects the output element type.
+int decode_impl(const void* q, const void* kv_cache, int num_pages, const int32_t* block_table,
+                int max_pages, const int32_t* cache_seqlens, int batch, int s_q, int h_q,
+                const void* tile_meta, void* out, int out_f32, float* lse, float softmax_scale,
+                void* workspace, size_t workspace_bytes, void* stream) {
+  DecodeParams p;
+  int nc = 0, sms = 0;
+  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens,
+                                batch, s_q, h_q, tile_meta, out, lse, softmax_scale, workspace,
+                                workspace_bytes, &p, &nc, &sms);
+  if (rc != MLA_OK) return rc;
+  p.out_f32 = out_f32;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int a = attend(q, kv_cache, p, nc, s);
+  if (a != MLA_OK) return a;
+  return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int sparse_impl(const void* q, const void* kv_cache, int num_pages, const int32_t* block_table,
+                int max_pages, const int32_t* cache_seqlens, const int32_t* indices, int topk,
+                const int32_t* counts, int batch, int h_q, const void* tile_meta, void* out,
+                int out_f32, float* lse, float softmax_scale, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (!indices || !counts || !cache_seqlens || topk < 1 || !aligned(indices, 4) ||
+      !aligned(counts, 4) || (int64_t)batch * topk >= ((int64_t)1 << 31))
+    return MLA_ERR_INVALID_ARG;
+  DecodeParams p;
+  int nc = 0, sms = 0;
+  // the counts take the place of the sequence lengths: the plan splits them
+  // into chunks of 64 listed positions, and the kernel masks past them
+  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, counts, batch,
+                                1, h_q, tile_meta, out, lse, softmax_scale, workspace,
+                                workspace_bytes, &p, &nc, &sms);
+  if (rc != MLA_OK) return rc;
+  if (!aligned(cache_seqlens, 4)) return MLA_ERR_INVALID_ARG;
+  p.indices = indices;
+  p.cache_len = cache_seqlens;
+  p.topk = topk;
+  p.out_f32 = out_f32;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int a = attend(q, kv_cache, p, nc, s);
+  if (a != MLA_OK) return a;
+  return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -622,6 +676,7 @@ int mla_decode_combine(int batch, int s_q, int h_q, const void* tile_meta, void*
   p.plan = static_cast<const int32_t*>(tile_meta);
   p.out = out;
   p.lse = lse;
+  p.out_f32 = 0;
   const int64_t slots = workspace_slots(d.num_clusters);
   p.ws_o = static_cast<float*>(workspace);
   p.ws_lse = static_cast<float*>(workspace) + slots * kSlotFloats;
@@ -639,16 +694,18 @@ int mla_decode(const void* q, const void* kv_cache, int num_pages, const int32_t
                int max_pages, const int32_t* cache_seqlens, int batch, int s_q, int h_q,
                const void* tile_meta, void* out, float* lse, float softmax_scale,
                void* workspace, size_t workspace_bytes, void* stream) {
-  DecodeParams p;
-  int nc = 0, sms = 0;
-  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens,
-                                batch, s_q, h_q, tile_meta, out, lse, softmax_scale, workspace,
-                                workspace_bytes, &p, &nc, &sms);
-  if (rc != MLA_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int a = attend(q, kv_cache, p, nc, s);
-  if (a != MLA_OK) return a;
-  return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return decode_impl(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens, batch, s_q,
+                     h_q, tile_meta, out, 0, lse, softmax_scale, workspace, workspace_bytes,
+                     stream);
+}
+
+int mla_decode_f32(const void* q, const void* kv_cache, int num_pages,
+                   const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                   int batch, int s_q, int h_q, const void* tile_meta, float* out, float* lse,
+                   float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_impl(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens, batch, s_q,
+                     h_q, tile_meta, out, 1, lse, softmax_scale, workspace, workspace_bytes,
+                     stream);
 }
 
 int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
@@ -656,25 +713,20 @@ int mla_decode_sparse(const void* q, const void* kv_cache, int num_pages,
                       const int32_t* indices, int topk, const int32_t* counts, int batch, int h_q,
                       const void* tile_meta, void* out, float* lse, float softmax_scale,
                       void* workspace, size_t workspace_bytes, void* stream) {
-  if (!indices || !counts || !cache_seqlens || topk < 1 || !aligned(indices, 4) ||
-      !aligned(counts, 4) || (int64_t)batch * topk >= ((int64_t)1 << 31))
-    return MLA_ERR_INVALID_ARG;
-  DecodeParams p;
-  int nc = 0, sms = 0;
-  // the counts take the place of the sequence lengths: the plan splits them
-  // into chunks of 64 listed positions, and the kernel masks past them
-  const int rc = prepare_decode(q, kv_cache, num_pages, block_table, max_pages, counts, batch,
-                                1, h_q, tile_meta, out, lse, softmax_scale, workspace,
-                                workspace_bytes, &p, &nc, &sms);
-  if (rc != MLA_OK) return rc;
-  if (!aligned(cache_seqlens, 4)) return MLA_ERR_INVALID_ARG;
-  p.indices = indices;
-  p.cache_len = cache_seqlens;
-  p.topk = topk;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int a = attend(q, kv_cache, p, nc, s);
-  if (a != MLA_OK) return a;
-  return launch_combine(p, nc, sms, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return sparse_impl(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens, indices, topk,
+                     counts, batch, h_q, tile_meta, out, 0, lse, softmax_scale, workspace,
+                     workspace_bytes, stream);
+}
+
+int mla_decode_sparse_f32(const void* q, const void* kv_cache, int num_pages,
+                          const int32_t* block_table, int max_pages,
+                          const int32_t* cache_seqlens, const int32_t* indices, int topk,
+                          const int32_t* counts, int batch, int h_q, const void* tile_meta,
+                          float* out, float* lse, float softmax_scale, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  return sparse_impl(q, kv_cache, num_pages, block_table, max_pages, cache_seqlens, indices, topk,
+                     counts, batch, h_q, tile_meta, out, 1, lse, softmax_scale, workspace,
+                     workspace_bytes, stream);
 }
 
 int mla_selftest_wait_timeout(void* stream) {

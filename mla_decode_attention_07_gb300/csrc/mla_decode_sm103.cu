@@ -937,7 +937,15 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
       tmem_load32(x.tmem + lane_base + kColO + ch * 32, o);
       if (valid_e) {
         const int d0 = (int)x.rank * 256 + ch * 32;
-        if (direct) {
+        if (direct && prm.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(prm.out) + orow * kDv + d0);
+#pragma unroll
+          for (int qq = 0; qq < 8; ++qq)
+            dst[qq] = make_float4(__uint_as_float(o[4 * qq]) * inv_l,
+                                  __uint_as_float(o[4 * qq + 1]) * inv_l,
+                                  __uint_as_float(o[4 * qq + 2]) * inv_l,
+                                  __uint_as_float(o[4 * qq + 3]) * inv_l);
+        } else if (direct) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
                                                 orow * kDv + d0);
 #pragma unroll

@@ -21,12 +21,13 @@ struct DecodeParams {
   const int32_t* cache_len;    // sparse: cache lengths (bounds of the positions)
   int topk;
   const int32_t* plan;
-  void* out;          // bf16 [B, s_q, h_q, 512]
+  void* out;          // [B, s_q, h_q, 512]: bf16, or fp32 when out_f32
   float* lse;         // fp32 [B, h_q, s_q]
   float* ws_o;        // fp32 [slots][512 / 4][128 rows][4]
   float* ws_lse;      // fp32 [slots, 128]
   int* err;           // device error word
   int batch, s_q, h_q, max_pages, num_pages;
+  int out_f32;        // 1: out is fp32 (the normalised fp32 result, unrounded)
   float scale_log2;   // softmax_scale * log2(e)
 };
 

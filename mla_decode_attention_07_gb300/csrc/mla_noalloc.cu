@@ -62,7 +62,8 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv_cache, int num_p
                                   float softmax_scale, void* stream) {
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return MLA_ERR_CUDA;
-  if (device < 0 || device >= kMaxNoallocDevices) return MLA_ERR_UNSUPPORTED_DEVICE;
+  // the same code every other entry point gives for a device index it cannot track
+  if (device < 0 || device >= kMaxNoallocDevices) return MLA_ERR_INVALID_ARG;
   ScratchAddr& s = g_scratch_addr[device];
   // One-time set-up on this device (it is the current one): the array's
   // device address.  Host code must not hand the symbol itself to a kernel.

@@ -29,7 +29,8 @@ MLA_ERR_PLAN = -7
 
 EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_workspace_size", "mla_decode_plan", "mla_decode_plan_host", "mla_decode",
-            "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc", "mla_decode_sparse", "mla_selftest_wait_timeout",
+            "mla_decode_f32", "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc",
+            "mla_decode_sparse", "mla_decode_sparse_f32", "mla_selftest_wait_timeout",
             "mla_check_device_error", "mla_strerror"]
 
 _lib = None
@@ -64,6 +65,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_decode_plan_host.restype = I
     lib.mla_decode.argtypes = [V, V, I, V, I, V, I, I, I, V, V, V, F, V, Z, V]
     lib.mla_decode.restype = I
+    lib.mla_decode_f32.argtypes = [V, V, I, V, I, V, I, I, I, V, V, V, F, V, Z, V]
+    lib.mla_decode_f32.restype = I
+    lib.mla_decode_sparse_f32.argtypes = [V, V, I, V, I, V, V, I, V, I, I, V, V, V, F, V, Z, V]
+    lib.mla_decode_sparse_f32.restype = I
     lib.mla_decode_attend.argtypes = [V, V, I, V, I, V, I, I, I, V, V, V, F, V, Z, V]
     lib.mla_decode_attend.restype = I
     lib.mla_decode_combine.argtypes = [I, I, I, V, V, V, V, Z, V]
@@ -150,6 +155,17 @@ def mla_decode_plan_host(cache_seqlens, s_q: int, h_q: int, num_clusters: int) -
     return meta
 
 
+def _decode(fn: str, q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
+            softmax_scale: float, workspace, stream) -> None:
+    B, s_q, h_q = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
+    rc = getattr(load(), fn)(_ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(block_table),
+                             int(block_table.shape[1]), _ptr(cache_seqlens), B, s_q, h_q,
+                             _ptr(tile_meta), _ptr(out), _ptr(lse), float(softmax_scale),
+                             _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                             _stream(stream))
+    _check(rc, fn)
+
+
 def mla_decode(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
                softmax_scale: float, workspace, stream=None) -> None:
     """Decode attention on the GPU.
@@ -159,13 +175,30 @@ def mla_decode(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
     lse [B, h_q, s_q] fp32; tile_meta from mla_decode_plan; workspace of at
     least mla_workspace_size bytes.
     """
-    B, s_q, h_q = int(q.shape[0]), int(q.shape[1]), int(q.shape[2])
-    rc = load().mla_decode(_ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]), _ptr(block_table),
-                           int(block_table.shape[1]), _ptr(cache_seqlens), B, s_q, h_q,
-                           _ptr(tile_meta), _ptr(out), _ptr(lse), float(softmax_scale),
-                           _ptr(workspace), int(workspace.numel() * workspace.element_size()),
-                           _stream(stream))
-    _check(rc, "mla_decode")
+    _decode("mla_decode", q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
+            softmax_scale, workspace, stream)
+
+
+def mla_decode_f32(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
+                   softmax_scale: float, workspace, stream=None) -> None:
+    """mla_decode with out fp32 [B, s_q, h_q, 512] (the unrounded result)."""
+    _decode("mla_decode_f32", q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,
+            softmax_scale, workspace, stream)
+
+
+def _decode_sparse(fn: str, q, kv_cache, block_table, cache_seqlens, indices, counts, tile_meta,
+                   out, lse, softmax_scale: float, workspace, stream) -> None:
+    B, h_q = int(q.shape[0]), int(q.shape[2])
+    if int(q.shape[1]) != 1:
+        raise MlaError(MLA_ERR_INVALID_ARG, f"{fn} (s_q must be 1)")
+    rc = getattr(load(), fn)(_ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]),
+                             _ptr(block_table), int(block_table.shape[1]),
+                             _ptr(cache_seqlens), _ptr(indices), int(indices.shape[1]),
+                             _ptr(counts), B, h_q, _ptr(tile_meta), _ptr(out), _ptr(lse),
+                             float(softmax_scale), _ptr(workspace),
+                             int(workspace.numel() * workspace.element_size()),
+                             _stream(stream))
+    _check(rc, fn)
 
 
 def mla_decode_sparse(q, kv_cache, block_table, cache_seqlens, indices, counts, tile_meta, out,
@@ -173,17 +206,15 @@ def mla_decode_sparse(q, kv_cache, block_table, cache_seqlens, indices, counts, 
     """Sparse decode: q [B, 1, h_q, 576]; indices [B, topk] int32 token
     positions; counts [B] int32; tile_meta from mla_decode_plan(counts, 1,
     h_q, ...); out [B, 1, h_q, 512] bf16; lse [B, h_q, 1] fp32."""
-    B, h_q = int(q.shape[0]), int(q.shape[2])
-    if int(q.shape[1]) != 1:
-        raise MlaError(MLA_ERR_INVALID_ARG, "mla_decode_sparse (s_q must be 1)")
-    rc = load().mla_decode_sparse(_ptr(q), _ptr(kv_cache), int(kv_cache.shape[0]),
-                                  _ptr(block_table), int(block_table.shape[1]),
-                                  _ptr(cache_seqlens), _ptr(indices), int(indices.shape[1]),
-                                  _ptr(counts), B, h_q, _ptr(tile_meta), _ptr(out), _ptr(lse),
-                                  float(softmax_scale), _ptr(workspace),
-                                  int(workspace.numel() * workspace.element_size()),
-                                  _stream(stream))
-    _check(rc, "mla_decode_sparse")
+    _decode_sparse("mla_decode_sparse", q, kv_cache, block_table, cache_seqlens, indices, counts,
+                   tile_meta, out, lse, softmax_scale, workspace, stream)
+
+
+def mla_decode_sparse_f32(q, kv_cache, block_table, cache_seqlens, indices, counts, tile_meta,
+                          out, lse, softmax_scale: float, workspace, stream=None) -> None:
+    """mla_decode_sparse with out fp32 [B, 1, h_q, 512]."""
+    _decode_sparse("mla_decode_sparse_f32", q, kv_cache, block_table, cache_seqlens, indices,
+                   counts, tile_meta, out, lse, softmax_scale, workspace, stream)
 
 
 def mla_decode_attend(q, kv_cache, block_table, cache_seqlens, tile_meta, out, lse,

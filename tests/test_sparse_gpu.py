@@ -1,8 +1,8 @@
 """Sparse decode (listed token positions) on the GPU against the fp64 oracle.
 
-Same tolerances as the dense path (max |out err| <= 1e-2, max |lse err| <=
-1e-3, empty rows exactly 0 / -inf, no NaN); rows that see only a few keys
-are held to the bound the bf16 probabilities allow, as in the dense tests.
+Same fixed tolerances as the dense path (max |out err| <= 1e-2, max |lse err|
+<= 1e-3, empty rows exactly 0 / -inf, no NaN), for the fp32 output and for
+the bf16 output, which must be the fp32 output rounded to nearest even.
 The identity list (position j at slot j, count = length) must reproduce the
 dense kernel bit for bit: both then stage the same rows in the same layout.
 """
@@ -11,47 +11,31 @@ import pytest
 
 from mla_decode_attention_07_gb300 import libmla
 from mla_decode_attention_07_gb300 import workloads as W
-from test_parity_gpu import LSE_TOL, assert_parity, run_gpu, to_device, torch_cuda  # noqa: F401
+from test_parity_gpu import (assert_bf16_is_rounded_f32, assert_parity, run_gpu,  # noqa: F401
+                             to_device, torch_cuda)
 
 pytestmark = pytest.mark.gpu
 
 
-def run_sparse(torch, si, check_err=True):
+def run_sparse(torch, si, check_err=True, out_f32=False):
     inp = si.base
     d = to_device(torch, inp)
     dev = torch.device("cuda", 0)
     idx = torch.from_numpy(np.ascontiguousarray(si.indices)).to(dev)
     cnt = torch.from_numpy(np.ascontiguousarray(si.counts)).to(dev)
     B, h_q = inp.batch, inp.h_q
-    out = torch.full((B, 1, h_q, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    odt = torch.float32 if out_f32 else torch.bfloat16
+    out = torch.full((B, 1, h_q, 512), float("nan"), dtype=odt, device="cuda")
     lse = torch.full((B, h_q, 1), float("nan"), dtype=torch.float32, device="cuda")
     meta, ws = libmla.alloc_plan_and_workspace(B, 1, h_q, 0)
     ws.fill_(float("nan"))
     libmla.mla_decode_plan(cnt, 1, h_q, meta)
-    libmla.mla_decode_sparse(d["q"], d["kv"], d["bt"], d["sl"], idx, cnt, meta, out, lse,
-                             inp.softmax_scale, ws)
+    fn = libmla.mla_decode_sparse_f32 if out_f32 else libmla.mla_decode_sparse
+    fn(d["q"], d["kv"], d["bt"], d["sl"], idx, cnt, meta, out, lse, inp.softmax_scale, ws)
     rc = libmla.mla_check_device_error()
     if check_err:
         assert rc == 0, libmla.mla_strerror(rc)
     return out.float().cpu().numpy(), lse.cpu().numpy(), rc
-
-
-def sparse_rounding_bound(si, ref_o):
-    """Elementwise bound on |out - exact| from bf16 P and bf16 out over the
-    selected rows (see the dense tests' bf16_rounding_bound)."""
-    inp = si.base
-    v = (inp.kv_cache.view(np.uint16).astype(np.uint32) << 16).view(np.float32)[:, :, 0, :512]
-    bound = np.zeros_like(ref_o)
-    for b in range(inp.batch):
-        c = int(si.counts[b])
-        if c == 0:
-            continue
-        ts = si.indices[b, :c]
-        rows = v[inp.block_table[b, ts // 64], ts % 64]
-        vmax = np.abs(rows).max(axis=0).astype(np.float64)
-        o = np.abs(ref_o[b])
-        bound[b] = 2.0 ** -8 * (vmax + o) + 2.0 ** -9 * o + 1e-5
-    return bound
 
 
 SPARSE_SMALL = [
@@ -69,16 +53,13 @@ SPARSE_SMALL = [
 def test_sparse_small_parity(torch_cuda, case, oracle_mod):
     seed, h_q, seqlens, topk, counts, repeats = case
     si = W.make_sparse_inputs(seed, len(seqlens), h_q, seqlens, topk, counts, repeats=repeats)
-    out, lse, _ = run_sparse(torch_cuda, si)
     ref_o, ref_l = oracle_mod.mla_decode_sparse(si)
-    assert not np.isnan(out).any() and not np.isnan(lse).any()
-    assert np.array_equal(np.isneginf(lse), np.isneginf(ref_l)), "-inf pattern differs"
-    err = np.abs(out.astype(np.float64) - ref_o)
-    bound = np.maximum(sparse_rounding_bound(si, ref_o), 1e-2)
-    assert (err <= bound).all(), f"case {seed}: max err/bound {float((err / bound).max()):.3f}"
-    fin = ~np.isneginf(ref_l)
-    if fin.any():
-        assert np.abs(lse[fin] - ref_l[fin]).max() <= LSE_TOL
+    out32, lse32, _ = run_sparse(torch_cuda, si, out_f32=True)
+    assert_parity(out32, lse32, ref_o, ref_l, f"sparse case {seed} fp32 out")
+    out16, lse16, _ = run_sparse(torch_cuda, si)
+    assert np.array_equal(lse16, lse32)
+    assert_bf16_is_rounded_f32(out16, out32, f"sparse case {seed}")
+    assert_parity(out16, lse16, ref_o, ref_l, f"sparse case {seed} bf16 out")
 
 
 def test_sparse_identity_list_is_dense(torch_cuda):
