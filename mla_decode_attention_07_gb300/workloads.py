@@ -347,3 +347,120 @@ SPARSE_WORKLOADS = {
                                                     h_q=128, seqlen=131072, topk=2048,
                                                     pool_pages=8192, seed=5),
 }
+
+
+# ---------------------------------------------------------------------------
+# The steps before the decode call (DeepSeek MLA): the new tokens' cache rows
+# and the query parts the absorption contracts, and the tensor-core GEMM's
+# factors.  Only numbers are drawn here; the arithmetic is elsewhere.
+D_NOPE = 128        # per-head query dims contracted with W_UK
+D_ROPE = 64         # per-head rotary query dims (the last 64 of the 576)
+D_C = 512           # latent dims
+
+TENSOR_KV_NEW = 0x4E57
+TENSOR_Q_NOPE = 0x514E
+TENSOR_Q_ROPE = 0x5152
+TENSOR_W_UK = 0x574B
+TENSOR_GEMM_A = 0x4741
+TENSOR_GEMM_B = 0x4742
+
+
+def normal_f16(seed: int, tensor_id: int, n: int) -> np.ndarray:
+    """``n`` N(0,1) samples (the same Box-Muller stream as normal_bf16)
+    rounded to float32, then to IEEE binary16 with round-to-nearest-even."""
+    start = (seed ^ tensor_id) & 0xFFFFFFFFFFFFFFFF
+    pairs = (n + 1) // 2
+    z = splitmix64(start, 0, 2 * pairs)
+    r = np.sqrt(-2.0 * np.log(_uniform01(z[0::2])))
+    th = 2.0 * math.pi * _uniform01(z[1::2])
+    vals = np.empty(2 * pairs, dtype=np.float64)
+    vals[0::2] = r * np.cos(th)
+    vals[1::2] = r * np.sin(th)
+    return vals[:n].astype(np.float32).astype(np.float16).view(np.uint16)
+
+
+def scaled_normal_bf16(seed: int, tensor_id: int, n: int, std: float) -> np.ndarray:
+    """N(0, std^2) samples rounded to bf16 bits (std applied in float32)."""
+    v = bf16_bits_to_float32(normal_bf16(seed, tensor_id, n)) * np.float32(std)
+    return float32_to_bf16_bits(v)
+
+
+@dataclasses.dataclass
+class PrologueInputs:
+    base: DecodeInputs           # cache, block table and lengths (counting the new tokens)
+    kv_new: np.ndarray           # uint16 [B, s_q, 576] rows of the new tokens
+    q_nope: np.ndarray           # uint16 [B, s_q, h_q, 128]
+    q_rope: np.ndarray           # uint16 [B, s_q, h_q, 64]
+    w_uk: np.ndarray             # uint16 [h_q, 128, 512], N(0, 1/128)
+
+
+def make_prologue_inputs(seed: int, batch: int, s_q: int, h_q: int, seqlens, *,
+                         extra_pages: int = 0) -> PrologueInputs:
+    base = make_inputs(seed, batch, s_q, h_q, seqlens, extra_pages=extra_pages, poison=False)
+    kv_new = normal_bf16(seed, TENSOR_KV_NEW, batch * s_q * D_QK).reshape(batch, s_q, D_QK)
+    q_nope = normal_bf16(seed, TENSOR_Q_NOPE, batch * s_q * h_q * D_NOPE).reshape(
+        batch, s_q, h_q, D_NOPE)
+    q_rope = normal_bf16(seed, TENSOR_Q_ROPE, batch * s_q * h_q * D_ROPE).reshape(
+        batch, s_q, h_q, D_ROPE)
+    w_uk = scaled_normal_bf16(seed, TENSOR_W_UK, h_q * D_NOPE * D_C, D_NOPE ** -0.5).reshape(
+        h_q, D_NOPE, D_C)
+    return PrologueInputs(base=base, kv_new=kv_new, q_nope=q_nope, q_rope=q_rope, w_uk=w_uk)
+
+
+@dataclasses.dataclass
+class PrologueWorkload:
+    """Append + absorption at the shape of a decode workload."""
+    name: str
+    batch: int
+    s_q: int
+    h_q: int
+    seqlen: int
+    seed: int = 0
+
+    def make(self) -> PrologueInputs:
+        return make_prologue_inputs(self.seed, self.batch, self.s_q, self.h_q,
+                                    np.full(self.batch, self.seqlen, dtype=np.int32))
+
+    def absorb_flops(self) -> float:
+        return 2.0 * self.batch * self.s_q * self.h_q * D_NOPE * D_C
+
+    def absorb_bytes(self) -> float:
+        """W_UK once, q_nope and q_rope read, the 576-wide query written."""
+        rows = self.batch * self.s_q * self.h_q
+        return float(self.h_q * D_NOPE * D_C * 2 + rows * (D_NOPE + D_ROPE) * 2 + rows * D_QK * 2)
+
+    def append_bytes(self) -> float:
+        """Each new row read once and written once."""
+        return float(2 * self.batch * self.s_q * D_QK * 2)
+
+
+PROLOGUE_WORKLOADS = {
+    "prologue_b16_h128": PrologueWorkload("prologue_b16_h128", 16, 1, 128, 4096, seed=1),
+    "prologue_b132_sq2_h128": PrologueWorkload("prologue_b132_sq2_h128", 132, 2, 128, 8192,
+                                               seed=3),
+}
+
+
+@dataclasses.dataclass
+class GemmWorkload:
+    """C = A B with A [M, K], B [K, N] row-major, fp16 inputs N(0, 1)."""
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int = 0
+
+    def make(self):
+        a = normal_f16(self.seed, TENSOR_GEMM_A, self.M * self.K).reshape(self.M, self.K)
+        b = normal_f16(self.seed, TENSOR_GEMM_B, self.K * self.N).reshape(self.K, self.N)
+        return a, b
+
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    def bytes(self) -> float:
+        return float(2 * (self.M * self.K + self.K * self.N + self.M * self.N))
+
+
+# The GEMM tutorial's comparison: FP16, 2048 x 2048 x 2048.
+GEMM_WORKLOADS = {"gemm_f16_2048": GemmWorkload("gemm_f16_2048", 2048, 2048, 2048, seed=6)}

@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for paged MLA decode (test infrastructure).
+"""fp64 CPU oracles for paged MLA decode and its neighbouring steps (test infrastructure).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package; the library itself never does.  The arithmetic
@@ -11,6 +11,11 @@ tokens), values = the first 512 dims of the same row, lse = natural log of
 the softmax denominator of the scaled logits.  Sparse decode (one query
 token per entry) is the same attention over the cache rows at a listed set of
 token positions.  The header of ``mla_oracle.c`` states both in full.
+
+``prologue_oracle.c`` writes out the two steps that prepare a decode call
+(the new tokens' rows appended to the paged cache, bit for bit; the query
+absorbed through W_UK, in fp64) and ``gemm_oracle.c`` the plain matrix
+product C = A B of the tensor-core GEMM, in fp64 from fp16 or bf16 inputs.
 """
 from __future__ import annotations
 
@@ -24,6 +29,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "mla_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "libmla_oracle.so")
+PROLOGUE_SOURCE = os.path.join(_HERE, "prologue_oracle.c")
+_PROLOGUE_LIB = os.path.join(_HERE, "_build", "libprologue_oracle.so")
+GEMM_SOURCE = os.path.join(_HERE, "gemm_oracle.c")
+_GEMM_LIB = os.path.join(_HERE, "_build", "libgemm_oracle.so")
 
 D_V = 512
 
@@ -38,11 +47,18 @@ def compile_source(src: str, lib_path: str) -> str:
     return lib_path
 
 
+def _build_one(src: str, lib: str, force: bool) -> str:
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
+        compile_source(src, lib)
+    return lib
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle (plain C, no target-specific flags)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
-        compile_source(SOURCE, _LIB)
-    return _LIB
+    """Compile the oracles (plain C, no target-specific flags); returns the
+    decode oracle's library."""
+    _build_one(PROLOGUE_SOURCE, _PROLOGUE_LIB, force)
+    _build_one(GEMM_SOURCE, _GEMM_LIB, force)
+    return _build_one(SOURCE, _LIB, force)
 
 
 def default_threads() -> int:
@@ -152,7 +168,95 @@ class Oracle:
         return float(lse[0]), out
 
 
+class Prologue:
+    """ctypes front end of the cache-append / query-absorption oracle."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_cache_append.argtypes = [P, P, I, P, I, P, I, I]
+        lib.oracle_cache_append.restype = I
+        lib.oracle_q_absorb.argtypes = [P, P, I, I, I, I, P]
+        lib.oracle_q_absorb.restype = None
+        self.lib = lib
+
+    def cache_append(self, kv_new, kv_cache, block_table, cache_seqlens):
+        """Returns a copy of kv_cache (uint16 [pages, 64, 1, 576]) with the new
+        rows (uint16 [B, s_q, 576]) written at positions L_b - s_q + i."""
+        kv_new = np.ascontiguousarray(kv_new, dtype=np.uint16)
+        B, s_q = int(kv_new.shape[0]), int(kv_new.shape[1])
+        cache = np.array(kv_cache, dtype=np.uint16, copy=True, order="C")
+        _n, np_ = _c(kv_new, np.uint16)
+        _bt, btp = _c(block_table, np.int32)
+        _sl, slp = _c(cache_seqlens, np.int32)
+        rc = self.lib.oracle_cache_append(np_, cache.ctypes.data_as(ctypes.c_void_p),
+                                          int(cache.shape[0]), btp, int(_bt.shape[1]), slp, B,
+                                          s_q)
+        if rc != 0:
+            raise ValueError("oracle: new token position or page out of range")
+        return cache
+
+    def q_absorb(self, q_nope, w_uk):
+        """q_nope uint16 [B, s_q, h_q, d_nope], w_uk uint16 [h_q, d_nope, d_c]
+        -> fp64 [B, s_q, h_q, d_c]."""
+        q_nope = np.ascontiguousarray(q_nope, dtype=np.uint16)
+        B, s_q, h_q, dn = (int(x) for x in q_nope.shape)
+        w_uk = np.ascontiguousarray(w_uk, dtype=np.uint16)
+        assert w_uk.shape[0] == h_q and w_uk.shape[1] == dn
+        dc = int(w_uk.shape[2])
+        out = np.zeros((B, s_q, h_q, dc), dtype=np.float64)
+        self.lib.oracle_q_absorb(q_nope.ctypes.data_as(ctypes.c_void_p),
+                                 w_uk.ctypes.data_as(ctypes.c_void_p), B * s_q, h_q, dn, dc,
+                                 out.ctypes.data_as(ctypes.c_void_p))
+        return out
+
+
+class Gemm:
+    """ctypes front end of the GEMM oracle (fmt 0: fp16 inputs, 1: bf16)."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        lib.oracle_gemm.argtypes = [P, P, I, I, I, I, P, I]
+        lib.oracle_gemm.restype = I
+        lib.oracle_gemm_entries.argtypes = [P, P, I, I, I, I, I, P, P, I]
+        lib.oracle_gemm_entries.restype = I
+        self.lib = lib
+
+    def gemm(self, a_bits, b_bits, fmt: int, nthreads: int | None = None):
+        """a_bits uint16 [M, K], b_bits uint16 [K, N] -> C fp64 [M, N]."""
+        a = np.ascontiguousarray(a_bits, dtype=np.uint16)
+        b = np.ascontiguousarray(b_bits, dtype=np.uint16)
+        M, K = a.shape
+        K2, N = b.shape
+        assert K == K2
+        c = np.zeros((M, N), dtype=np.float64)
+        self.lib.oracle_gemm(a.ctypes.data_as(ctypes.c_void_p), b.ctypes.data_as(ctypes.c_void_p),
+                             M, N, K, int(fmt), c.ctypes.data_as(ctypes.c_void_p),
+                             nthreads or default_threads())
+        return c
+
+    def gemm_entries(self, a_bits, b_bits, fmt: int, entries, nthreads: int | None = None):
+        """Selected entries (array of (m, n)) of C = A B, fp64 [n]."""
+        a = np.ascontiguousarray(a_bits, dtype=np.uint16)
+        b = np.ascontiguousarray(b_bits, dtype=np.uint16)
+        M, K = a.shape
+        N = b.shape[1]
+        e = np.ascontiguousarray(np.asarray(entries, dtype=np.int32).reshape(-1, 2))
+        out = np.zeros(e.shape[0], dtype=np.float64)
+        rc = self.lib.oracle_gemm_entries(a.ctypes.data_as(ctypes.c_void_p),
+                                          b.ctypes.data_as(ctypes.c_void_p), M, N, K, int(fmt),
+                                          int(e.shape[0]), e.ctypes.data_as(ctypes.c_void_p),
+                                          out.ctypes.data_as(ctypes.c_void_p),
+                                          nthreads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle: GEMM entry out of range")
+        return out
+
+
 _default: Oracle | None = None
+_prologue: Prologue | None = None
+_gemm: Gemm | None = None
 
 
 def default() -> Oracle:
@@ -181,6 +285,38 @@ def mla_decode_sparse(si, nthreads=None, scale=None):
 def mla_decode_sparse_rows(si, rows_bh, key_begin=0, key_end=2**31 - 1, nthreads=None,
                            scale=None):
     return default().mla_decode_sparse_rows(si, rows_bh, key_begin, key_end, nthreads, scale)
+
+
+def prologue() -> Prologue:
+    global _prologue
+    if _prologue is None:
+        build()
+        _prologue = Prologue(_PROLOGUE_LIB)
+    return _prologue
+
+
+def gemm_oracle() -> Gemm:
+    global _gemm
+    if _gemm is None:
+        build()
+        _gemm = Gemm(_GEMM_LIB)
+    return _gemm
+
+
+def cache_append(kv_new, kv_cache, block_table, cache_seqlens):
+    return prologue().cache_append(kv_new, kv_cache, block_table, cache_seqlens)
+
+
+def q_absorb(q_nope, w_uk):
+    return prologue().q_absorb(q_nope, w_uk)
+
+
+def gemm(a_bits, b_bits, fmt, nthreads=None):
+    return gemm_oracle().gemm(a_bits, b_bits, fmt, nthreads)
+
+
+def gemm_entries(a_bits, b_bits, fmt, entries, nthreads=None):
+    return gemm_oracle().gemm_entries(a_bits, b_bits, fmt, entries, nthreads)
 
 
 if __name__ == "__main__":  # pragma: no cover

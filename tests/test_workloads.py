@@ -99,3 +99,22 @@ def test_sparse_pool_block_tables_stay_in_the_pool():
     assert si.base.block_table.shape == (3, 16)
     assert ((si.base.block_table >= 0) & (si.base.block_table < 7)).all()
     assert si.base.q.shape == (3, 1, 16, W.D_QK)
+
+
+def test_step_generators_shapes_and_determinism():
+    p1 = W.make_prologue_inputs(3, 2, 2, 16, [100, 70])
+    p2 = W.make_prologue_inputs(3, 2, 2, 16, [100, 70])
+    assert p1.kv_new.shape == (2, 2, W.D_QK) and p1.q_nope.shape == (2, 2, 16, W.D_NOPE)
+    assert p1.q_rope.shape == (2, 2, 16, W.D_ROPE) and p1.w_uk.shape == (16, W.D_NOPE, W.D_C)
+    assert np.array_equal(p1.w_uk, p2.w_uk) and np.array_equal(p1.kv_new, p2.kv_new)
+    std = float(W.bf16_bits_to_float32(p1.w_uk).std())
+    assert abs(std - W.D_NOPE ** -0.5) < 0.01
+
+
+def test_normal_f16_is_rounded_from_the_float32_stream():
+    a = W.normal_f16(6, W.TENSOR_GEMM_A, 4096)
+    v = a.view(np.float16).astype(np.float64)
+    assert abs(v.mean()) < 0.1 and abs(v.std() - 1.0) < 0.05
+    # rounding float16 -> float32 -> float16 is the identity on these bits
+    assert np.array_equal(v.astype(np.float32).astype(np.float16).view(np.uint16), a)
+    assert np.array_equal(W.normal_f16(6, W.TENSOR_GEMM_A, 10), a[:10])
