@@ -58,7 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=sorted(W.WORKLOADS) + sorted(W.SPARSE_WORKLOADS))
+                    choices=sorted(W.WORKLOADS) + sorted(W.SPARSE_WORKLOADS) +
+                    sorted(W.GEMM_WORKLOADS) + sorted(W.PROLOGUE_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the oracle baseline leg")
@@ -764,8 +765,251 @@ def run_sparse(args):
         torch.distributed.destroy_process_group()
 
 
+def _timed_loop(torch, stream, fn, n):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for i in range(n):
+        fn(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def _single_gpu_setup():
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    return torch, world, rank, dev
+
+
+GEMM_METRIC = "FP16 GEMM TFLOP/s and % of GB300 dense-bf16/fp16 tensor peak (1 GPU)"
+
+
+def run_gemm(args):
+    """C = A B (fp16 in, fp32 accumulate, fp16 out) through mla_gemm; cuBLAS
+    (torch.matmul) timed on the same rotating input sets beside it."""
+    torch, world, rank, dev = _single_gpu_setup()
+    from mla_decode_attention_07_gb300 import libmla
+    libmla.load()
+    w = W.GEMM_WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    nsets = max(2, math.ceil(2.5 * l2 / w.bytes()))
+    sets = []
+    for k in range(nsets):
+        if k == 0:
+            a, b = w.make()
+        else:
+            a = W.normal_f16(w.seed + 7919 * k, W.TENSOR_GEMM_A, w.M * w.K).reshape(w.M, w.K)
+            b = W.normal_f16(w.seed + 7919 * k, W.TENSOR_GEMM_B, w.K * w.N).reshape(w.K, w.N)
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x.view(np.int16))).to(dev).view(
+            torch.float16)
+        sets.append((t(a), t(b), torch.empty((w.M, w.N), dtype=torch.float16, device=dev)))
+    stream = torch.cuda.current_stream(dev)
+
+    def ours(i):
+        a, b, c = sets[i % nsets]
+        libmla.mla_gemm(a, b, c, stream)
+
+    def cublas(i):
+        a, b, c = sets[i % nsets]
+        torch.matmul(a, b, out=c)
+
+    for i in range(max(3, args.warmup)):
+        ours(i)
+        cublas(i)
+    torch.cuda.synchronize()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error during warm-up: {libmla.mla_strerror(rc)}")
+    sampler = ClockSampler(physical_gpu_index(dev.index))
+    sampler.start()
+    t_end = time.perf_counter() + 1.0
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            ours(i)
+            i += 1
+        torch.cuda.synchronize()
+    K = args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    ms = aggregate_max(_timed_loop(torch, stream, ours, K), world)
+    ms_cublas = _timed_loop(torch, stream, cublas, K)
+    clocks = sampler.stop()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error in timed region: {libmla.mla_strerror(rc)}")
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    tf_cublas = w.flops() / (ms_cublas * 1e-3) / 1e12
+    # e2e: A and B copied in from pinned host memory, C copied back, per step
+    ha = torch.from_numpy(np.ascontiguousarray(w.make()[0].view(np.int16))).pin_memory()
+    hb = torch.from_numpy(np.ascontiguousarray(w.make()[1].view(np.int16))).pin_memory()
+    hc = torch.empty((w.M, w.N), dtype=torch.int16).pin_memory()
+    da, db, dc = sets[0]
+
+    def e2e(i):
+        da.view(torch.int16).copy_(ha, non_blocking=True)
+        db.view(torch.int16).copy_(hb, non_blocking=True)
+        libmla.mla_gemm(da, db, dc, stream)
+        hc.copy_(dc.view(torch.int16), non_blocking=True)
+
+    for i in range(3):
+        e2e(i)
+    e2e_ms = aggregate_max(_timed_loop(torch, stream, e2e, max(5, K // 4)), world)
+    result = {
+        "metric": GEMM_METRIC, "value": round(tf * world, 3), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1) rounded to fp16)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "l2": f"rotating {nsets} input sets of {w.bytes() / 1e6:.1f} MB (> 2.5 x L2)",
+                   "parallelism": "single GPU" if world == 1 else f"{world} replicas"},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "traffic": None, "kernel": "mla_gemm_kernel",
+                     "peak_source": f"{peak_src}: bf16 burst (fp16 has the same nominal rate)"},
+        "cublas": {"value": round(tf_cublas, 3), "unit": "TFLOP/s",
+                   "ms_per_step": round(ms_cublas, 5), "ratio": round(tf / tf_cublas, 4),
+                   "how": "torch.matmul(out=) on the same rotating fp16 sets"},
+        "gpu_launches": K,
+        "e2e": {"value": round(w.flops() * world / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": 2 * 2 * w.M * w.K,
+                "d2h_bytes_per_step": 2 * w.M * w.N},
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        a0, b0 = w.make()
+        rng = np.random.default_rng(0)
+        n = 4096
+        ent = np.stack([rng.integers(0, w.M, n), rng.integers(0, w.N, n)], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.gemm_entries(a0, b0, 0, ent)
+        dt = time.perf_counter() - t0
+        result["cpu_baseline"] = {"value": 2.0 * w.K * n / dt / 1e12, "unit": "TFLOP/s",
+                                  "cores": oracle.default_threads(), "kind": "oracle",
+                                  "sample": f"{n} sampled entries of C, fp64 C oracle, "
+                                            f"{dt:.2f} s"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+PROLOGUE_METRIC = "MLA decode-step prologue (cache append + query absorption) GB/s and us per call"
+
+
+def run_prologue(args):
+    """mla_cache_append + mla_q_absorb per step at a decode workload's shape;
+    input sets (W_UK of a layer each) rotate so that every step reads its
+    weights from HBM, as successive layers do."""
+    torch, world, rank, dev = _single_gpu_setup()
+    from mla_decode_attention_07_gb300 import libmla
+    libmla.load()
+    w = W.PROLOGUE_WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20))
+    p0 = w.make()
+    bf = torch.bfloat16
+    t = lambda x, dt=None: (torch.from_numpy(np.ascontiguousarray(x)).to(dev) if dt is None else
+                            torch.from_numpy(np.ascontiguousarray(x.view(np.int16))).to(dev).view(dt))
+    kv = t(p0.base.kv_cache, bf)
+    bt, sl = t(p0.base.block_table), t(p0.base.cache_seqlens)
+    nsets = max(2, math.ceil(2.5 * l2 / w.absorb_bytes()))
+    sets = []
+    for k in range(nsets):
+        sd = w.seed + 7919 * k
+        rows = w.batch * w.s_q
+        sets.append(dict(
+            new=t(W.normal_bf16(sd, W.TENSOR_KV_NEW, rows * W.D_QK).reshape(w.batch, w.s_q, W.D_QK), bf),
+            qn=t(W.normal_bf16(sd, W.TENSOR_Q_NOPE, rows * w.h_q * W.D_NOPE).reshape(
+                w.batch, w.s_q, w.h_q, W.D_NOPE), bf),
+            qr=t(W.normal_bf16(sd, W.TENSOR_Q_ROPE, rows * w.h_q * W.D_ROPE).reshape(
+                w.batch, w.s_q, w.h_q, W.D_ROPE), bf),
+            wuk=t(W.scaled_normal_bf16(sd, W.TENSOR_W_UK, w.h_q * W.D_NOPE * W.D_C,
+                                       W.D_NOPE ** -0.5).reshape(w.h_q, W.D_NOPE, W.D_C), bf),
+            q=torch.empty((w.batch, w.s_q, w.h_q, W.D_QK), dtype=bf, device=dev)))
+    stream = torch.cuda.current_stream(dev)
+
+    def append(i):
+        st = sets[i % nsets]
+        libmla.mla_cache_append(st["new"], kv, bt, sl, stream)
+
+    def absorb(i):
+        st = sets[i % nsets]
+        libmla.mla_q_absorb(st["qn"], st["qr"], st["wuk"], st["q"], stream)
+
+    def step(i):
+        append(i)
+        absorb(i)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error during warm-up: {libmla.mla_strerror(rc)}")
+    sampler = ClockSampler(physical_gpu_index(dev.index))
+    sampler.start()
+    K = args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    ms = aggregate_max(_timed_loop(torch, stream, step, K), world)
+    ms_append = _timed_loop(torch, stream, append, K)
+    ms_absorb = _timed_loop(torch, stream, absorb, K)
+    clocks = sampler.stop()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error in timed region: {libmla.mla_strerror(rc)}")
+    nbytes = w.absorb_bytes() + w.append_bytes()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    absorb_gbs = w.absorb_bytes() / (ms_absorb * 1e-3) / 1e9
+    result = {
+        "metric": PROLOGUE_METRIC, "value": round(gbs * world, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rows and queries, W_UK ~ N(0, 1/128), bf16)",
+        "config": {"workload": w.name, "batch": w.batch, "s_q": w.s_q, "h_q": w.h_q,
+                   "d_nope": W.D_NOPE, "d_c": W.D_C,
+                   "l2": f"rotating {nsets} weight/query sets of {w.absorb_bytes() / 1e6:.1f} MB "
+                         "(> 2.5 x L2)",
+                   "parallelism": "single GPU" if world == 1 else f"{world} replicas"},
+        "us_per_call": {"append": round(ms_append * 1e3, 3), "absorb": round(ms_absorb * 1e3, 3),
+                        "step": round(ms * 1e3, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(absorb_gbs, 2), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(absorb_gbs / peaks["hbm_gbs"], 4),
+                     "traffic": None,
+                     "kernel": "mla_gemm_kernel (absorption; + its rotary copy)",
+                     "bytes_per_call": w.absorb_bytes(), "peak_source": peak_src},
+        "absorb_tflops": round(w.absorb_flops() / (ms_absorb * 1e-3) / 1e12, 3),
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.workload in W.GEMM_WORKLOADS or args.workload in W.PROLOGUE_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm is timed on the decode workloads; this line "
+                              "carries its own cpu_baseline or cuBLAS comparison"}), flush=True)
+        elif args.workload in W.GEMM_WORKLOADS:
+            run_gemm(args)
+        else:
+            run_prologue(args)
+        return
     if args.workload in W.SPARSE_WORKLOADS:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":

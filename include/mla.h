@@ -71,6 +71,11 @@ extern "C" {
 #define MLA_ERR_UNSUPPORTED_DEVICE (-6) /* the device is not sm_103 */
 #define MLA_ERR_PLAN (-7)               /* tile_meta does not match the call */
 
+/* Element types of mla_gemm's operands and result. */
+#define MLA_DTYPE_F16 0
+#define MLA_DTYPE_BF16 1
+#define MLA_DTYPE_F32 2
+
 /* Number of two-CTA clusters the decode kernel runs as a persistent grid on
  * `device` (the SM count halved, limited by cluster occupancy).  Returns a
  * negative code on error.
@@ -216,6 +221,62 @@ int mla_decode_sparse_f32(const void* q, const void* kv_cache, int num_pages,
                           const int32_t* counts, int batch, int h_q, const void* tile_meta,
                           float* out, float* lse, float softmax_scale, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------
+ * The steps before the decode call, and the tensor-core GEMM.
+ * --------------------------------------------------------------------- */
+
+/* Appends the new tokens' latent cache rows.  For batch entry b and new
+ * token i < s_q, position t = cache_seqlens[b] - s_q + i (the lengths
+ * already count the new tokens, as mla_decode expects), and
+ *   kv_cache[block_table[b][t / 64]][t % 64][0][0:576] = kv_new[b][i][0:576]
+ * bit for bit; nothing else in the cache changes.
+ *   kv_new        bf16 [batch, s_q, 576]      device, 16-byte aligned
+ *   kv_cache      bf16 [num_pages, 64, 1, 576] device, 16-byte aligned
+ *   block_table   int32 [batch, max_pages]    device
+ *   cache_seqlens int32 [batch]               device
+ * A position below 0 or past the block table, or a page outside the pool,
+ * is flagged as MLA_ERR_DEVICE_BOUNDS (read by mla_check_device_error) and
+ * that row is skipped; the other rows are written.
+ * Defined by: no passage.  The TileLang talk (section 什么是「TileLang」)
+ * names the DeepSeek MLA decode kernel this feeds; the pages say nothing of
+ * how the cache is filled, and this is DeepSeek's paged-cache write of the
+ * 512 latent + 64 rotary dims of each new token.
+ * Errors: MLA_ERR_INVALID_ARG (null, misaligned, bad size) before anything
+ * is enqueued, MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA. */
+int mla_cache_append(const void* kv_new, void* kv_cache, int num_pages,
+                     const int32_t* block_table, int max_pages, const int32_t* cache_seqlens,
+                     int batch, int s_q, void* stream);
+
+/* Query absorption: builds mla_decode's query from the per-head query parts.
+ *   q[b][i][h][0:512]   = sum_{d<128} q_nope[b][i][h][d] * w_uk[h][d][0:512]
+ *   q[b][i][h][512:576] = q_rope[b][i][h][0:64]
+ *   q_nope bf16 [batch, s_q, h_q, 128], q_rope bf16 [batch, s_q, h_q, 64],
+ *   w_uk bf16 [h_q, 128, 512] (the key up-projection of each head),
+ *   q bf16 [batch, s_q, h_q, 576]; all device, 16-byte aligned.
+ * The contraction runs on the tensor cores as a GEMM batched over heads
+ * (fp32 accumulation; q_latent rounded to bf16, nearest even).
+ * Defined by: no passage (as mla_cache_append): DeepSeek MLA's absorbed
+ * form, in which W_UK is folded into the query so that the scores are taken
+ * against the 512-dim latent cache directly.
+ * Errors: MLA_ERR_INVALID_ARG before anything is enqueued,
+ * MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA; a bounded device wait that ran
+ * out is reported by mla_check_device_error. */
+int mla_q_absorb(const void* q_nope, const void* q_rope, const void* w_uk, void* q, int batch,
+                 int s_q, int h_q, void* stream);
+
+/* Tensor-core GEMM: C = A B with A [M, K] and B [K, N] row-major, both
+ * in_dtype (MLA_DTYPE_F16 or MLA_DTYPE_BF16), fp32 accumulation, C [M, N]
+ * row-major in out_dtype (F16, BF16: round to nearest even; or F32).
+ * N and K must be multiples of 8; A, B, C 16-byte aligned; any M.
+ * Defined by: the GEMM tutorial summary ("Designing high-performance GPU
+ * kernels with TileLang: Tensor-Core GEMM", the comparison table): an FP16
+ * 2048 x 2048 x 2048 GEMM measured against cuBLAS, relative error < 2e-2.
+ * Errors: MLA_ERR_INVALID_ARG before anything is enqueued,
+ * MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA; a bounded device wait that ran
+ * out is reported by mla_check_device_error. */
+int mla_gemm(const void* A, const void* B, void* C, int M, int N, int K, int in_dtype,
+             int out_dtype, void* stream);
 
 /* Failure-path self-test: enqueues a two-CTA kernel whose only wait, on a
  * barrier nothing completes, runs through the same bounded wait as the

@@ -455,6 +455,34 @@ int64_t workspace_bytes_for(int num_clusters) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
+
+int device_current(int* device, int* num_sms, int** err) {
+  if (cudaGetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = setup_device(*device);
+  if (st != MLA_OK) return st;
+  *num_sms = g_dev[*device].num_sms;
+  *err = g_dev[*device].err;
+  return MLA_OK;
+}
+
+bool encode_tiled_map(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  return enc(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mla
 
 using namespace mla;

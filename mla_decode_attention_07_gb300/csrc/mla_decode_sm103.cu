@@ -937,15 +937,7 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
       tmem_load32(x.tmem + lane_base + kColO + ch * 32, o);
       if (valid_e) {
         const int d0 = (int)x.rank * 256 + ch * 32;
-        if (direct && prm.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(prm.out) + orow * kDv + d0);
-#pragma unroll
-          for (int qq = 0; qq < 8; ++qq)
-            dst[qq] = make_float4(__uint_as_float(o[4 * qq]) * inv_l,
-                                  __uint_as_float(o[4 * qq + 1]) * inv_l,
-                                  __uint_as_float(o[4 * qq + 2]) * inv_l,
-                                  __uint_as_float(o[4 * qq + 3]) * inv_l);
-        } else if (direct) {
+        if (direct && !prm.out_f32) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
                                                 orow * kDv + d0);
 #pragma unroll
@@ -962,15 +954,19 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
             dst[qq] = u;
           }
         } else {
-          float4* base =
-              reinterpret_cast<float4*>(prm.ws_o) + slot * (kDv / 4) * kTileRows + re;
+          // fp32: the final output row (fp32 out), or this split's partial
+          // ([dim / 4][row][4] in the workspace slot)
+          float4* base = direct ? reinterpret_cast<float4*>(static_cast<float*>(prm.out) +
+                                                            orow * kDv + d0)
+                                : reinterpret_cast<float4*>(prm.ws_o) +
+                                      slot * (kDv / 4) * kTileRows + (int64_t)(d0 / 4) * kTileRows + re;
+          const int64_t step = direct ? 1 : kTileRows;
 #pragma unroll
           for (int qq = 0; qq < 8; ++qq)
-            base[(int64_t)(d0 / 4 + qq) * kTileRows] =
-                make_float4(__uint_as_float(o[4 * qq]) * inv_l,
-                            __uint_as_float(o[4 * qq + 1]) * inv_l,
-                            __uint_as_float(o[4 * qq + 2]) * inv_l,
-                            __uint_as_float(o[4 * qq + 3]) * inv_l);
+            base[qq * step] = make_float4(__uint_as_float(o[4 * qq]) * inv_l,
+                                          __uint_as_float(o[4 * qq + 1]) * inv_l,
+                                          __uint_as_float(o[4 * qq + 2]) * inv_l,
+                                          __uint_as_float(o[4 * qq + 3]) * inv_l);
         }
       }
     }

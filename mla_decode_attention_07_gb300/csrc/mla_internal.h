@@ -51,6 +51,16 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_decode(const TensorMaps& maps, const DecodeParams& p, int num_clusters,
                           cudaStream_t stream);
 
+// Device set-up shared by every entry point (mla_api.cu): the current device,
+// its SM count and the address of its device error word; MLA_OK or an error.
+int device_current(int* device, int* num_sms, int** err);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point; `rank`
+// dims (innermost first), rank - 1 byte strides, a box of `box` elements.
+bool encode_tiled_map(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base,
+                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swz);
+
 // Combine kernel (mla_api.cu).
 cudaError_t launch_combine(const DecodeParams& p, int num_clusters, int num_sms,
                            cudaStream_t stream);

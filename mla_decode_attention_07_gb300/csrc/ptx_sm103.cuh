@@ -189,6 +189,14 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y,
+                                            int32_t z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -265,6 +273,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 #undef MLA_W32
+// 32 lanes x 32 consecutive 32-bit columns, waited on in the same statement
+// (no use of the registers can be scheduled before the wait).
+#define MLA_R32(i) "=r"(r[i])
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MLA_R32(0), MLA_R32(1), MLA_R32(2), MLA_R32(3), MLA_R32(4), MLA_R32(5), MLA_R32(6),
+        MLA_R32(7), MLA_R32(8), MLA_R32(9), MLA_R32(10), MLA_R32(11), MLA_R32(12), MLA_R32(13),
+        MLA_R32(14), MLA_R32(15), MLA_R32(16), MLA_R32(17), MLA_R32(18), MLA_R32(19),
+        MLA_R32(20), MLA_R32(21), MLA_R32(22), MLA_R32(23), MLA_R32(24), MLA_R32(25),
+        MLA_R32(26), MLA_R32(27), MLA_R32(28), MLA_R32(29), MLA_R32(30), MLA_R32(31)
+      : "r"(taddr)
+      : "memory");
+}
+#undef MLA_R32
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -296,6 +322,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
+
+// The same for either 16-bit input type: ab_bf16 = 0 for fp16 A and B, 1
+// for bf16 (kind::f16 takes both operands in the same type).
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int b_mn, int ab_bf16) {
+  return (1u << 4) | ((uint32_t)ab_bf16 << 7) | ((uint32_t)ab_bf16 << 10) |
+         ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+static_assert(idesc_f32acc(128, 256, 0, 1, 1) == idesc_bf16_f32(128, 256, 0, 1),
+              "the two descriptor builders agree on bf16");
 
 // ---------------------------------------------------------------- misc
 // 2^x on the special-function unit (flush-to-zero; max relative error 2^-22).
@@ -332,6 +368,11 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

@@ -31,7 +31,12 @@ EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_workspace_size", "mla_decode_plan", "mla_decode_plan_host", "mla_decode",
             "mla_decode_f32", "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc",
             "mla_decode_sparse", "mla_decode_sparse_f32", "mla_selftest_wait_timeout",
-            "mla_check_device_error", "mla_strerror"]
+            "mla_check_device_error", "mla_strerror", "mla_cache_append", "mla_q_absorb",
+            "mla_gemm"]
+
+MLA_DTYPE_F16 = 0
+MLA_DTYPE_BF16 = 1
+MLA_DTYPE_F32 = 2
 
 _lib = None
 
@@ -77,6 +82,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_decode_noalloc.restype = I
     lib.mla_decode_sparse.argtypes = [V, V, I, V, I, V, V, I, V, I, I, V, V, V, F, V, Z, V]
     lib.mla_decode_sparse.restype = I
+    lib.mla_cache_append.argtypes = [V, V, I, V, I, V, I, I, V]
+    lib.mla_cache_append.restype = I
+    lib.mla_q_absorb.argtypes = [V, V, V, V, I, I, I, V]
+    lib.mla_q_absorb.restype = I
+    lib.mla_gemm.argtypes = [V, V, V, I, I, I, I, I, V]
+    lib.mla_gemm.restype = I
     lib.mla_selftest_wait_timeout.argtypes = [V]
     lib.mla_selftest_wait_timeout.restype = I
     lib.mla_check_device_error.argtypes = [V]
@@ -261,6 +272,42 @@ def mla_selftest_wait_timeout(stream=None) -> None:
 
 def mla_check_device_error(stream=None) -> int:
     return int(load().mla_check_device_error(_stream(stream)))
+
+
+def mla_cache_append(kv_new, kv_cache, block_table, cache_seqlens, stream=None) -> None:
+    """kv_new [B, s_q, 576] bf16 rows of the new tokens into kv_cache [pages,
+    64, 1, 576] at positions cache_seqlens[b] - s_q + i (the lengths count
+    the new tokens)."""
+    B, s_q = int(kv_new.shape[0]), int(kv_new.shape[1])
+    rc = load().mla_cache_append(_ptr(kv_new), _ptr(kv_cache), int(kv_cache.shape[0]),
+                                 _ptr(block_table), int(block_table.shape[1]),
+                                 _ptr(cache_seqlens), B, s_q, _stream(stream))
+    _check(rc, "mla_cache_append")
+
+
+def mla_q_absorb(q_nope, q_rope, w_uk, q, stream=None) -> None:
+    """q [B, s_q, h_q, 576] bf16 = [q_nope W_UK per head | q_rope]; q_nope [B,
+    s_q, h_q, 128], q_rope [B, s_q, h_q, 64], w_uk [h_q, 128, 512], all bf16."""
+    B, s_q, h_q = int(q_nope.shape[0]), int(q_nope.shape[1]), int(q_nope.shape[2])
+    rc = load().mla_q_absorb(_ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(q), B, s_q, h_q,
+                             _stream(stream))
+    _check(rc, "mla_q_absorb")
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.float16: MLA_DTYPE_F16, torch.bfloat16: MLA_DTYPE_BF16,
+            torch.float32: MLA_DTYPE_F32}[t.dtype]
+
+
+def mla_gemm(a, b, c, stream=None) -> None:
+    """c [M, N] = a [M, K] @ b [K, N] on the tensor cores (a, b fp16 or bf16
+    of one type; c fp16, bf16 or fp32)."""
+    M, K = int(a.shape[0]), int(a.shape[1])
+    N = int(b.shape[1])
+    rc = load().mla_gemm(_ptr(a), _ptr(b), _ptr(c), M, N, K, _dtype_code(a), _dtype_code(c),
+                         _stream(stream))
+    _check(rc, "mla_gemm")
 
 
 def alloc_plan_and_workspace(batch: int, s_q: int, h_q: int, device: int = 0):

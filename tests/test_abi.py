@@ -78,6 +78,32 @@ def test_sparse_rejects_bad_args_on_host(lib, kw):
     assert _sparse(lib, **kw) == libmla.MLA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("args", [
+    (None, 0x2000, 0x3000, 64, 64, 64), (0x1000, None, 0x3000, 64, 64, 64),
+    (0x1000, 0x2000, None, 64, 64, 64), (0x1000, 0x2000, 0x3000, 0, 64, 64),
+    (0x1000, 0x2000, 0x3000, 64, 60, 64), (0x1000, 0x2000, 0x3000, 64, 64, 12),
+    (0x1008, 0x2000, 0x3000, 64, 64, 64), (0x1000, 0x2000, 0x3004, 64, 64, 64),
+])
+def test_gemm_rejects_bad_args_on_host(lib, args):
+    A, B, C, M, N, K = args
+    assert lib.mla_gemm(A, B, C, M, N, K, 0, 0, None) == libmla.MLA_ERR_INVALID_ARG
+    assert lib.mla_gemm(0x1000, 0x2000, 0x3000, 64, 64, 64, 2, 0, None) == \
+        libmla.MLA_ERR_INVALID_ARG                         # fp32 inputs are not supported
+    assert lib.mla_gemm(0x1000, 0x2000, 0x3000, 64, 64, 64, 0, 3, None) == \
+        libmla.MLA_ERR_INVALID_ARG
+
+
+def test_prologue_rejects_bad_args_on_host(lib):
+    E = libmla.MLA_ERR_INVALID_ARG
+    assert lib.mla_q_absorb(None, 0x2000, 0x3000, 0x4000, 1, 1, 16, None) == E
+    assert lib.mla_q_absorb(0x1000, 0x2008, 0x3000, 0x4000, 1, 1, 16, None) == E
+    assert lib.mla_q_absorb(0x1000, 0x2000, 0x3000, 0x4000, 1, 0, 16, None) == E
+    assert lib.mla_cache_append(0x1000, 0x2000, 4, 0x3000, 4, 0x4000, 0, 1, None) == E
+    assert lib.mla_cache_append(0x1000, 0x2000, 4, 0x3002, 4, 0x4000, 1, 1, None) == E
+    assert lib.mla_cache_append(0x1004, 0x2000, 4, 0x3000, 4, 0x4000, 1, 1, None) == E
+    assert lib.mla_cache_append(0x1000, 0x2000, 0, 0x3000, 4, 0x4000, 1, 1, None) == E
+
+
 def test_plan_rejects_bad_args_on_host(lib):
     assert lib.mla_decode_plan(None, 1, 1, 16, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_plan(0x4000, 1, 1, 0, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
@@ -101,3 +127,7 @@ def test_no_gpu_means_error_not_fallback(lib):
     assert _sparse(lib) in (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
     assert lib.mla_num_clusters(0) < 0
     assert lib.mla_plan_size(1, 1, 16, 0) == 0
+    assert lib.mla_gemm(0x1000, 0x2000, 0x3000, 64, 64, 64, 0, 0, None) in \
+        (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
+    assert lib.mla_cache_append(0x1000, 0x2000, 4, 0x3000, 4, 0x4000, 1, 1, None) in \
+        (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
