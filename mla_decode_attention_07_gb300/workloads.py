@@ -464,3 +464,68 @@ class GemmWorkload:
 
 # The GEMM tutorial's comparison: FP16, 2048 x 2048 x 2048.
 GEMM_WORKLOADS = {"gemm_f16_2048": GemmWorkload("gemm_f16_2048", 2048, 2048, 2048, seed=6)}
+
+
+# ---------------------------------------------------------------------------
+# Dense attention forward (FlashAttention-style), [B, S, H, d] layouts.  The
+# MLA prefill reading: DeepSeek's prefill runs attention in the MHA form,
+# 128 heads with d_qk = 128 + 64 = 192 and d_v = 128, causal, scale 192^-0.5.
+TENSOR_ATT_Q = 0x4151
+TENSOR_ATT_K = 0x414B
+TENSOR_ATT_V = 0x4156
+
+
+@dataclasses.dataclass
+class AttentionInputs:
+    q: np.ndarray        # uint16 [B, S, H, d_qk]
+    k: np.ndarray        # uint16 [B, S, H, d_qk]
+    v: np.ndarray        # uint16 [B, S, H, d_v]
+    causal: bool
+    scale: float
+
+
+def make_attention_inputs(seed: int, batch: int, seqlen: int, heads: int, d_qk: int, d_v: int,
+                          causal: bool = True, scale: float | None = None) -> AttentionInputs:
+    n_qk = batch * seqlen * heads * d_qk
+    q = normal_bf16(seed, TENSOR_ATT_Q, n_qk).reshape(batch, seqlen, heads, d_qk)
+    k = normal_bf16(seed, TENSOR_ATT_K, n_qk).reshape(batch, seqlen, heads, d_qk)
+    v = normal_bf16(seed, TENSOR_ATT_V, batch * seqlen * heads * d_v).reshape(
+        batch, seqlen, heads, d_v)
+    return AttentionInputs(q=q, k=k, v=v, causal=causal,
+                           scale=float(d_qk ** -0.5 if scale is None else scale))
+
+
+@dataclasses.dataclass
+class AttentionWorkload:
+    name: str
+    batch: int
+    seqlen: int
+    heads: int
+    d_qk: int
+    d_v: int
+    causal: bool = True
+    seed: int = 0
+
+    def make(self) -> AttentionInputs:
+        return make_attention_inputs(self.seed, self.batch, self.seqlen, self.heads, self.d_qk,
+                                     self.d_v, self.causal)
+
+    def pairs(self) -> float:
+        """(query, key) pairs attended."""
+        S = self.seqlen
+        per = S * (S + 1) / 2 if self.causal else S * S
+        return float(self.batch * self.heads * per)
+
+    def flops(self) -> float:
+        return 2.0 * (self.d_qk + self.d_v) * self.pairs()
+
+    def bytes(self) -> float:
+        rows = self.batch * self.seqlen * self.heads
+        return float(rows * (2 * self.d_qk * 2 + self.d_v * 2 + self.d_v * 2 + 4))
+
+
+ATTENTION_WORKLOADS = {
+    # DeepSeek MLA prefill in the MHA form: one 4096-token sequence, 128 heads
+    "prefill_b1_h128_s4096_d192": AttentionWorkload("prefill_b1_h128_s4096_d192", 1, 4096, 128,
+                                                    192, 128, True, seed=8),
+}

@@ -12,6 +12,8 @@ the softmax denominator of the scaled logits.  Sparse decode (one query
 token per entry) is the same attention over the cache rows at a listed set of
 token positions.  The header of ``mla_oracle.c`` states both in full.
 
+``attention_oracle.c`` is dense scaled-dot-product attention (causal or
+not) over [B, S, H, d] tensors, the result a FlashAttention kernel computes.
 ``prologue_oracle.c`` writes out the two steps that prepare a decode call
 (the new tokens' rows appended to the paged cache, bit for bit; the query
 absorbed through W_UK, in fp64) and ``gemm_oracle.c`` the plain matrix
@@ -33,6 +35,8 @@ PROLOGUE_SOURCE = os.path.join(_HERE, "prologue_oracle.c")
 _PROLOGUE_LIB = os.path.join(_HERE, "_build", "libprologue_oracle.so")
 GEMM_SOURCE = os.path.join(_HERE, "gemm_oracle.c")
 _GEMM_LIB = os.path.join(_HERE, "_build", "libgemm_oracle.so")
+ATTENTION_SOURCE = os.path.join(_HERE, "attention_oracle.c")
+_ATTENTION_LIB = os.path.join(_HERE, "_build", "libattention_oracle.so")
 
 D_V = 512
 
@@ -58,6 +62,7 @@ def build(force: bool = False) -> str:
     decode oracle's library."""
     _build_one(PROLOGUE_SOURCE, _PROLOGUE_LIB, force)
     _build_one(GEMM_SOURCE, _GEMM_LIB, force)
+    _build_one(ATTENTION_SOURCE, _ATTENTION_LIB, force)
     return _build_one(SOURCE, _LIB, force)
 
 
@@ -254,7 +259,59 @@ class Gemm:
         return out
 
 
+class Attention:
+    """ctypes front end of the dense attention oracle."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        lib.oracle_attention.argtypes = [P, P, P, I, I, I, I, I, I, D, P, P, I]
+        lib.oracle_attention.restype = I
+        lib.oracle_attention_rows.argtypes = [P, P, P, I, I, I, I, I, I, D, I, P, P, P, I]
+        lib.oracle_attention_rows.restype = I
+        self.lib = lib
+
+    @staticmethod
+    def _shapes(ai):
+        B, S, H, dqk = (int(x) for x in ai.q.shape)
+        return B, S, H, dqk, int(ai.v.shape[3])
+
+    def attention(self, ai, nthreads: int | None = None):
+        """Every row: out fp64 [B, S, H, d_v], lse fp64 [B, H, S]."""
+        B, S, H, dqk, dv = self._shapes(ai)
+        _q, qp = _c(ai.q, np.uint16)
+        _k, kp = _c(ai.k, np.uint16)
+        _v, vp = _c(ai.v, np.uint16)
+        out = np.zeros((B, S, H, dv), dtype=np.float64)
+        lse = np.zeros((B, H, S), dtype=np.float64)
+        self.lib.oracle_attention(qp, kp, vp, B, S, H, dqk, dv, int(ai.causal), float(ai.scale),
+                                  out.ctypes.data_as(ctypes.c_void_p),
+                                  lse.ctypes.data_as(ctypes.c_void_p),
+                                  nthreads or default_threads())
+        return out, lse
+
+    def attention_rows(self, ai, rows, nthreads: int | None = None):
+        """Selected rows (array of (b, h, i)): out [n, d_v], lse [n]."""
+        B, S, H, dqk, dv = self._shapes(ai)
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+        _q, qp = _c(ai.q, np.uint16)
+        _k, kp = _c(ai.k, np.uint16)
+        _v, vp = _c(ai.v, np.uint16)
+        out = np.zeros((r.shape[0], dv), dtype=np.float64)
+        lse = np.zeros((r.shape[0],), dtype=np.float64)
+        rc = self.lib.oracle_attention_rows(qp, kp, vp, B, S, H, dqk, dv, int(ai.causal),
+                                            float(ai.scale), int(r.shape[0]),
+                                            r.ctypes.data_as(ctypes.c_void_p),
+                                            out.ctypes.data_as(ctypes.c_void_p),
+                                            lse.ctypes.data_as(ctypes.c_void_p),
+                                            nthreads or default_threads())
+        if rc != 0:
+            raise ValueError("oracle: attention row out of range")
+        return out, lse
+
+
 _default: Oracle | None = None
+_attention: Attention | None = None
 _prologue: Prologue | None = None
 _gemm: Gemm | None = None
 
@@ -301,6 +358,22 @@ def gemm_oracle() -> Gemm:
         build()
         _gemm = Gemm(_GEMM_LIB)
     return _gemm
+
+
+def attention_oracle() -> Attention:
+    global _attention
+    if _attention is None:
+        build()
+        _attention = Attention(_ATTENTION_LIB)
+    return _attention
+
+
+def attention(ai, nthreads=None):
+    return attention_oracle().attention(ai, nthreads)
+
+
+def attention_rows(ai, rows, nthreads=None):
+    return attention_oracle().attention_rows(ai, rows, nthreads)
 
 
 def cache_append(kv_new, kv_cache, block_table, cache_seqlens):

@@ -1,8 +1,9 @@
-"""The cache-append / query-absorption oracle and the GEMM oracle against
-their pins, and planted mistakes in copies of each that the pins must catch.
-Every mutant keeps its reads in bounds."""
+"""The cache-append / query-absorption, GEMM and dense-attention oracles
+against their pins, and planted mistakes in copies of each that the pins
+must catch.  Every mutant keeps its reads in bounds."""
 import pytest
 
+import attention_pins
 import gemm_pins
 import prologue_pins
 
@@ -15,6 +16,25 @@ def test_prologue_pin(check, oracle_mod):
 @pytest.mark.parametrize("check", gemm_pins.ALL_CHECKS, ids=lambda c: c.__name__)
 def test_gemm_pin(check, oracle_mod):
     check(oracle_mod.gemm_oracle())
+
+
+@pytest.mark.parametrize("check", attention_pins.ALL_CHECKS, ids=lambda c: c.__name__)
+def test_attention_pin(check, oracle_mod):
+    check(oracle_mod.attention_oracle())
+
+
+ATTENTION_MUTANTS = {
+    "causal_off_by_one": ("const int n = J->causal ? i + 1 : J->S;",
+                          "const int n = J->causal ? (i > 0 ? i : 1) : J->S;"),
+    "no_scale": ("s[t] = J->scale * dot;", "s[t] = dot;"),
+    "lse_log2": ("const double lse = m + log(sum);", "const double lse = m + log2(sum);"),
+    "value_from_key_row": ("const uint16_t* v = J->v + (((size_t)b * J->S + t) * J->H + h) * J->dv;",
+                           "const uint16_t* v = J->v + (((size_t)b * J->S + 0) * J->H + h) * J->dv;"),
+    "head_seq_swapped": ("const uint16_t* q = J->q + (((size_t)b * J->S + i) * J->H + h) * J->dqk;",
+                         "const uint16_t* q = J->q + (((size_t)b * J->S + (i % J->S)) * J->H + (h + i) % J->H) * J->dqk;"),
+    "short_dot": ("for (int d = 0; d < J->dqk; ++d)", "for (int d = 0; d < J->dqk - 1; ++d)"),
+    "weights_not_normalised": ("const double w = exp(s[t] - lse);", "const double w = exp(s[t] - m);"),
+}
 
 
 PROLOGUE_MUTANTS = {
@@ -72,3 +92,10 @@ def test_gemm_mutant_is_caught(name, tmp_path, oracle_mod):
     old, new = GEMM_MUTANTS[name]
     assert _caught(oracle_mod, oracle_mod.GEMM_SOURCE, old, new, tmp_path, name,
                    oracle_mod.Gemm, gemm_pins.ALL_CHECKS), f"no pin rejects {name}"
+
+
+@pytest.mark.parametrize("name", sorted(ATTENTION_MUTANTS))
+def test_attention_mutant_is_caught(name, tmp_path, oracle_mod):
+    old, new = ATTENTION_MUTANTS[name]
+    assert _caught(oracle_mod, oracle_mod.ATTENTION_SOURCE, old, new, tmp_path, name,
+                   oracle_mod.Attention, attention_pins.ALL_CHECKS), f"no pin rejects {name}"
