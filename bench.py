@@ -59,7 +59,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(W.WORKLOADS) + sorted(W.SPARSE_WORKLOADS) +
-                    sorted(W.GEMM_WORKLOADS) + sorted(W.PROLOGUE_WORKLOADS))
+                    sorted(W.GEMM_WORKLOADS) + sorted(W.PROLOGUE_WORKLOADS) +
+                    sorted(W.ATTENTION_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the oracle baseline leg")
@@ -998,8 +999,119 @@ def run_prologue(args):
         torch.distributed.destroy_process_group()
 
 
+ATTENTION_METRIC = "Dense attention forward TFLOP/s and % of GB300 dense-bf16 tensor peak (1 GPU)"
+
+
+def run_attention(args):
+    """mla_attention_fwd per step (MLA prefill in the MHA form); torch's
+    scaled_dot_product_attention timed on the same tensors beside it."""
+    torch, world, rank, dev = _single_gpu_setup()
+    from mla_decode_attention_07_gb300 import libmla
+    libmla.load()
+    w = W.ATTENTION_WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    ai = w.make()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16))).to(dev).view(
+        torch.bfloat16)
+    q, k, v = t(ai.q), t(ai.k), t(ai.v)
+    out = torch.empty((w.batch, w.seqlen, w.heads, w.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.batch, w.heads, w.seqlen), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def ours(i):
+        libmla.mla_attention_fwd(q, k, v, out, lse, w.causal, ai.scale, stream)
+
+    for i in range(max(3, args.warmup)):
+        ours(i)
+    torch.cuda.synchronize()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error during warm-up: {libmla.mla_strerror(rc)}")
+    sampler = ClockSampler(physical_gpu_index(dev.index))
+    sampler.start()
+    t_end = time.perf_counter() + 1.0
+    i = 0
+    while time.perf_counter() < t_end:
+        ours(i)
+        i += 1
+        torch.cuda.synchronize()
+    K = args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    ms = aggregate_max(_timed_loop(torch, stream, ours, K), world)
+    clocks = sampler.stop()
+    rc = libmla.mla_check_device_error(stream)
+    if rc != 0:
+        raise RuntimeError(f"device error in timed region: {libmla.mla_strerror(rc)}")
+    tf = w.flops() / (ms * 1e-3) / 1e12
+    sdpa = None
+    try:
+        import torch.nn.functional as F
+        qt, kt, vt = q.transpose(1, 2), k.transpose(1, 2), v.transpose(1, 2)
+
+        def theirs(i):
+            F.scaled_dot_product_attention(qt, kt, vt, is_causal=w.causal, scale=ai.scale)
+
+        for i in range(3):
+            theirs(i)
+        ms_t = _timed_loop(torch, stream, theirs, max(3, K // 2))
+        sdpa = {"value": round(w.flops() / (ms_t * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(ms_t, 4), "ratio": round(ms_t / ms, 4),
+                "how": "torch.nn.functional.scaled_dot_product_attention on the same tensors "
+                       "(its own backend choice)"}
+    except Exception as ex:   # backend without this head-dim combination
+        sdpa = {"unavailable": f"{type(ex).__name__}: {str(ex)[:160]}"}
+    result = {
+        "metric": ATTENTION_METRIC, "value": round(tf * world, 3), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) rounded to bf16)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "heads": w.heads,
+                   "d_qk": w.d_qk, "d_v": w.d_v, "causal": w.causal,
+                   "l2": f"inputs {w.bytes() / 1e6:.0f} MB per call (> L2)",
+                   "parallelism": "single GPU" if world == 1 else f"{world} replicas"},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "traffic": None, "kernel": "mla_attention_kernel",
+                     "flops_per_call": w.flops(), "peak_source": f"{peak_src}: bf16 burst"},
+        "sdpa": sdpa,
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        rng = np.random.default_rng(0)
+        n = 64
+        while True:   # grow the row sample until the oracle works for a few seconds
+            rows = np.stack([rng.integers(0, w.batch, n), rng.integers(0, w.heads, n),
+                             rng.integers(0, w.seqlen, n)], 1).astype(np.int32)
+            t0 = time.perf_counter()
+            oracle.attention_rows(ai, rows)
+            dt = time.perf_counter() - t0
+            if dt >= min(5.0, args.cpu_seconds) or n >= 1 << 16:
+                break
+            n *= 4
+        keys = sum(int(r[2]) + 1 if w.causal else w.seqlen for r in rows)
+        result["cpu_baseline"] = {"value": 2.0 * (w.d_qk + w.d_v) * keys / dt / 1e12,
+                                  "unit": "TFLOP/s", "cores": oracle.default_threads(),
+                                  "kind": "oracle",
+                                  "sample": f"{n} sampled query rows, fp64 C oracle, {dt:.2f} s"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.workload in W.ATTENTION_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm is timed on the decode workloads; this line "
+                              "carries its own cpu_baseline and SDPA comparison"}), flush=True)
+        else:
+            run_attention(args)
+        return
     if args.workload in W.GEMM_WORKLOADS or args.workload in W.PROLOGUE_WORKLOADS:
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable":

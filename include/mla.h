@@ -278,6 +278,30 @@ int mla_q_absorb(const void* q_nope, const void* q_rope, const void* w_uk, void*
 int mla_gemm(const void* A, const void* B, void* C, int M, int N, int K, int in_dtype,
              int out_dtype, void* stream);
 
+/* Dense attention forward (FlashAttention style):
+ *   for batch b, head h, query i < seqlen, keys t < seqlen (t <= i if causal):
+ *     s_t = softmax_scale * q[b][i][h][0:d_qk] . k[b][t][h][0:d_qk]
+ *     out[b][i][h][0:d_v] = sum_t softmax(s)_t v[b][t][h][0:d_v]   (bf16)
+ *     lse[b][h][i] = ln sum_t exp(s_t)                             (fp32)
+ *   q, k bf16 [batch, seqlen, heads, d_qk]; v bf16 [batch, seqlen, heads,
+ *   d_v]; out bf16 [batch, seqlen, heads, d_v]; all device, 16-byte aligned;
+ *   lse fp32 [batch, heads, seqlen], 4-byte aligned.
+ * Supported: d_qk in {64, 128, 192}, d_v = 128, softmax_scale > 0.  MLA
+ * prefill in DeepSeek's MHA form is d_qk = 192 (128 + 64 rotary), d_v = 128,
+ * causal, 128 heads.  bf16 inputs, fp32 accumulation on the tensor cores,
+ * probabilities enter P.V as bf16; out is normalised by their sum.
+ * Defined by: the TileLang talk, performance section (MLA, FlashAttention
+ * and block-sparse kernels on par with CUTLASS), and the GEMM tutorial
+ * summary, key capabilities (FlashAttention; GEMM + softmax fused so the
+ * scores stay out of HBM); neither prints the formula, which is the plain
+ * definition above.
+ * Errors: MLA_ERR_INVALID_ARG before anything is enqueued,
+ * MLA_ERR_UNSUPPORTED_DEVICE, MLA_ERR_CUDA; a bounded device wait that ran
+ * out is reported by mla_check_device_error. */
+int mla_attention_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      int batch, int seqlen, int heads, int d_qk, int d_v, int causal,
+                      float softmax_scale, void* stream);
+
 /* Failure-path self-test: enqueues a two-CTA kernel whose only wait, on a
  * barrier nothing completes, runs through the same bounded wait as the
  * decode kernel.  After about 2 s it gives up, records

@@ -1,0 +1,421 @@
+// Dense attention forward (FlashAttention style) for sm_103a (GB300).
+//
+// What it computes: for batch entry b, head h and query i < S, scaled-dot-
+// product attention over keys t < S (t <= i when causal):
+//   s_t = scale * q[b][i][h] . k[b][t][h]          (d_qk dims)
+//   out[b][i][h] = sum_t softmax(s)_t v[b][t][h]  (d_v dims, bf16)
+//   lse[b][h][i] = ln sum_t exp(s_t)               (fp32)
+// The pages name FlashAttention without a formula: the TileLang talk
+// ("Tile级原语与自动推理机制融合，TileAI社区发起人深度剖析TileLang核心技术与优势",
+// performance section: MLA, FlashAttention and block-sparse kernels on par
+// with CUTLASS) and the GEMM tutorial summary ("Designing high-performance
+// GPU kernels with TileLang: Tensor-Core GEMM", key capabilities: fused GEMM
+// + softmax that keeps the scores out of HBM).  DeepSeek's MLA prefill runs
+// this form with 128 heads, d_qk = 192 (128 + 64 rotary) and d_v = 128.
+//
+// GB300 design:
+//  * One CTA per (128-query tile, head, batch entry); a causal grid starts
+//    the longest tiles first.  Warp 0 issues TMA loads (Q once, then K and V
+//    tiles of 128 keys through two-deep rings of their own), warp 1 owns
+//    TMEM and issues the MMAs, warps 4-7 run the softmax and the epilogue
+//    with one query row per thread (warp w reaches TMEM lanes 32 (w % 4) ..).
+//  * S = Q K^T (M=128, N=128, K=d_qk, both operands K-major from shared
+//    memory) lands in one of two 128-column TMEM tiles.  The softmax writes
+//    P as bf16 over the first 64 columns of the same tile, and P.V reads P
+//    from TMEM as its A operand (M=128, N=d_v, K=128) with V as the MN-major
+//    B operand: P never goes through shared memory, O (d_v fp32 columns)
+//    stays in TMEM until the epilogue.
+//  * The MMAs are issued in the order S(j), P.V(j-1): the score MMA of the
+//    next tile runs on the tensor pipe while this tile's softmax computes.
+//  * Online softmax in the log2 domain with a lazy rescale: O and the sums
+//    are rescaled only when a row max grows by more than 2^8, and the final
+//    1/l and lse use the same reference max, so the result is exact.  out is
+//    normalised by the sum of the bf16 probabilities P.V multiplies; lse
+//    comes from the fp32 sum.
+//  * Every wait is bounded (2 s on %globaltimer): on expiry the kernel
+//    records MLA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land,
+//    frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "mla.h"
+#include "mla_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kAttThreads = 256;
+constexpr int kSoftWarp0 = 4;                 // warps 4-7: softmax and epilogue
+constexpr int kTQ = 128, kTK = 128;           // query rows and keys per tile
+constexpr int kAttDv = 128;
+constexpr int kMaxDqkBoxes = 3;               // d_qk <= 192
+constexpr uint32_t kBox = 16384;              // 128 rows x 64 bf16, 128-byte swizzle
+constexpr uint32_t kSQ = 0;
+constexpr uint32_t kSK = kSQ + kMaxDqkBoxes * kBox;             // 2 stages x 3 boxes
+constexpr uint32_t kSV = kSK + 2 * kMaxDqkBoxes * kBox;         // 2 stages x 2 boxes
+constexpr uint32_t kABar = kSV + 2 * 2 * kBox;
+enum ABar : int {
+  A_QFULL = 0,
+  A_KFULL = 1,     // [2]
+  A_KEMPTY = 3,    // [2]
+  A_VFULL = 5,     // [2]
+  A_VEMPTY = 7,    // [2]
+  A_SFULL = 9,     // [2] score tile ready (MMA commit)
+  A_PFULL = 11,    // [2] P written over the tile, O rescaled if needed (4 softmax warps)
+  A_ODONE = 13,    // one phase per P.V MMA group
+  A_COUNT = 14
+};
+constexpr uint32_t kAMisc = kABar + 8 * 16;
+constexpr uint32_t kASmem = kAMisc + 16 + 1024;
+constexpr uint32_t kColS = 0, kColO = 256, kATmemCols = 512;
+constexpr float kARescale = 8.0f;
+constexpr float kALn2 = 0.69314718055994530942f;
+constexpr uint64_t kAWaitNs = 2000000000ull;
+constexpr uint64_t kADrainNs = 2000000ull;
+static_assert(kASmem <= 232448, "shared memory");
+
+struct AttArgs {
+  void* out;       // bf16 [B, S, H, d_v]
+  float* lse;      // fp32 [B, H, S]
+  int B, S, H, dqk, causal, n_qt;
+  float scale_log2;
+  int* err;
+};
+
+struct ACtx {
+  uint32_t sbase, abort_addr;
+  int* err;
+  __device__ __forceinline__ uint32_t bar(int i) const { return sbase + kABar + 8u * i; }
+};
+
+__device__ __forceinline__ bool await_(const ACtx& x, uint32_t bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
+      if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) return false;
+      if (ptx::globaltimer() - t0 > kAWaitNs) {
+        atomicCAS(x.err, 0, MLA_ERR_DEVICE_TIMEOUT);
+        ptx::st_shared_u32(x.abort_addr, 1u);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool await_warp(const ACtx& x, uint32_t bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, await_(x, bar, parity));
+}
+
+__global__ void __launch_bounds__(kAttThreads, 1)
+    mla_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const AttArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ACtx x;
+  x.sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
+  x.abort_addr = x.sbase + kAMisc + 4;
+  x.err = args.err;
+  const uint32_t tslot = x.sbase + kAMisc;
+
+  // Work item: the heaviest (last) query tiles of every (b, h) first.
+  const int bh_n = args.B * args.H;
+  const int rank = (int)blockIdx.x / bh_n, bh = (int)blockIdx.x % bh_n;
+  const int qt = args.causal ? args.n_qt - 1 - rank : rank;
+  const int b = bh / args.H, h = bh % args.H;
+  const int n_kt = args.causal ? qt + 1 : (args.S + kTK - 1) / kTK;
+  const int nbq = args.dqk / 64;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(x.bar(A_QFULL), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(x.bar(A_KFULL + s), 1);
+      ptx::mbar_init(x.bar(A_KEMPTY + s), 1);
+      ptx::mbar_init(x.bar(A_VFULL + s), 1);
+      ptx::mbar_init(x.bar(A_VEMPTY + s), 1);
+      ptx::mbar_init(x.bar(A_SFULL + s), 1);
+      ptx::mbar_init(x.bar(A_PFULL + s), 4);
+    }
+    ptx::mbar_init(x.bar(A_ODONE), 1);
+    ptx::st_shared_u32(x.abort_addr, 0u);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tslot, kATmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ptx::ld_shared_u32_volatile(tslot);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(x.bar(A_QFULL), nbq * kBox);
+      for (int c = 0; c < nbq; ++c)
+        ptx::tma_load_4d(x.sbase + kSQ + c * kBox, &tm_q, 64 * c, h, qt * kTQ, b, x.bar(A_QFULL));
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = ((uint32_t)j >> 1) & 1u;
+        if (!await_(x, x.bar(A_KEMPTY + s), ph ^ 1u)) break;
+        ptx::mbar_arrive_expect_tx(x.bar(A_KFULL + s), nbq * kBox);
+        for (int c = 0; c < nbq; ++c)
+          ptx::tma_load_4d(x.sbase + kSK + (s * kMaxDqkBoxes + c) * kBox, &tm_k, 64 * c, h, j * kTK,
+                           b, x.bar(A_KFULL + s));
+        if (!await_(x, x.bar(A_VEMPTY + s), ph ^ 1u)) break;
+        ptx::mbar_arrive_expect_tx(x.bar(A_VFULL + s), 2 * kBox);
+        for (int c = 0; c < 2; ++c)
+          ptx::tma_load_4d(x.sbase + kSV + (s * 2 + c) * kBox, &tm_v, 64 * c, h, j * kTK, b,
+                           x.bar(A_VFULL + s));
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // S(j) = Q K(j)^T, then P(j-1).V(j-1).
+    constexpr uint32_t id_s = ptx::idesc_f32acc(kTQ, kTK, 0, 0, 1);
+    constexpr uint32_t id_o = ptx::idesc_f32acc(kTQ, kAttDv, 0, 1, 1);
+    auto issue_pv = [&](int jj) -> bool {
+      const int s = jj & 1;
+      const uint32_t ph = ((uint32_t)jj >> 1) & 1u;
+      if (!await_warp(x, x.bar(A_PFULL + s), ph)) return false;
+      if (!await_warp(x, x.bar(A_VFULL + s), ph)) return false;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kTK / 16; ++k) {
+        // V tile: 64-dim boxes 16 KB apart along N, 8-key groups 1 KB apart
+        const uint64_t bd = ptx::smem_desc(x.sbase + kSV + s * 2 * kBox + k * 2048, kBox, 1024,
+                                           ptx::kLayoutSw128);
+        ptx::mma_ts_elect(tmem + kColO, tmem + kColS + 128u * s + 8u * k, bd, id_o,
+                          (jj > 0 || k > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit_elect(x.bar(A_VEMPTY + s));
+      ptx::mma_commit_elect(x.bar(A_ODONE));
+      return true;
+    };
+    bool ok = await_warp(x, x.bar(A_QFULL), 0u);
+    for (int j = 0; ok && j < n_kt; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = ((uint32_t)j >> 1) & 1u;
+      if (!await_warp(x, x.bar(A_KFULL + s), ph)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      for (int k = 0; k < nbq * 4; ++k) {
+        const uint32_t off = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
+        const uint64_t ad = ptx::smem_desc(x.sbase + kSQ + off, 16, 1024, ptx::kLayoutSw128);
+        const uint64_t bd = ptx::smem_desc(x.sbase + kSK + s * kMaxDqkBoxes * kBox + off, 16, 1024,
+                                           ptx::kLayoutSw128);
+        ptx::mma_ss_elect(tmem + kColS + 128u * s, ad, bd, id_s, k ? 1u : 0u);
+      }
+      ptx::mma_commit_elect(x.bar(A_SFULL + s));
+      ptx::mma_commit_elect(x.bar(A_KEMPTY + s));
+      if (j >= 1) ok = issue_pv(j - 1);
+    }
+    if (ok) issue_pv(n_kt - 1);
+    __syncwarp();
+  } else if (warp >= kSoftWarp0) {
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int qi = qt * kTQ + r;
+    const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+    const float sl2 = args.scale_log2;
+    float m_ref = -INFINITY, l_f = 0.f, l_b = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int s = j & 1;
+      if (!await_warp(x, x.bar(A_SFULL + s), ((uint32_t)j >> 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      float sv[kTK];
+#pragma unroll
+      for (int c = 0; c < kTK / 32; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32_wait(tmem + lanes + kColS + 128u * s + 32u * c, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) sv[32 * c + k] = __uint_as_float(v[k]);
+      }
+      // keys past the sequence, or after the query when causal, get no weight
+      const int k0 = j * kTK;
+      const int lim = args.causal ? min(qi + 1, args.S) : args.S;
+      if (__any_sync(0xffffffffu, k0 + kTK > lim)) {
+#pragma unroll
+        for (int k = 0; k < kTK; ++k)
+          if (k0 + k >= lim) sv[k] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kTK; k += 4)
+        mx = fmaxf(mx, ptx::max3(sv[k], sv[k + 1], fmaxf(sv[k + 2], sv[k + 3])));
+      const float m_cand = fmaxf(m_ref, mx * sl2);
+      const bool rescale = (j > 0) && (m_cand > m_ref + kARescale);
+      float alpha = 1.0f;
+      if (j == 0) {
+        m_ref = m_cand;
+      } else if (rescale) {
+        alpha = ptx::ex2(m_ref - m_cand);
+        m_ref = m_cand;
+        l_f *= alpha;
+        l_b *= alpha;
+      }
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      uint32_t pk[kTK / 2];
+      float sf0 = 0.f, sf1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < kTK / 2; ++k) {
+        const float a = ptx::ex2(fmaf(sv[2 * k], sl2, neg_m));
+        const float c = ptx::ex2(fmaf(sv[2 * k + 1], sl2, neg_m));
+        sf0 += a;
+        sf1 += c;
+        pk[k] = ptx::pack_bf16x2(a, c);
+        sb0 += __uint_as_float(pk[k] << 16);
+        sb1 += __uint_as_float(pk[k] & 0xffff0000u);
+      }
+      l_f += sf0 + sf1;
+      l_b += sb0 + sb1;
+      // P (bf16 pairs) over the first 64 columns of the score tile
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = pk[32 * c + k];
+        ptx::tmem_st32(tmem + lanes + kColS + 128u * s + 32u * c, w);
+      }
+      ptx::tmem_wait_st();
+      // O must not be rescaled before the previous P.V has landed
+      if (j > 0 && !await_warp(x, x.bar(A_ODONE), ((uint32_t)(j - 1)) & 1u)) {
+        ok = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kAttDv / 32; ++c) {
+          uint32_t o[32];
+          ptx::tmem_ld32_wait(tmem + lanes + kColO + 32u * c, o);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          ptx::tmem_st32(tmem + lanes + kColO + 32u * c, o);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(A_PFULL + s));
+    }
+    // Epilogue: O / l and lse once the last P.V has landed.
+    if (ok && await_warp(x, x.bar(A_ODONE), ((uint32_t)(n_kt - 1)) & 1u)) {
+      ptx::tc_fence_after();
+      const float inv_l = l_b > 0.f ? 1.0f / l_b : 0.f;
+      const bool valid = qi < args.S;
+      uint16_t* orow = static_cast<uint16_t*>(args.out) +
+                       (((int64_t)b * args.S + (valid ? qi : 0)) * args.H + h) * kAttDv;
+#pragma unroll 1
+      for (int c = 0; c < kAttDv / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32_wait(tmem + lanes + kColO + 32u * c, o);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            dst[q4] = make_uint4(
+                ptx::pack_bf16x2(__uint_as_float(o[8 * q4]) * inv_l, __uint_as_float(o[8 * q4 + 1]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv_l, __uint_as_float(o[8 * q4 + 3]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv_l, __uint_as_float(o[8 * q4 + 5]) * inv_l),
+                ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv_l, __uint_as_float(o[8 * q4 + 7]) * inv_l));
+        }
+      }
+      if (valid)
+        args.lse[((int64_t)b * args.H + h) * args.S + qi] =
+            l_f > 0.f ? (m_ref + log2f(l_f)) * kALn2 : -INFINITY;
+    }
+  }
+
+  __syncthreads();
+  if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < kADrainNs) __nanosleep(1000);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kATmemCols);
+  }
+}
+
+std::once_flag g_att_once[64];
+cudaError_t g_att_status[64];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_attention_fwd(const void* q, const void* k, const void* v, void* out,
+                                 float* lse, int batch, int seqlen, int heads, int d_qk, int d_v,
+                                 int causal, float softmax_scale, void* stream) {
+  if (!q || !k || !v || !out || !lse || batch < 1 || seqlen < 1 || heads < 1 ||
+      (d_qk != 64 && d_qk != 128 && d_qk != 192) || d_v != kAttDv || !(softmax_scale > 0.f) ||
+      !isfinite(softmax_scale) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  const long long n_qt = (seqlen + kTQ - 1) / kTQ;
+  const long long grid = n_qt * batch * heads;
+  if (grid >= (1ll << 31) || (long long)batch * seqlen * heads * d_qk >= (1ll << 40))
+    return MLA_ERR_INVALID_ARG;
+  int device = 0, sms = 0;
+  int* err = nullptr;
+  const int st = device_current(&device, &sms, &err);
+  if (st != MLA_OK) return st;
+  if (device < 0 || device >= 64) return MLA_ERR_INVALID_ARG;
+  std::call_once(g_att_once[device], [&]() {
+    g_att_status[device] = cudaFuncSetAttribute(
+        mla_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem);
+  });
+  if (g_att_status[device] != cudaSuccess) return MLA_ERR_CUDA;
+  CUtensorMap mq, mk, mv;
+  const uint64_t dqk4[4] = {(uint64_t)d_qk, (uint64_t)heads, (uint64_t)seqlen, (uint64_t)batch};
+  const uint64_t sqk[3] = {(uint64_t)d_qk * 2, (uint64_t)heads * d_qk * 2,
+                           (uint64_t)seqlen * heads * d_qk * 2};
+  const uint64_t dv4[4] = {(uint64_t)d_v, (uint64_t)heads, (uint64_t)seqlen, (uint64_t)batch};
+  const uint64_t sv[3] = {(uint64_t)d_v * 2, (uint64_t)heads * d_v * 2,
+                          (uint64_t)seqlen * heads * d_v * 2};
+  const uint32_t box[4] = {64, 1, kTQ, 1};
+  if (!encode_tiled_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, q, dqk4, sqk, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, k, dqk4, sqk, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, v, dv4, sv, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+    return MLA_ERR_CUDA;
+  AttArgs a;
+  a.out = out;
+  a.lse = lse;
+  a.B = batch;
+  a.S = seqlen;
+  a.H = heads;
+  a.dqk = d_qk;
+  a.causal = causal ? 1 : 0;
+  a.n_qt = (int)n_qt;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.err = err;
+  mla_attention_kernel<<<(unsigned)grid, kAttThreads, kASmem, static_cast<cudaStream_t>(stream)>>>(
+      mq, mk, mv, a);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}

@@ -32,7 +32,7 @@ EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_decode_f32", "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc",
             "mla_decode_sparse", "mla_decode_sparse_f32", "mla_selftest_wait_timeout",
             "mla_check_device_error", "mla_strerror", "mla_cache_append", "mla_q_absorb",
-            "mla_gemm"]
+            "mla_gemm", "mla_attention_fwd"]
 
 MLA_DTYPE_F16 = 0
 MLA_DTYPE_BF16 = 1
@@ -88,6 +88,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.mla_q_absorb.restype = I
     lib.mla_gemm.argtypes = [V, V, V, I, I, I, I, I, V]
     lib.mla_gemm.restype = I
+    lib.mla_attention_fwd.argtypes = [V, V, V, V, V, I, I, I, I, I, I, F, V]
+    lib.mla_attention_fwd.restype = I
     lib.mla_selftest_wait_timeout.argtypes = [V]
     lib.mla_selftest_wait_timeout.restype = I
     lib.mla_check_device_error.argtypes = [V]
@@ -308,6 +310,17 @@ def mla_gemm(a, b, c, stream=None) -> None:
     rc = load().mla_gemm(_ptr(a), _ptr(b), _ptr(c), M, N, K, _dtype_code(a), _dtype_code(c),
                          _stream(stream))
     _check(rc, "mla_gemm")
+
+
+def mla_attention_fwd(q, k, v, out, lse, causal: bool, softmax_scale: float,
+                      stream=None) -> None:
+    """Dense attention forward: q, k [B, S, H, d_qk], v [B, S, H, d_v], out
+    [B, S, H, d_v] (bf16), lse [B, H, S] fp32."""
+    B, S, H, dqk = (int(x) for x in q.shape)
+    dv = int(v.shape[3])
+    rc = load().mla_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, dqk,
+                                  dv, 1 if causal else 0, float(softmax_scale), _stream(stream))
+    _check(rc, "mla_attention_fwd")
 
 
 def alloc_plan_and_workspace(batch: int, s_q: int, h_q: int, device: int = 0):

@@ -104,6 +104,21 @@ def test_prologue_rejects_bad_args_on_host(lib):
     assert lib.mla_cache_append(0x1000, 0x2000, 0, 0x3000, 4, 0x4000, 1, 1, None) == E
 
 
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(lse=None), dict(batch=0), dict(seqlen=0), dict(heads=0), dict(dqk=96),
+    dict(dqk=256), dict(dv=64), dict(scale=0.0), dict(scale=float("nan")), dict(out=0x4008),
+    dict(lse=0x5002),
+])
+def test_attention_rejects_bad_args_on_host(lib, kw):
+    a = dict(q=0x1000, k=0x2000, v=0x3000, out=0x4000, lse=0x5000, batch=1, seqlen=128,
+             heads=2, dqk=128, dv=128, causal=1, scale=0.08)
+    a.update(kw)
+    rc = lib.mla_attention_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["batch"],
+                               a["seqlen"], a["heads"], a["dqk"], a["dv"], a["causal"],
+                               ctypes.c_float(a["scale"]), None)
+    assert rc == libmla.MLA_ERR_INVALID_ARG
+
+
 def test_plan_rejects_bad_args_on_host(lib):
     assert lib.mla_decode_plan(None, 1, 1, 16, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
     assert lib.mla_decode_plan(0x4000, 1, 1, 0, 0x5000, 4096, None) == libmla.MLA_ERR_INVALID_ARG
