@@ -130,7 +130,9 @@ int mla_decode_plan_host(const int32_t* cache_seqlens_host, int batch, int s_q, 
  * TMA page streaming, tcgen05 MMAs with TMEM accumulators, online softmax)
  * and the LSE-combine kernel on `stream`.  tile_meta must come from
  * mla_decode_plan (or the host variant, copied to the device) for the same
- * batch, s_q, h_q and sequence lengths.  workspace: device scratch of at
+ * batch, s_q, h_q and sequence lengths, in a buffer of at least
+ * mla_plan_size(batch, s_q, h_q, device) bytes (the kernel reads its cluster
+ * entry at the position this shape gives before it checks the header).  workspace: device scratch of at
  * least mla_workspace_size bytes, 256-byte aligned; its contents on entry do
  * not matter.  softmax_scale multiplies q.k before the softmax.  out is
  * bf16, the fp32 result rounded to nearest even.

@@ -124,7 +124,8 @@ constexpr uint32_t kAlpha = kP + kPBufs * kPBytes;   // float[kPBufs][owner rank
 constexpr uint32_t kInvL = kAlpha + kPBufs * kAlphaBufBytes;   // float[2 parities][owner rank][64] 1/l
 constexpr uint32_t kHand = kInvL + 2 * 128 * 4;   // float[2 sets][4 quadrants][16] running max
 constexpr uint32_t kSums = kHand + 2 * 4 * 16 * 4;  // float[2 parities][4][32 lanes][3] set 1's sums
-constexpr uint32_t kBar = kSums + 2 * 4 * 32 * 12;
+constexpr uint32_t kEpiInv = kSums + 2 * 4 * 32 * 12;   // float[128]: 1/l of each tile row, for set 1
+constexpr uint32_t kBar = kEpiInv + 128 * 4;
 constexpr uint32_t kMisc = kBar + 8 * 48;
 constexpr uint32_t kSmemAlloc = kMisc + 64 + 1024;  // + slack for 1024-byte alignment
 static_assert(kP % 1024 == 0 && kStage0 % 1024 == 0, "swizzled buffers need 1 KB alignment");
@@ -151,7 +152,7 @@ enum Bar : uint32_t {
   B_PFULL = B_SEMPTY + 2,     // [2] all 128 rows of P in shared memory and O rescaled (4 workers x 2)
   B_PEMPTY = B_PFULL + 2,     // [2] P.V done (MMA commit)
   B_OFULL = B_PEMPTY + 2,
-  B_OEMPTY,                   // set 0's 4 warps have drained O
+  B_OEMPTY,                   // both sets' 8 warps have drained their columns of O
   B_RFULL,                    // [2] the peer's partial scores for my rows (st.async tx)
   B_REMPTY = B_RFULL + 2,     // [2] the peer's workers have read what I sent (4 remote arrives)
   B_PRECV = B_REMPTY + 2,     // [2] the peer's P rows and rescale factors arrived (bulk-copy tx)
@@ -161,6 +162,7 @@ enum Bar : uint32_t {
   B_SUMS = B_HAND + 8,        // [2] set 1's sums of a tile handed to set 0 (per tile parity)
   B_SUMSFREE = B_SUMS + 2,    // [2] set 0 has read them
   B_TEARDOWN = B_SUMSFREE + 2,
+  B_EPI,                      // set 0 has published 1/l of the tile's rows (4 warps)
   B_COUNT,
 };
 static_assert(B_COUNT <= 48, "barrier space");
@@ -263,11 +265,18 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
   int b, pb, pe;
   uint32_t g = 0, n_item = 0;
   const int32_t xq_lat = 256 * (int32_t)x.rank, xq_rope = 512 + 32 * (int32_t)x.rank;
+  // The first page's block-table entry is read alongside the first batch
+  // item (SegIter), not after it: the cluster's first segment starts at
+  // (b0, p0).
+  const int first_page = ((unsigned)w.b0 < (unsigned)prm.batch && (unsigned)w.p0 < (unsigned)prm.max_pages)
+                             ? prm.block_table[(size_t)w.b0 * prm.max_pages + w.p0]
+                             : -1;
   while (it.next(b, pb, pe)) {
     // Entries past max_pages are never read: a sequence longer than its
     // block-table row is reported and served from page 0.
     const int32_t* bt = prm.block_table + (size_t)b * prm.max_pages;
-    int next_page = pb < prm.max_pages ? bt[pb] : -1;
+    int next_page = (g == 0 && b == w.b0 && pb == w.p0) ? first_page
+                                                       : (pb < prm.max_pages ? bt[pb] : -1);
     if (!wait_bar(x, x.bar(B_QEMPTY), (n_item & 1u) ^ 1u)) return false;
     ptx::mbar_arrive_expect_tx(x.bar(B_QFULL), kQRopeTx);
     const int32_t row0 = b * w.rows + w.tile * kTileRows;
@@ -856,15 +865,79 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
     // End of the tile.
     const uint32_t par = n_item & 1u;
     const uint32_t sums = x.sbase + kSums + ((par * 4 + (uint32_t)quad) * 32 + (uint32_t)lane) * 12u;
+    const int ns = w.items[b * kItemWords + 1];
+    const bool direct = (ns == 1);
+    const int sidx = (n_item == 0) ? w.split0 : 0;
+    const int64_t slot = (int64_t)w.tile * w.stotal + w.items[b * kItemWords + 2] + sidx;
+    // rows of the epilogue: lane -> tile row quad * 32 + lane (mine when its
+    // half quadrant is this CTA's, and then this thread owned it)
+    const int re = quad * 32 + lane;
+    const int qe = w.tile * kTileRows + re;
+    const bool valid_e = qe < w.rows;
+    const int ie = qe / prm.h_q;
+    const int he = qe - ie * prm.h_q;
+    const int64_t orow = ((int64_t)b * prm.s_q + ie) * prm.h_q + he;
+    // O / l for this CTA's columns [32 ch0, 32 ch1) of the row, to the final
+    // output or to this split's partial slot
+    auto drain = [&](int ch0, int ch1, float inv_l) {
+      ptx::tc_fence_after();
+#pragma unroll 1
+      for (int ch = ch0; ch < ch1; ++ch) {
+        uint32_t o[32];
+        tmem_load32(x.tmem + lane_base + kColO + ch * 32, o);
+        if (valid_e) {
+          const int d0 = (int)x.rank * 256 + ch * 32;
+          if (direct && !prm.out_f32) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
+                                                  orow * kDv + d0);
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              uint4 u;
+              u.x = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 0]) * inv_l,
+                                     __uint_as_float(o[8 * qq + 1]) * inv_l);
+              u.y = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 2]) * inv_l,
+                                     __uint_as_float(o[8 * qq + 3]) * inv_l);
+              u.z = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 4]) * inv_l,
+                                     __uint_as_float(o[8 * qq + 5]) * inv_l);
+              u.w = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 6]) * inv_l,
+                                     __uint_as_float(o[8 * qq + 7]) * inv_l);
+              dst[qq] = u;
+            }
+          } else {
+            // fp32: the final output row (fp32 out), or this split's partial
+            // ([dim / 4][row][4] in the workspace slot)
+            float4* base = direct ? reinterpret_cast<float4*>(static_cast<float*>(prm.out) +
+                                                              orow * kDv + d0)
+                                  : reinterpret_cast<float4*>(prm.ws_o) +
+                                        slot * (kDv / 4) * kTileRows +
+                                        (int64_t)(d0 / 4) * kTileRows + re;
+            const int64_t step = direct ? 1 : kTileRows;
+#pragma unroll
+            for (int qq = 0; qq < 8; ++qq)
+              base[qq * step] = make_float4(__uint_as_float(o[4 * qq]) * inv_l,
+                                            __uint_as_float(o[4 * qq + 1]) * inv_l,
+                                            __uint_as_float(o[4 * qq + 2]) * inv_l,
+                                            __uint_as_float(o[4 * qq + 3]) * inv_l);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(x.bar(B_OEMPTY));
+    };
     if (set == 1) {
       // hand this worker's sums (and the max they are scaled to) to set 0,
-      // once set 0 has read those of the tile before last
+      // once set 0 has read those of the tile before last; then drain the
+      // upper half of this CTA's columns once set 0 has published 1/l
       if (!wait_warp(x, x.bar(B_SUMSFREE + par), ((n_item >> 1) & 1u) ^ 1u)) return false;
       ptx::st_shared_u32(sums, __float_as_uint(m_run));
       ptx::st_shared_u32(sums + 4, __float_as_uint(l_run));
       ptx::st_shared_u32(sums + 8, __float_as_uint(lb_run));
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(x.bar(B_SUMS + par));
+      if (!wait_warp(x, x.bar(B_EPI), n_item & 1u)) return false;
+      if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
+      drain(4, 8, __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + kEpiInv + (uint32_t)re * 4u)));
       ++n_item;
       continue;
     }
@@ -889,10 +962,6 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
     // all that follows it.
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
     lb_run += __shfl_xor_sync(0xffffffffu, lb_run, 16);
-    const int ns = w.items[b * kItemWords + 1];
-    const bool direct = (ns == 1);
-    const int sidx = (n_item == 0) ? w.split0 : 0;
-    const int64_t slot = (int64_t)w.tile * w.stotal + w.items[b * kItemWords + 2] + sidx;
     const float inv_own = lb_run > 0.f ? 1.0f / lb_run : 0.f;
     if (half == 0)
       ptx::st_shared_u32(x.sbase + kInvL + par * 512u + (x.rank * kHalfRows + (uint32_t)hr) * 4u,
@@ -917,62 +986,18 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
     }
     if (!wait_warp(x, x.bar(B_OFULL), n_item & 1u)) return false;
     if (!wait_warp(x, x.bar(B_LRECV + par), (n_item >> 1) & 1u, true)) return false;
-    // rows of the epilogue: lane -> tile row quad * 32 + lane (mine when its
-    // half quadrant is this CTA's, and then this thread owned it)
-    const int re = quad * 32 + lane;
     const float inv_l =
         (half == (int)x.rank)
             ? inv_own
             : __uint_as_float(ptx::ld_shared_u32_volatile(
                   x.sbase + kInvL + par * 512u + (x.peer * kHalfRows + (uint32_t)hr) * 4u));
-    const int qe = w.tile * kTileRows + re;
-    const bool valid_e = qe < w.rows;
-    const int ie = qe / prm.h_q;
-    const int he = qe - ie * prm.h_q;
-    const int64_t orow = ((int64_t)b * prm.s_q + ie) * prm.h_q + he;
-    ptx::tc_fence_after();
-#pragma unroll 1
-    for (int ch = 0; ch < 8; ++ch) {
-      uint32_t o[32];
-      tmem_load32(x.tmem + lane_base + kColO + ch * 32, o);
-      if (valid_e) {
-        const int d0 = (int)x.rank * 256 + ch * 32;
-        if (direct && !prm.out_f32) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
-                                                orow * kDv + d0);
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            uint4 u;
-            u.x = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 0]) * inv_l,
-                                   __uint_as_float(o[8 * qq + 1]) * inv_l);
-            u.y = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 2]) * inv_l,
-                                   __uint_as_float(o[8 * qq + 3]) * inv_l);
-            u.z = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 4]) * inv_l,
-                                   __uint_as_float(o[8 * qq + 5]) * inv_l);
-            u.w = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 6]) * inv_l,
-                                   __uint_as_float(o[8 * qq + 7]) * inv_l);
-            dst[qq] = u;
-          }
-        } else {
-          // fp32: the final output row (fp32 out), or this split's partial
-          // ([dim / 4][row][4] in the workspace slot)
-          float4* base = direct ? reinterpret_cast<float4*>(static_cast<float*>(prm.out) +
-                                                            orow * kDv + d0)
-                                : reinterpret_cast<float4*>(prm.ws_o) +
-                                      slot * (kDv / 4) * kTileRows + (int64_t)(d0 / 4) * kTileRows + re;
-          const int64_t step = direct ? 1 : kTileRows;
-#pragma unroll
-          for (int qq = 0; qq < 8; ++qq)
-            base[qq * step] = make_float4(__uint_as_float(o[4 * qq]) * inv_l,
-                                          __uint_as_float(o[4 * qq + 1]) * inv_l,
-                                          __uint_as_float(o[4 * qq + 2]) * inv_l,
-                                          __uint_as_float(o[4 * qq + 3]) * inv_l);
-        }
-      }
-    }
-    ptx::tc_fence_before();
+    // publish 1/l of row re for set 1 (set 1 reads it before it arrives on
+    // OEMPTY, and the next tile's 1/l is written only after that tile's
+    // first P.V, which waits for OEMPTY)
+    ptx::st_shared_u32(x.sbase + kEpiInv + (uint32_t)re * 4u, __float_as_uint(inv_l));
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(x.bar(B_OEMPTY));
+    if (lane == 0) ptx::mbar_arrive(x.bar(B_EPI));
+    drain(0, 4, inv_l);
     ++n_item;
   }
   return true;
@@ -1043,7 +1068,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreads :
     }
     ptx::mbar_init(x.bar(B_OFULL), 1);
     for (int h = 0; h < 8; ++h) ptx::mbar_init(x.bar(B_HAND + h), 1);
-    ptx::mbar_init(x.bar(B_OEMPTY), kQuadWarps);
+    ptx::mbar_init(x.bar(B_OEMPTY), 2 * kQuadWarps);
+    ptx::mbar_init(x.bar(B_EPI), kQuadWarps);
     ptx::mbar_init(x.bar(B_TEARDOWN), 2);   // both MMA-issuing threads
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
@@ -1071,20 +1097,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreads :
   const int32_t* plan = prm.plan;
   Work w;
   bool has_work = false;
+  // The group size follows from the grid and the call's shape, so this
+  // cluster's entry is read in the same memory round trip as the header
+  // (it lies inside any plan of this call's shape, whose size the caller
+  // must provide); the header then decides whether it is used.
+  const int tiles_l = plan_tiles(prm.s_q, prm.h_q);
+  const int gt_l = plan_group_clusters((int)(gridDim.x >> 1), tiles_l);
+  const int tile_l = gt_l > 0 ? cluster / gt_l : tiles_l;
+  const int c_l = gt_l > 0 ? cluster - tile_l * gt_l : 0;
+  const int32_t* cl = plan + H_WORDS + c_l * kClusterWords;
+  const int e_b0 = cl[0], e_p0 = cl[1], e_b1 = cl[2], e_p1 = cl[3], e_s0 = cl[4];
   if (plan[H_MAGIC] != kPlanMagic || plan[H_BATCH] != prm.batch || plan[H_SQ] != prm.s_q ||
-      plan[H_HQ] != prm.h_q || plan[H_NCLUSTERS] != (int)(gridDim.x >> 1) || plan[H_GT] <= 0) {
+      plan[H_HQ] != prm.h_q || plan[H_NCLUSTERS] != (int)(gridDim.x >> 1) ||
+      plan[H_GT] != gt_l || plan[H_TILES] != tiles_l || gt_l <= 0) {
     if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
   } else {
-    const int tiles = plan[H_TILES], gt = plan[H_GT], gused = plan[H_GUSED];
-    w.tile = cluster / gt;
-    const int c = cluster - w.tile * gt;
-    if (w.tile < tiles && c < gused) {
-      const int32_t* cl = plan + H_WORDS + c * kClusterWords;
-      w.b0 = cl[0];
-      w.p0 = cl[1];
-      w.b1 = cl[2];
-      w.p1 = cl[3];
-      w.split0 = cl[4];
+    const int gused = plan[H_GUSED];
+    w.tile = tile_l;
+    if (w.tile < tiles_l && c_l < gused) {
+      w.b0 = e_b0;
+      w.p0 = e_p0;
+      w.b1 = e_b1;
+      w.p1 = e_p1;
+      w.split0 = e_s0;
       if (w.b0 < 0 || w.p0 < 0 || w.p1 < 0 || w.b0 > w.b1 || w.b1 > prm.batch ||
           (w.b1 == prm.batch && w.p1 != 0)) {
         if (threadIdx.x == 0 && rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
@@ -1092,7 +1127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kSparse ? kThreads :
         has_work = true;
         w.rows = prm.s_q * prm.h_q;
         w.stotal = plan[H_STOTAL];
-        w.items = plan + plan_off_items(gt) / 4;
+        w.items = plan + plan_off_items(gt_l) / 4;
       }
     }
   }
