@@ -17,8 +17,9 @@
 //  * One CTA per (128-query tile, head, batch entry); a causal grid starts
 //    the longest tiles first.  Warp 0 issues TMA loads (Q once, then K and V
 //    tiles of 128 keys through two-deep rings of their own), warp 1 owns
-//    TMEM and issues the MMAs, warps 4-7 run the softmax and the epilogue
-//    with one query row per thread (warp w reaches TMEM lanes 32 (w % 4) ..).
+//    TMEM and issues the MMAs, warps 4-11 run the softmax and the epilogue
+//    with two threads per query row, 64 key columns each (warp w reaches 16
+//    lanes of TMEM lane quadrant w % 4 through the 16x32bx2 access shape).
 //  * S = Q K^T (M=128, N=128, K=d_qk, both operands K-major from shared
 //    memory) lands in one of two 128-column TMEM tiles.  The softmax writes
 //    P as bf16 over the first 64 columns of the same tile, and P.V reads P
@@ -49,8 +50,9 @@
 namespace mla {
 namespace {
 
-constexpr int kAttThreads = 256;
-constexpr int kSoftWarp0 = 4;                 // warps 4-7: softmax and epilogue
+constexpr int kAttThreads = 384;
+constexpr int kSoftWarp0 = 4;                 // warps 4-11: softmax and epilogue
+constexpr int kSoftWarps = 8;                 // two per TMEM lane quadrant, 16 rows each
 constexpr int kTQ = 128, kTK = 128;           // query rows and keys per tile
 constexpr int kAttDv = 128;
 constexpr int kMaxDqkBoxes = 3;               // d_qk <= 192
@@ -66,7 +68,7 @@ enum ABar : int {
   A_VFULL = 5,     // [2]
   A_VEMPTY = 7,    // [2]
   A_SFULL = 9,     // [2] score tile ready (MMA commit)
-  A_PFULL = 11,    // [2] P written over the tile, O rescaled if needed (4 softmax warps)
+  A_PFULL = 11,    // [2] P written over the tile, O rescaled if needed (8 softmax warps)
   A_ODONE = 13,    // one phase per P.V MMA group
   A_COUNT = 14
 };
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       ptx::mbar_init(x.bar(A_VFULL + s), 1);
       ptx::mbar_init(x.bar(A_VEMPTY + s), 1);
       ptx::mbar_init(x.bar(A_SFULL + s), 1);
-      ptx::mbar_init(x.bar(A_PFULL + s), 4);
+      ptx::mbar_init(x.bar(A_PFULL + s), kSoftWarps);
     }
     ptx::mbar_init(x.bar(A_ODONE), 1);
     ptx::st_shared_u32(x.abort_addr, 0u);
@@ -226,12 +228,18 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     if (ok) issue_pv(n_kt - 1);
     __syncwarp();
   } else if (warp >= kSoftWarp0) {
+    // Two threads per query row: warp w works on 16 lanes (the first or the
+    // second 16) of TMEM lane quadrant w % 4; lane t takes lane t & 15 of
+    // them and key columns [64 (t >> 4), +64) of each tile.
+    const int sw = warp - kSoftWarp0;
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;
+    const int sub = sw >> 2;
+    const int half = lane >> 4;
+    const int r = quad * 32 + sub * 16 + (lane & 15);
     const int qi = qt * kTQ + r;
-    const uint32_t lanes = (uint32_t)(quad * 32) << 16;
+    const uint32_t lanes = (uint32_t)(quad * 32 + sub * 16) << 16;
     const float sl2 = args.scale_log2;
-    float m_ref = -INFINITY, l_f = 0.f, l_b = 0.f;
+    float m_ref = -INFINITY, l_f = 0.f, l_b = 0.f;   // sums of this thread's columns
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
       const int s = j & 1;
@@ -240,26 +248,32 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      float sv[kTK];
+      float sv[64];
 #pragma unroll
-      for (int c = 0; c < kTK / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        ptx::tmem_ld32_wait(tmem + lanes + kColS + 128u * s + 32u * c, v);
+        ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColS + 128u * s + 32u * c, v);
 #pragma unroll
         for (int k = 0; k < 32; ++k) sv[32 * c + k] = __uint_as_float(v[k]);
       }
       // keys past the sequence, or after the query when causal, get no weight
-      const int k0 = j * kTK;
+      const int k0 = j * kTK + 64 * half;
       const int lim = args.causal ? min(qi + 1, args.S) : args.S;
-      if (__any_sync(0xffffffffu, k0 + kTK > lim)) {
+      if (__any_sync(0xffffffffu, k0 + 64 > lim)) {
 #pragma unroll
-        for (int k = 0; k < kTK; ++k)
+        for (int k = 0; k < 64; ++k)
           if (k0 + k >= lim) sv[k] = -INFINITY;
       }
-      float mx = -INFINITY;
+      float m4[4];
 #pragma unroll
-      for (int k = 0; k < kTK; k += 4)
-        mx = fmaxf(mx, ptx::max3(sv[k], sv[k + 1], fmaxf(sv[k + 2], sv[k + 3])));
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float* a = sv + 16 * q4;
+        m4[q4] = ptx::max3(ptx::max3(ptx::max3(a[0], a[1], a[2]), ptx::max3(a[3], a[4], a[5]),
+                                     ptx::max3(a[6], a[7], a[8])),
+                           ptx::max3(a[9], a[10], a[11]), ptx::max3(a[12], a[13], fmaxf(a[14], a[15])));
+      }
+      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // the row's other half
       const float m_cand = fmaxf(m_ref, mx * sl2);
       const bool rescale = (j > 0) && (m_cand > m_ref + kARescale);
       float alpha = 1.0f;
@@ -272,28 +286,30 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         l_b *= alpha;
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      uint32_t pk[kTK / 2];
-      float sf0 = 0.f, sf1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+      uint32_t pk[32];
+      const uint64_t sc2 = ptx::f2_pack(sl2, sl2);
+      const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+      uint64_t sf2[2] = {0ull, 0ull}, sb2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int k = 0; k < kTK / 2; ++k) {
-        const float a = ptx::ex2(fmaf(sv[2 * k], sl2, neg_m));
-        const float c = ptx::ex2(fmaf(sv[2 * k + 1], sl2, neg_m));
-        sf0 += a;
-        sf1 += c;
+      for (int k = 0; k < 32; ++k) {
+        float xa, xc;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[2 * k], sv[2 * k + 1]), sc2, nm2), xa, xc);
+        const float a = ptx::ex2(xa), c = ptx::ex2(xc);
+        sf2[k & 1] = ptx::f2_add(sf2[k & 1], ptx::f2_pack(a, c));
         pk[k] = ptx::pack_bf16x2(a, c);
-        sb0 += __uint_as_float(pk[k] << 16);
-        sb1 += __uint_as_float(pk[k] & 0xffff0000u);
+        sb2[k & 1] = ptx::f2_add(sb2[k & 1], ptx::f2_pack(__uint_as_float(pk[k] << 16),
+                                                          __uint_as_float(pk[k] & 0xffff0000u)));
       }
-      l_f += sf0 + sf1;
-      l_b += sb0 + sb1;
-      // P (bf16 pairs) over the first 64 columns of the score tile
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) w[k] = pk[32 * c + k];
-        ptx::tmem_st32(tmem + lanes + kColS + 128u * s + 32u * c, w);
+      {
+        float fa, fc, ba, bc;
+        ptx::f2_unpack(ptx::f2_add(sf2[0], sf2[1]), fa, fc);
+        ptx::f2_unpack(ptx::f2_add(sb2[0], sb2[1]), ba, bc);
+        l_f += fa + fc;
+        l_b += ba + bc;
       }
+      // P (bf16 pairs) over the first 64 columns of the score tile: this
+      // thread's 64 keys are packed columns [32 half, +32)
+      ptx::tmem_st16x2<32>(tmem + lanes + kColS + 128u * s, pk);
       ptx::tmem_wait_st();
       // O must not be rescaled before the previous P.V has landed
       if (j > 0 && !await_warp(x, x.bar(A_ODONE), ((uint32_t)(j - 1)) & 1u)) {
@@ -303,12 +319,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       if (__any_sync(0xffffffffu, rescale)) {
         ptx::tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < kAttDv / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          ptx::tmem_ld32_wait(tmem + lanes + kColO + 32u * c, o);
+          ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColO + 32u * c, o);
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          ptx::tmem_st32(tmem + lanes + kColO + 32u * c, o);
+          ptx::tmem_st16x2<64>(tmem + lanes + kColO + 32u * c, o);
         }
         ptx::tmem_wait_st();
       }
@@ -316,17 +332,20 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(x.bar(A_PFULL + s));
     }
-    // Epilogue: O / l and lse once the last P.V has landed.
+    // Epilogue: O / l and lse once the last P.V has landed; each thread
+    // writes its 64 of the row's 128 output dims.
+    l_f += __shfl_xor_sync(0xffffffffu, l_f, 16);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 16);
     if (ok && await_warp(x, x.bar(A_ODONE), ((uint32_t)(n_kt - 1)) & 1u)) {
       ptx::tc_fence_after();
       const float inv_l = l_b > 0.f ? 1.0f / l_b : 0.f;
       const bool valid = qi < args.S;
       uint16_t* orow = static_cast<uint16_t*>(args.out) +
-                       (((int64_t)b * args.S + (valid ? qi : 0)) * args.H + h) * kAttDv;
+                       (((int64_t)b * args.S + (valid ? qi : 0)) * args.H + h) * kAttDv + 64 * half;
 #pragma unroll 1
-      for (int c = 0; c < kAttDv / 32; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        ptx::tmem_ld32_wait(tmem + lanes + kColO + 32u * c, o);
+        ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColO + 32u * c, o);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
@@ -338,7 +357,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
                 ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv_l, __uint_as_float(o[8 * q4 + 7]) * inv_l));
         }
       }
-      if (valid)
+      if (valid && half == 0)
         args.lse[((int64_t)b * args.H + h) * args.S + qi] =
             l_f > 0.f ? (m_ref + log2f(l_f)) * kALn2 : -INFINITY;
     }

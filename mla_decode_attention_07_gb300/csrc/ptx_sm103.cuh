@@ -299,6 +299,43 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 #undef MLA_R32
+// 16 lanes x 2 column groups: thread t reaches lane base + (t & 15), columns
+// col + (t >> 4) * OFF + j, j < 32.  The load waits for its data in the same
+// statement, as tmem_ld32_wait.
+#define MLA_R32(i) "=r"(r[i])
+template <int OFF>
+__device__ __forceinline__ void tmem_ld16x2_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32], "
+      "%33;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : MLA_R32(0), MLA_R32(1), MLA_R32(2), MLA_R32(3), MLA_R32(4), MLA_R32(5), MLA_R32(6),
+        MLA_R32(7), MLA_R32(8), MLA_R32(9), MLA_R32(10), MLA_R32(11), MLA_R32(12), MLA_R32(13),
+        MLA_R32(14), MLA_R32(15), MLA_R32(16), MLA_R32(17), MLA_R32(18), MLA_R32(19),
+        MLA_R32(20), MLA_R32(21), MLA_R32(22), MLA_R32(23), MLA_R32(24), MLA_R32(25),
+        MLA_R32(26), MLA_R32(27), MLA_R32(28), MLA_R32(29), MLA_R32(30), MLA_R32(31)
+      : "r"(taddr), "n"(OFF)
+      : "memory");
+}
+#undef MLA_R32
+#define MLA_W32(i) "r"(v[i])
+template <int OFF>
+__device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x32.b32 [%0], %1, "
+      "{%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, "
+      "%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};" ::"r"(
+          taddr),
+      "n"(OFF), MLA_W32(0), MLA_W32(1), MLA_W32(2), MLA_W32(3), MLA_W32(4), MLA_W32(5),
+      MLA_W32(6), MLA_W32(7), MLA_W32(8), MLA_W32(9), MLA_W32(10), MLA_W32(11), MLA_W32(12),
+      MLA_W32(13), MLA_W32(14), MLA_W32(15), MLA_W32(16), MLA_W32(17), MLA_W32(18), MLA_W32(19),
+      MLA_W32(20), MLA_W32(21), MLA_W32(22), MLA_W32(23), MLA_W32(24), MLA_W32(25), MLA_W32(26),
+      MLA_W32(27), MLA_W32(28), MLA_W32(29), MLA_W32(30), MLA_W32(31)
+      : "memory");
+}
+#undef MLA_W32
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
