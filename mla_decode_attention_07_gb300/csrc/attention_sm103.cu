@@ -14,8 +14,10 @@
 // this form with 128 heads, d_qk = 192 (128 + 64 rotary) and d_v = 128.
 //
 // GB300 design:
-//  * One CTA per (128-query tile, head, batch entry); a causal grid starts
-//    the longest tiles first.  Warp 0 issues TMA loads (Q once, then K and V
+//  * One CTA per (128-query tile, head, batch entry), launched in chunks of
+//    16 (batch, head) pairs so that the resident CTAs share the K/V of a few
+//    heads in L2; within a chunk a causal grid starts the longest tiles
+//    first.  Warp 0 issues TMA loads (Q once, then K and V
 //    tiles of 128 keys through two-deep rings of their own), warp 1 owns
 //    TMEM and issues the MMAs, warps 4-11 run the softmax and the epilogue
 //    with two threads per query row, 64 key columns each (warp w reaches 16
@@ -56,6 +58,7 @@ constexpr int kSoftWarps = 8;                 // two per TMEM lane quadrant, 16 
 constexpr int kTQ = 128, kTK = 128;           // query rows and keys per tile
 constexpr int kAttDv = 128;
 constexpr int kMaxDqkBoxes = 3;               // d_qk <= 192
+constexpr int kChunk = 16;                    // (batch, head) pairs whose blocks run together
 constexpr uint32_t kBox = 16384;              // 128 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t kSQ = 0;
 constexpr uint32_t kSK = kSQ + kMaxDqkBoxes * kBox;             // 2 stages x 3 boxes
@@ -126,9 +129,17 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   x.err = args.err;
   const uint32_t tslot = x.sbase + kAMisc;
 
-  // Work item: the heaviest (last) query tiles of every (b, h) first.
+  // Work item.  Blocks run in chunks of kChunk (batch, head) pairs, and
+  // within a chunk the heaviest (last) query tiles of its pairs come first:
+  // the blocks resident at one time then share the K/V of a few heads, which
+  // stay in L2 (all heads at once would stream K/V from HBM once per query
+  // tile).
   const int bh_n = args.B * args.H;
-  const int rank = (int)blockIdx.x / bh_n, bh = (int)blockIdx.x % bh_n;
+  const int chunk = (int)blockIdx.x / (kChunk * args.n_qt);
+  const int in_chunk = (int)blockIdx.x - chunk * kChunk * args.n_qt;
+  const int width = min(kChunk, bh_n - chunk * kChunk);
+  const int rank = in_chunk / width;
+  const int bh = chunk * kChunk + in_chunk % width;
   const int qt = args.causal ? args.n_qt - 1 - rank : rank;
   const int b = bh / args.H, h = bh % args.H;
   const int n_kt = args.causal ? qt + 1 : (args.S + kTK - 1) / kTK;

@@ -9,7 +9,8 @@
 // TileLang: Tensor-Core GEMM", its comparison table) measures exactly this
 // product in FP16 at 2048 x 2048 x 2048 against cuBLAS; the same kernel does
 // DeepSeek MLA's query absorption, q_latent[., h, :] = q_nope[., h, :] W_UK[h]
-// (d_nope 128 -> d_c 512 per head), with the heads as the batch.
+// (d_nope 128 -> d_c 512 per head), with the heads as the batch; its
+// epilogue also copies each row's rotary part beside the latent part.
 //
 // GB300 design:
 //  * One CTA per SM, persistent over 128 x 256 output tiles.  Warp 0 issues
@@ -62,6 +63,9 @@ struct GemmArgs {
   int M, N, K, batch, tiles_m, tiles_n;
   int out_type;             // MLA_DTYPE_F16 / BF16 / F32
   int* err;
+  // Query absorption only (else null): q_rope [M][batch][64] bf16, copied to
+  // the 64 elements that follow N in each row of C by the tiles with n = 0.
+  const uint4* rope;
 };
 
 struct GCtx {
@@ -240,9 +244,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int nt = t % args.tiles_n, rest = t / args.tiles_n;
       const int mt = rest % args.tiles_m, b = rest / args.tiles_m;
       const uint32_t acc = lt & 1u;
+      const int row = mt * kBM + quad * 32 + lane;
+      // the row's rotary part (absorption, tiles with n = 0): loaded before
+      // the accumulator wait so that its latency overlaps the MMAs
+      const bool rope = args.rope != nullptr && nt == 0 && row < args.M;
+      uint4 rp[8];
+      if (rope) {
+        const uint4* src = args.rope + ((long long)row * args.batch + b) * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) rp[j] = src[j];
+      }
       if (!gwait_warp(x, x.bar(G_ACC_FULL + acc), (lt >> 1) & 1u)) break;
       ptx::tc_fence_after();
-      const int row = mt * kBM + quad * 32 + lane;
       const int esize = args.out_type == MLA_DTYPE_F32 ? 4 : 2;
       char* crow = static_cast<char*>(args.c) +
                    ((long long)b * args.c_batch + (long long)row * args.ldc) * esize;
@@ -252,6 +265,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ptx::tmem_ld32_wait(tmem + ((uint32_t)(quad * 32) << 16) + acc * (uint32_t)kBN + ch * 32, v);
         const int n0 = nt * kBN + ch * 32;
         if (row < args.M && n0 < args.N) store_row32(args, crow, n0, v);
+      }
+      if (rope) {
+        // next to the row's absorbed latent part
+        uint4* dst = reinterpret_cast<uint4*>(crow + (long long)args.N * esize);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dst[j] = rp[j];
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -271,17 +290,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kGTmemCols);
-  }
-}
-
-// The rotary part of each query row next to its absorbed latent part:
-// q[r][h][512:576] = q_rope[r][h][0:64] (16-byte pieces).
-__global__ void mla_q_rope_kernel(const uint4* __restrict__ q_rope, uint4* __restrict__ q,
-                                  long long pieces) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pieces;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long rh = i >> 3, c = i & 7;
-    q[rh * 72 + 64 + c] = q_rope[i];
   }
 }
 
@@ -418,14 +426,9 @@ int mla_q_absorb(const void* q_nope, const void* q_rope, const void* w_uk, void*
   a.K = kNope;
   a.batch = h_q;
   a.out_type = MLA_DTYPE_BF16;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int rc = launch_gemm(MLA_DTYPE_BF16, ma, mb, a, s);
-  if (rc != MLA_OK) return rc;
-  const long long pieces = rows * h_q * (kRope * 2 / 16);
-  const int grid = (int)((pieces + 255) / 256 < 1024 ? (pieces + 255) / 256 : 1024);
-  mla_q_rope_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(q_rope), static_cast<uint4*>(q),
-                                         pieces);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  a.rope = static_cast<const uint4*>(q_rope);
+  static_assert(kRope * 2 == 8 * 16, "the rotary part of a row is eight 16-byte pieces");
+  return launch_gemm(MLA_DTYPE_BF16, ma, mb, a, static_cast<cudaStream_t>(stream));
 }
 
 int mla_cache_append(const void* kv_new, void* kv_cache, int num_pages, const int32_t* block_table,
