@@ -33,8 +33,9 @@
 //  * Online softmax in the log2 domain with a lazy rescale: O and the sums
 //    are rescaled only when a row max grows by more than 2^8, and the final
 //    1/l and lse use the same reference max, so the result is exact.  out is
-//    normalised by the sum of the bf16 probabilities P.V multiplies; lse
-//    comes from the fp32 sum.
+//    normalised by the sum of the bf16 probabilities P.V multiplies, which
+//    the tensor core accumulates beside O (P times a block of ones, M=128
+//    N=16); lse comes from the softmax threads' fp32 sum.
 //  * Every wait is bounded (2 s on %globaltimer): on expiry the kernel
 //    records MLA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land,
 //    frees TMEM and returns.
@@ -63,7 +64,11 @@ constexpr uint32_t kBox = 16384;              // 128 rows x 64 bf16, 128-byte sw
 constexpr uint32_t kSQ = 0;
 constexpr uint32_t kSK = kSQ + kMaxDqkBoxes * kBox;             // 2 stages x 3 boxes
 constexpr uint32_t kSV = kSK + 2 * kMaxDqkBoxes * kBox;         // 2 stages x 2 boxes
-constexpr uint32_t kABar = kSV + 2 * 2 * kBox;
+// bf16 ones, the B operand (16 columns x 128 keys) of an MMA that sums each
+// row of P; every element is 1, so the layout inside is immaterial
+constexpr uint32_t kSOnes = kSV + 2 * 2 * kBox;
+constexpr uint32_t kOnesBytes = 4096;
+constexpr uint32_t kABar = kSOnes + kOnesBytes;
 enum ABar : int {
   A_QFULL = 0,
   A_KFULL = 1,     // [2]
@@ -77,7 +82,8 @@ enum ABar : int {
 };
 constexpr uint32_t kAMisc = kABar + 8 * 16;
 constexpr uint32_t kASmem = kAMisc + 16 + 1024;
-constexpr uint32_t kColS = 0, kColO = 256, kATmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256, kColL = 384, kATmemCols = 512;
+constexpr int kSumCols = 16;                  // P.1: every column holds the row's sum
 constexpr float kARescale = 8.0f;
 constexpr float kALn2 = 0.69314718055994530942f;
 constexpr uint64_t kAWaitNs = 2000000000ull;
@@ -159,6 +165,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
   }
+  for (uint32_t o = threadIdx.x * 16u; o < kOnesBytes; o += kAttThreads * 16u)
+    ptx::st_shared_v4(x.sbase + kSOnes + o, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  ptx::fence_proxy_async_smem();   // the tensor core reads them
   if (warp == 1) {
     ptx::tmem_alloc(tslot, kATmemCols);
     ptx::tmem_relinquish();
@@ -198,6 +207,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // S(j) = Q K(j)^T, then P(j-1).V(j-1).
     constexpr uint32_t id_s = ptx::idesc_f32acc(kTQ, kTK, 0, 0, 1);
     constexpr uint32_t id_o = ptx::idesc_f32acc(kTQ, kAttDv, 0, 1, 1);
+    constexpr uint32_t id_l = ptx::idesc_f32acc(kTQ, kSumCols, 0, 0, 1);
     auto issue_pv = [&](int jj) -> bool {
       const int s = jj & 1;
       const uint32_t ph = ((uint32_t)jj >> 1) & 1u;
@@ -210,6 +220,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const uint64_t bd = ptx::smem_desc(x.sbase + kSV + s * 2 * kBox + k * 2048, kBox, 1024,
                                            ptx::kLayoutSw128);
         ptx::mma_ts_elect(tmem + kColO, tmem + kColS + 128u * s + 8u * k, bd, id_o,
+                          (jj > 0 || k > 0) ? 1u : 0u);
+        // the same P against ones: the sums of the bf16 probabilities P.V
+        // multiplies, accumulated (and rescaled) beside O
+        const uint64_t ld = ptx::smem_desc(x.sbase + kSOnes + (uint32_t)(k >> 2) * 2048u +
+                                               (uint32_t)(k & 3) * 32u,
+                                           16, 1024, ptx::kLayoutSw128);
+        ptx::mma_ts_elect(tmem + kColL, tmem + kColS + 128u * s + 8u * k, ld, id_l,
                           (jj > 0 || k > 0) ? 1u : 0u);
       }
       ptx::mma_commit_elect(x.bar(A_VEMPTY + s));
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int qi = qt * kTQ + r;
     const uint32_t lanes = (uint32_t)(quad * 32 + sub * 16) << 16;
     const float sl2 = args.scale_log2;
-    float m_ref = -INFINITY, l_f = 0.f, l_b = 0.f;   // sums of this thread's columns
+    float m_ref = -INFINITY, l_f = 0.f;   // fp32 sum of this thread's columns (for lse)
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
       const int s = j & 1;
@@ -294,13 +311,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         alpha = ptx::ex2(m_ref - m_cand);
         m_ref = m_cand;
         l_f *= alpha;
-        l_b *= alpha;
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
       uint32_t pk[32];
       const uint64_t sc2 = ptx::f2_pack(sl2, sl2);
       const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-      uint64_t sf2[2] = {0ull, 0ull}, sb2[2] = {0ull, 0ull};
+      uint64_t sf2[2] = {0ull, 0ull};
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         float xa, xc;
@@ -308,15 +324,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const float a = ptx::ex2(xa), c = ptx::ex2(xc);
         sf2[k & 1] = ptx::f2_add(sf2[k & 1], ptx::f2_pack(a, c));
         pk[k] = ptx::pack_bf16x2(a, c);
-        sb2[k & 1] = ptx::f2_add(sb2[k & 1], ptx::f2_pack(__uint_as_float(pk[k] << 16),
-                                                          __uint_as_float(pk[k] & 0xffff0000u)));
       }
       {
-        float fa, fc, ba, bc;
+        float fa, fc;
         ptx::f2_unpack(ptx::f2_add(sf2[0], sf2[1]), fa, fc);
-        ptx::f2_unpack(ptx::f2_add(sb2[0], sb2[1]), ba, bc);
         l_f += fa + fc;
-        l_b += ba + bc;
       }
       // P (bf16 pairs) over the first 64 columns of the score tile: this
       // thread's 64 keys are packed columns [32 half, +32)
@@ -337,6 +349,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
           ptx::tmem_st16x2<64>(tmem + lanes + kColO + 32u * c, o);
         }
+        {
+          uint32_t l8[8];   // the row's P sums, 8 of the 16 columns per thread
+          ptx::tmem_ld16x2_x8_wait<8>(tmem + lanes + kColL, l8);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) l8[k] = __float_as_uint(__uint_as_float(l8[k]) * alpha);
+          ptx::tmem_st16x2_x8<8>(tmem + lanes + kColL, l8);
+        }
         ptx::tmem_wait_st();
       }
       ptx::tc_fence_before();
@@ -346,9 +365,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // Epilogue: O / l and lse once the last P.V has landed; each thread
     // writes its 64 of the row's 128 output dims.
     l_f += __shfl_xor_sync(0xffffffffu, l_f, 16);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 16);
     if (ok && await_warp(x, x.bar(A_ODONE), ((uint32_t)(n_kt - 1)) & 1u)) {
       ptx::tc_fence_after();
+      uint32_t l8[8];
+      ptx::tmem_ld16x2_x8_wait<8>(tmem + lanes + kColL, l8);
+      const float l_b = __uint_as_float(l8[0]);
       const float inv_l = l_b > 0.f ? 1.0f / l_b : 0.f;
       const bool valid = qi < args.S;
       uint16_t* orow = static_cast<uint16_t*>(args.out) +

@@ -336,6 +336,27 @@ __device__ __forceinline__ void tmem_st16x2(uint32_t taddr, const uint32_t (&v)[
       : "memory");
 }
 #undef MLA_W32
+// 16 lanes x 2 groups of 8 columns: thread t reaches lane base + (t & 15),
+// columns col + (t >> 4) * OFF + j, j < 8 (load waited on in the statement).
+template <int OFF>
+__device__ __forceinline__ void tmem_ld16x2_x8_wait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr), "n"(OFF)
+      : "memory");
+}
+template <int OFF>
+__device__ __forceinline__ void tmem_st16x2_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, {%2, %3, %4, %5, %6, %7, %8, %9};" ::"r"(
+          taddr),
+      "n"(OFF), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+      "r"(v[7])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
