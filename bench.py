@@ -959,6 +959,13 @@ def run_prologue(args):
         raise RuntimeError(f"device error during warm-up: {libmla.mla_strerror(rc)}")
     sampler = ClockSampler(physical_gpu_index(dev.index))
     sampler.start()
+    t_end = time.perf_counter() + 1.0     # load under the clock sampler
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
     K = args.steps
     if world > 1:
         torch.distributed.barrier()

@@ -98,6 +98,11 @@ SMALL = [
     # one set), which exercises the running-max and sums hand-offs
     (112, 300, 1, 128, list(W.uniform_int(112, W.TENSOR_SEQLENS, 300, 1, 64)), 0),
     (113, 200, 2, 64, list(W.uniform_int(113, W.TENSOR_SEQLENS, 200, 0, 256)), 1),
+    # more query tokens per entry: 4 x 64 rows (two tiles), 8 x 128 rows
+    # (eight tiles, so eight groups of clusters), and a single head
+    (114, 3, 4, 64, [300, 4, 1100], 1),
+    (115, 2, 8, 128, [900, 2000], 0),
+    (116, 3, 1, 1, [70, 1, 500], 1),
 ]
 
 
