@@ -254,6 +254,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32, MINB) mla_combine_kernel(c
   // shared memory: every block reads the same few words, and one L2 request
   // per block instead of one per warp keeps that line from becoming a hot
   // spot.
+  // The next kernel on the stream (the next call's main kernel) may launch
+  // now: it waits for this grid to complete before it reads anything, and
+  // meanwhile its set-up (barriers, TMEM, cluster sync) overlaps this grid.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t* plan = p.plan;
   __shared__ int s_hdr[4];
   __shared__ int s_item[2];
