@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmla.so")
-SOURCES = ["mla_api.cu", "mla_decode_sm103.cu", "mla_noalloc.cu", "gemm_sm103.cu",
-           "attention_sm103.cu"]
+SOURCES = ["mla_api.cu", "mla_decode_sm103.cu", "mla_decode_narrow_sm103.cu", "mla_noalloc.cu",
+           "gemm_sm103.cu", "attention_sm103.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

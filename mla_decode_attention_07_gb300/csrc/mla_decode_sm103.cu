@@ -210,28 +210,6 @@ __device__ __forceinline__ bool wait_warp(const Ctx& x, uint32_t bar, uint32_t p
   return __all_sync(0xffffffffu, ok);
 }
 
-// Segments of the cluster's page range: item b, pages [pb, pe).
-struct SegIter {
-  int b, p, b1, p1;
-  const int32_t* items;
-  __device__ __forceinline__ bool next(int& sb, int& spb, int& spe) {
-    while (b < b1 || (b == b1 && p < p1)) {
-      const int P = items[b * kItemWords + 0];
-      const int pe = (b == b1) ? p1 : P;
-      const int cb = b, cp = p;
-      b += 1;
-      p = 0;
-      if (cp < pe) {
-        sb = cb;
-        spb = cp;
-        spe = pe;
-        return true;
-      }
-    }
-    return false;
-  }
-};
-
 struct Work {
   int tile, rows, b0, p0, b1, p1, split0, stotal;
   const int32_t* items;
@@ -1223,8 +1201,10 @@ cudaError_t decode_kernel_setup(int /*device*/) {
   const cudaError_t e = cudaFuncSetAttribute(
       mla_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kSmemAlloc);
+  const cudaError_t e2 = cudaFuncSetAttribute(
+      mla_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  if (e2 != cudaSuccess) return e2;
+  return narrow_kernel_setup();
 }
 
 int decode_max_clusters(int device) {
@@ -1238,8 +1218,11 @@ int decode_max_clusters(int device) {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)kSmemAlloc;
     int m = 0;
-    // the sparse instantiation (more threads) bounds both
+    // the sparse instantiation (more threads) bounds both; the narrow
+    // kernel runs on the same plans, so it bounds the count too
     if (cudaOccupancyMaxActiveClusters(&m, mla_decode_kernel<true>, &cfg) == cudaSuccess) n = m;
+    const int mn = narrow_max_clusters();
+    if (n > 0 && (mn < 0 || mn < n)) n = mn;
   }
   if (prev != device) cudaSetDevice(prev);
   return n;
@@ -1257,6 +1240,8 @@ cudaError_t launch_decode(const TensorMaps& m, const DecodeParams& p, int num_cl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.indices == nullptr && narrow_decode_shape(p.s_q, p.h_q, p.batch, p.max_pages, num_clusters))
+    return launch_decode_narrow(m.kv_lat, p, num_clusters, stream);
   if (p.indices != nullptr)
     return cudaLaunchKernelEx(&cfg, mla_decode_kernel<true>, m.q_rope, m.kv_lat, m.kv_rope, p);
   return cudaLaunchKernelEx(&cfg, mla_decode_kernel<false>, m.q_rope, m.kv_lat, m.kv_rope, p);

@@ -51,6 +51,15 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_decode(const TensorMaps& maps, const DecodeParams& p, int num_clusters,
                           cudaStream_t stream);
 
+// Decode kernel for at most 16 query rows per entry (mla_decode_narrow_sm103.cu):
+// the same plan, partials and combine as the general kernel.  launch_decode
+// routes dense calls to it when narrow_decode_shape holds.
+bool narrow_decode_shape(int s_q, int h_q, int batch, int max_pages, int num_clusters);
+cudaError_t narrow_kernel_setup();
+int narrow_max_clusters();   // co-resident 2-CTA clusters, or < 0
+cudaError_t launch_decode_narrow(const CUtensorMap& kv_map, const DecodeParams& p,
+                                 int num_clusters, cudaStream_t stream);
+
 // Device set-up shared by every entry point (mla_api.cu): the current device,
 // its SM count and the address of its device error word; MLA_OK or an error.
 int device_current(int* device, int* num_sms, int** err);

@@ -108,4 +108,26 @@ MLA_HD void cursor_of(const int64_t* starts, int batch, int64_t x, int* b_out, i
   *p_out = p;
 }
 
+// Segments of the cluster's page range: item b, pages [pb, pe).
+struct SegIter {
+  int b, p, b1, p1;
+  const int32_t* items;
+  MLA_HD bool next(int& sb, int& spb, int& spe) {
+    while (b < b1 || (b == b1 && p < p1)) {
+      const int P = items[b * kItemWords + 0];
+      const int pe = (b == b1) ? p1 : P;
+      const int cb = b, cp = p;
+      b += 1;
+      p = 0;
+      if (cp < pe) {
+        sb = cb;
+        spb = cp;
+        spe = pe;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
 }  // namespace mla

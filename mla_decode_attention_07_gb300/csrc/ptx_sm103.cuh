@@ -102,6 +102,13 @@ __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t remote_bar)
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                : "memory");
 }
+// Arrive on a barrier of another CTA of the cluster, releasing this thread's
+// earlier memory operations (global stores included) at cluster scope: a
+// waiter that acquires the phase at cluster scope sees them.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+               : "memory");
+}
 // Makes the value v an input of an (empty) volatile statement: everything v
 // depends on is computed before any later volatile statement is issued.
 __device__ __forceinline__ void consume(float v) { asm volatile("" ::"f"(v)); }
@@ -110,6 +117,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of the same condition (for a thread that polls several
+// barriers in turn).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)

@@ -103,6 +103,17 @@ SMALL = [
     (114, 3, 4, 64, [300, 4, 1100], 1),
     (115, 2, 8, 128, [900, 2000], 0),
     (116, 3, 1, 1, [70, 1, 500], 1),
+    # At most 16 query rows per entry with more than 4 block-table pages per
+    # cluster run the narrow kernel (the CTA pair takes alternate pages and
+    # merges per entry; cases 101, 109 and 116 above stay on the general
+    # kernel).  Many short entries (several entries per cluster, one-page
+    # segments where one CTA has no page, split and whole entries), two and
+    # four query tokens with rows that see no key, an empty entry, and long
+    # entries split across clusters.
+    (117, 300, 1, 16, list(W.uniform_int(117, W.TENSOR_SEQLENS, 300, 1, 200)), 0),
+    (118, 4, 2, 8, [1, 64, 65, 20000], 1),
+    (119, 4, 4, 4, [0, 2, 900, 25000], 1),
+    (124, 2, 1, 16, [20000, 9000], 0),
 ]
 
 
@@ -185,6 +196,28 @@ def test_deterministic_and_relabel_invariant(torch_cuda):
                            cache_seqlens=inp.cache_seqlens, s_q=2, h_q=128)
     o3, l3, _ = run_gpu(torch_cuda, moved)
     assert np.array_equal(o1, o3) and np.array_equal(l1, l3)
+
+
+@pytest.mark.parametrize("s_q,h_q,seqlens", [(1, 16, [12000, 7000]), (2, 8, [12000, 7000]),
+                                             (1, 16, [3000, 1700]), (1, 128, [3000, 1700]),
+                                             (2, 64, [3000, 1700])])
+def test_growing_scores_rescale(torch_cuda, oracle_mod, s_q, h_q, seqlens):
+    """Scores that grow along the sequence (a rotary dim of every key set to
+    a ramp, q's matching dim to 2) move the running max by more than the lazy
+    rescale threshold many times per entry: O and the sums are rescaled on
+    the GPU (the narrow kernel for the first two, the general one for the
+    rest), and the result must still match the oracle."""
+    inp = W.make_inputs(125, 2, s_q, h_q, seqlens, poison=False)
+    d = W.D_QK - 1
+    for b in range(inp.batch):
+        L = int(inp.cache_seqlens[b])
+        t = np.arange(L)
+        inp.kv_cache[inp.block_table[b, t // 64], t % 64, 0, d] = W.float32_to_bf16_bits(
+            t.astype(np.float32) * np.float32(0.05))
+    inp.q[..., d] = W.float32_to_bf16_bits(np.float32([2.0]))[0]
+    ref_o, ref_l = oracle_mod.mla_decode(inp)
+    out, lse, _ = run_gpu(torch_cuda, inp, out_f32=True)
+    assert_parity(out, lse, ref_o, ref_l, f"ramp s_q={s_q} h_q={h_q}")
 
 
 def test_shift_invariance_on_gpu(torch_cuda):
