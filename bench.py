@@ -49,6 +49,7 @@ DEFAULT_WORKLOAD = "b16_h128_l4096"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attend_traffic.json")
 SPARSE_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sparse_traffic.json")
 DECODE_SRC = os.path.join(ROOT, "mla_decode_attention_07_gb300", "csrc", "mla_decode_sm103.cu")
+NARROW_SRC = os.path.join(ROOT, "mla_decode_attention_07_gb300", "csrc", "mla_decode_narrow_sm103.cu")
 
 
 def parse_args(argv=None):
@@ -113,17 +114,21 @@ def kernel_code_sha(path: str) -> str:
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
-def traffic_per_launch(workload: str, path: str = TRAFFIC_FILE):
-    """DRAM bytes per attend launch from the committed ncu summary, if it was
-    taken on this workload and the kernel code is unchanged since."""
+def traffic_per_launch(workload: str, path: str = TRAFFIC_FILE, src: str = DECODE_SRC):
+    """DRAM bytes per launch from the committed ncu summary: the record taken
+    on this workload, if the source of the kernel that ran is unchanged since
+    (a file holds one record, or a list under "records")."""
     if not os.path.exists(path):
         return None
     try:
         with open(path) as f:
-            rec = json.load(f)
-        if rec.get("workload") != workload or rec.get("code_sha256") != kernel_code_sha(DECODE_SRC):
-            return None
-        return float(rec["dram_bytes_per_launch_full_workload"])
+            data = json.load(f)
+        recs = data.get("records", [data])
+        sha = kernel_code_sha(src)
+        for rec in recs:
+            if rec.get("workload") == workload and rec.get("code_sha256") == sha:
+                return float(rec["dram_bytes_per_launch_full_workload"])
+        return None
     except Exception:
         return None
 
@@ -487,7 +492,10 @@ def run_ours(args):
     else:
         achieved = w.flops() / attend_s / 1e12
         peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-    traffic = traffic_per_launch(w.name)
+    # which decode kernel this shape runs (the narrow one: <= 16 query rows)
+    narrow = libmla.mla_decode_kernel_kind(B, s_q, h_q, int(sets[0]["bt"].shape[1]), dev.index) == 1
+    kernel_name = "mla_decode_narrow_kernel (attend)" if narrow else "mla_decode_kernel (attend)"
+    traffic = traffic_per_launch(w.name, TRAFFIC_FILE, NARROW_SRC if narrow else DECODE_SRC)
 
     result = {
         "metric": METRIC,
@@ -513,7 +521,7 @@ def run_ours(args):
         "roofline_pct": round(100.0 * roof_s / (ms_step * 1e-3), 2),
         "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "mla_decode_kernel (attend)",
+                     "kernel": kernel_name,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured"
                      else "fallback"},
         "kernels_us": {"plan": round(plan_us, 3), "attend": round(attend_us, 3),

@@ -83,6 +83,16 @@ extern "C" {
  * this library's design needs the count to size the plan. */
 int mla_num_clusters(int device);
 
+/* Which decode kernel mla_decode (and mla_decode_f32, mla_decode_attend)
+ * runs for a call of this shape on `device`: 1 = the narrow kernel (at most
+ * 16 query rows per entry, s_q * h_q <= 16, and a block table of more than 4
+ * pages per cluster, batch * max_pages > 4 * mla_num_clusters), 0 = the
+ * general kernel; a negative code on error.  Both take the same plan and
+ * workspace and meet the same tolerances; this only names the kernel a
+ * profile will show.
+ * Defined by: no passage (a choice between two designs of this library). */
+int mla_decode_kernel_kind(int batch, int s_q, int h_q, int max_pages, int device);
+
 /* Bytes of tile metadata for a plan of this shape on `device` (0 on error).
  * The plan is the split-KV work partition: which pages of which batch entry
  * each cluster processes, and how many partial results each entry has.

@@ -498,6 +498,13 @@ int mla_num_clusters(int device) {
   return st == MLA_OK ? g_dev[device].num_clusters : st;
 }
 
+int mla_decode_kernel_kind(int batch, int s_q, int h_q, int max_pages, int device) {
+  if (!shape_ok(batch, s_q, h_q) || max_pages < 1) return MLA_ERR_INVALID_ARG;
+  const int st = setup_device(device);
+  if (st != MLA_OK) return st;
+  return narrow_decode_shape(s_q, h_q, batch, max_pages, g_dev[device].num_clusters) ? 1 : 0;
+}
+
 size_t mla_plan_size_for_clusters(int batch, int s_q, int h_q, int num_clusters) {
   if (!shape_ok(batch, s_q, h_q) || num_clusters < 1) return 0;
   const int gt = plan_group_clusters(num_clusters, plan_tiles(s_q, h_q));

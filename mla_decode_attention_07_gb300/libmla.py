@@ -32,7 +32,7 @@ EXPORTED = ["mla_num_clusters", "mla_plan_size", "mla_plan_size_for_clusters",
             "mla_decode_f32", "mla_decode_attend", "mla_decode_combine", "mla_decode_noalloc",
             "mla_decode_sparse", "mla_decode_sparse_f32", "mla_selftest_wait_timeout",
             "mla_check_device_error", "mla_strerror", "mla_cache_append", "mla_q_absorb",
-            "mla_gemm", "mla_attention_fwd"]
+            "mla_gemm", "mla_attention_fwd", "mla_decode_kernel_kind"]
 
 MLA_DTYPE_F16 = 0
 MLA_DTYPE_BF16 = 1
@@ -58,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     V, I, Z, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
     lib.mla_num_clusters.argtypes = [I]
     lib.mla_num_clusters.restype = I
+    lib.mla_decode_kernel_kind.argtypes = [I, I, I, I, I]
+    lib.mla_decode_kernel_kind.restype = I
     lib.mla_plan_size.argtypes = [I, I, I, I]
     lib.mla_plan_size.restype = Z
     lib.mla_plan_size_for_clusters.argtypes = [I, I, I, I]
@@ -131,6 +133,14 @@ def mla_num_clusters(device: int = 0) -> int:
     n = load().mla_num_clusters(int(device))
     _check(n if n < 0 else MLA_OK, "mla_num_clusters")
     return n
+
+
+def mla_decode_kernel_kind(batch: int, s_q: int, h_q: int, max_pages: int, device: int = 0) -> int:
+    """1 when mla_decode runs the narrow kernel for this shape, 0 for the
+    general one."""
+    k = load().mla_decode_kernel_kind(int(batch), int(s_q), int(h_q), int(max_pages), int(device))
+    _check(k if k < 0 else MLA_OK, "mla_decode_kernel_kind")
+    return k
 
 
 def mla_plan_size(batch: int, s_q: int, h_q: int, device: int = 0) -> int:

@@ -146,3 +146,9 @@ def test_no_gpu_means_error_not_fallback(lib):
         (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
     assert lib.mla_cache_append(0x1000, 0x2000, 4, 0x3000, 4, 0x4000, 1, 1, None) in \
         (libmla.MLA_ERR_CUDA, libmla.MLA_ERR_UNSUPPORTED_DEVICE)
+
+
+@pytest.mark.parametrize("args", [(0, 1, 16, 4), (1, 0, 16, 4), (1, 9, 16, 4), (1, 1, 0, 4),
+                                  (1, 1, 129, 4), (1, 1, 16, 0)])
+def test_kernel_kind_rejects_bad_shapes_on_host(lib, args):
+    assert lib.mla_decode_kernel_kind(*args, 0) == libmla.MLA_ERR_INVALID_ARG
