@@ -14,11 +14,15 @@
 // this form with 128 heads, d_qk = 192 (128 + 64 rotary) and d_v = 128.
 //
 // GB300 design:
-//  * One CTA per (128-query tile, head, batch entry), launched in chunks of
-//    16 (batch, head) pairs so that the resident CTAs share the K/V of a few
-//    heads in L2; within a chunk a causal grid starts the longest tiles
-//    first.  Warp 0 issues TMA loads (Q once, then K and V
-//    tiles of 128 keys through two-deep rings of their own), warp 1 owns
+//  * Persistent: one CTA per SM, each taking every grid-th work item, a
+//    work item being a (128-query tile, head, batch entry).  Items are
+//    ordered in chunks of 16 (batch, head) pairs so that the items running
+//    at one time share the K/V of a few heads in L2; within a chunk a causal
+//    grid takes the longest tiles first.  The roles count K/V tiles across
+//    items, so the loads, score MMAs and softmax of one item overlap the
+//    tail of the one before (set-up, Q and the first K/V tiles are no
+//    longer paid per item).  Warp 0 issues TMA loads (Q per item, then K and
+//    V tiles of 128 keys through two-deep rings of their own), warp 1 owns
 //    TMEM and issues the MMAs, warps 4-11 run the softmax and the epilogue
 //    with two threads per query row, 64 key columns each (warp w reaches 16
 //    lanes of TMEM lane quadrant w % 4 through the 16x32bx2 access shape).
@@ -78,7 +82,8 @@ enum ABar : int {
   A_SFULL = 9,     // [2] score tile ready (MMA commit)
   A_PFULL = 11,    // [2] P written over the tile, O rescaled if needed (8 softmax warps)
   A_ODONE = 13,    // one phase per P.V MMA group
-  A_COUNT = 14
+  A_QEMPTY = 14,   // the item's last score MMA is done: Q may be reloaded
+  A_COUNT = 15
 };
 constexpr uint32_t kAMisc = kABar + 8 * 16;
 constexpr uint32_t kASmem = kAMisc + 16 + 1024;
@@ -123,6 +128,29 @@ __device__ __forceinline__ bool await_warp(const ACtx& x, uint32_t bar, uint32_t
   return __all_sync(0xffffffffu, await_(x, bar, parity));
 }
 
+// Work item `item` (a 128-query tile of one head of one batch entry).  Items
+// run in chunks of kChunk (batch, head) pairs, and within a chunk the
+// heaviest (last) query tiles of its pairs come first: the items running at
+// one time then share the K/V of a few heads, which stay in L2 (all heads at
+// once would stream K/V from HBM once per query tile).
+struct AItem {
+  int b, h, qt, n_kt;
+};
+__device__ __forceinline__ AItem att_item(const AttArgs& a, int item) {
+  const int bh_n = a.B * a.H;
+  const int chunk = item / (kChunk * a.n_qt);
+  const int in_chunk = item - chunk * kChunk * a.n_qt;
+  const int width = min(kChunk, bh_n - chunk * kChunk);
+  const int rank = in_chunk / width;
+  const int bh = chunk * kChunk + in_chunk % width;
+  AItem it;
+  it.qt = a.causal ? a.n_qt - 1 - rank : rank;
+  it.b = bh / a.H;
+  it.h = bh % a.H;
+  it.n_kt = a.causal ? it.qt + 1 : (a.S + kTK - 1) / kTK;
+  return it;
+}
+
 __global__ void __launch_bounds__(kAttThreads, 1)
     mla_attention_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -135,24 +163,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   x.err = args.err;
   const uint32_t tslot = x.sbase + kAMisc;
 
-  // Work item.  Blocks run in chunks of kChunk (batch, head) pairs, and
-  // within a chunk the heaviest (last) query tiles of its pairs come first:
-  // the blocks resident at one time then share the K/V of a few heads, which
-  // stay in L2 (all heads at once would stream K/V from HBM once per query
-  // tile).
-  const int bh_n = args.B * args.H;
-  const int chunk = (int)blockIdx.x / (kChunk * args.n_qt);
-  const int in_chunk = (int)blockIdx.x - chunk * kChunk * args.n_qt;
-  const int width = min(kChunk, bh_n - chunk * kChunk);
-  const int rank = in_chunk / width;
-  const int bh = chunk * kChunk + in_chunk % width;
-  const int qt = args.causal ? args.n_qt - 1 - rank : rank;
-  const int b = bh / args.H, h = bh % args.H;
-  const int n_kt = args.causal ? qt + 1 : (args.S + kTK - 1) / kTK;
   const int nbq = args.dqk / 64;
+  const int total_items = args.n_qt * args.B * args.H;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(x.bar(A_QFULL), 1);
+    ptx::mbar_init(x.bar(A_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(x.bar(A_KFULL + s), 1);
       ptx::mbar_init(x.bar(A_KEMPTY + s), 1);
@@ -182,35 +198,61 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_u32_volatile(tslot);
 
+  // Every role walks the same items (item = blockIdx.x + k * gridDim.x) and
+  // counts K/V tiles across them (jt): stage, score tile and barrier phases
+  // follow jt, so one item's tail overlaps the next one's head.
   if (warp == 0) {
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(x.bar(A_QFULL), nbq * kBox);
-      for (int c = 0; c < nbq; ++c)
-        ptx::tma_load_4d(x.sbase + kSQ + c * kBox, &tm_q, 64 * c, h, qt * kTQ, b, x.bar(A_QFULL));
-      for (int j = 0; j < n_kt; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = ((uint32_t)j >> 1) & 1u;
-        if (!await_(x, x.bar(A_KEMPTY + s), ph ^ 1u)) break;
+      uint32_t jt = 0, nq = 0;
+      bool ok = true;
+      auto load_k = [&](const AItem& it, int j) -> bool {
+        const int s = (int)(jt & 1u);
+        const uint32_t ph = (jt >> 1) & 1u;
+        if (!await_(x, x.bar(A_KEMPTY + s), ph ^ 1u)) return false;
         ptx::mbar_arrive_expect_tx(x.bar(A_KFULL + s), nbq * kBox);
         for (int c = 0; c < nbq; ++c)
-          ptx::tma_load_4d(x.sbase + kSK + (s * kMaxDqkBoxes + c) * kBox, &tm_k, 64 * c, h, j * kTK,
-                           b, x.bar(A_KFULL + s));
-        if (!await_(x, x.bar(A_VEMPTY + s), ph ^ 1u)) break;
+          ptx::tma_load_4d(x.sbase + kSK + (s * kMaxDqkBoxes + c) * kBox, &tm_k, 64 * c, it.h,
+                           j * kTK, it.b, x.bar(A_KFULL + s));
+        return true;
+      };
+      auto load_v = [&](const AItem& it, int j) -> bool {
+        const int s = (int)(jt & 1u);
+        const uint32_t ph = (jt >> 1) & 1u;
+        if (!await_(x, x.bar(A_VEMPTY + s), ph ^ 1u)) return false;
         ptx::mbar_arrive_expect_tx(x.bar(A_VFULL + s), 2 * kBox);
         for (int c = 0; c < 2; ++c)
-          ptx::tma_load_4d(x.sbase + kSV + (s * 2 + c) * kBox, &tm_v, 64 * c, h, j * kTK, b,
+          ptx::tma_load_4d(x.sbase + kSV + (s * 2 + c) * kBox, &tm_v, 64 * c, it.h, j * kTK, it.b,
                            x.bar(A_VFULL + s));
+        return true;
+      };
+      for (int item = (int)blockIdx.x; ok && item < total_items; item += (int)gridDim.x) {
+        const AItem it = att_item(args, item);
+        // the item's first K tile (its stage is freed by the score MMA two
+        // tiles back), then Q (once the previous item's last score MMA is
+        // done), then the rest in tile order
+        ok = load_k(it, 0);
+        if (!ok) break;
+        if (!await_(x, x.bar(A_QEMPTY), (nq & 1u) ^ 1u)) break;
+        ptx::mbar_arrive_expect_tx(x.bar(A_QFULL), nbq * kBox);
+        for (int c = 0; c < nbq; ++c)
+          ptx::tma_load_4d(x.sbase + kSQ + c * kBox, &tm_q, 64 * c, it.h, it.qt * kTQ, it.b,
+                           x.bar(A_QFULL));
+        ++nq;
+        ok = load_v(it, 0);
+        ++jt;
+        for (int j = 1; ok && j < it.n_kt; ++j, ++jt) ok = load_k(it, j) && load_v(it, j);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // S(j) = Q K(j)^T, then P(j-1).V(j-1).
+    // S(t) = Q K(t)^T, then P(t-1).V(t-1) (+ P(t-1).1) within an item; an
+    // item's last P.V follows its last score MMA
     constexpr uint32_t id_s = ptx::idesc_f32acc(kTQ, kTK, 0, 0, 1);
     constexpr uint32_t id_o = ptx::idesc_f32acc(kTQ, kAttDv, 0, 1, 1);
     constexpr uint32_t id_l = ptx::idesc_f32acc(kTQ, kSumCols, 0, 0, 1);
-    auto issue_pv = [&](int jj) -> bool {
-      const int s = jj & 1;
-      const uint32_t ph = ((uint32_t)jj >> 1) & 1u;
+    auto issue_pv = [&](uint32_t tt, bool first) -> bool {
+      const int s = (int)(tt & 1u);
+      const uint32_t ph = (tt >> 1) & 1u;
       if (!await_warp(x, x.bar(A_PFULL + s), ph)) return false;
       if (!await_warp(x, x.bar(A_VFULL + s), ph)) return false;
       ptx::tc_fence_after();
@@ -220,40 +262,62 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         const uint64_t bd = ptx::smem_desc(x.sbase + kSV + s * 2 * kBox + k * 2048, kBox, 1024,
                                            ptx::kLayoutSw128);
         ptx::mma_ts_elect(tmem + kColO, tmem + kColS + 128u * s + 8u * k, bd, id_o,
-                          (jj > 0 || k > 0) ? 1u : 0u);
+                          (!first || k > 0) ? 1u : 0u);
         // the same P against ones: the sums of the bf16 probabilities P.V
         // multiplies, accumulated (and rescaled) beside O
         const uint64_t ld = ptx::smem_desc(x.sbase + kSOnes + (uint32_t)(k >> 2) * 2048u +
                                                (uint32_t)(k & 3) * 32u,
                                            16, 1024, ptx::kLayoutSw128);
         ptx::mma_ts_elect(tmem + kColL, tmem + kColS + 128u * s + 8u * k, ld, id_l,
-                          (jj > 0 || k > 0) ? 1u : 0u);
+                          (!first || k > 0) ? 1u : 0u);
       }
       ptx::mma_commit_elect(x.bar(A_VEMPTY + s));
       ptx::mma_commit_elect(x.bar(A_ODONE));
       return true;
     };
-    bool ok = await_warp(x, x.bar(A_QFULL), 0u);
-    for (int j = 0; ok && j < n_kt; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = ((uint32_t)j >> 1) & 1u;
-      if (!await_warp(x, x.bar(A_KFULL + s), ph)) {
+    uint32_t jt = 0, nq = 0;
+    bool ok = true, pending = false, pending_first = false;
+    uint32_t pending_t = 0;
+    for (int item = (int)blockIdx.x; ok && item < total_items; item += (int)gridDim.x) {
+      const AItem it = att_item(args, item);
+      if (!await_warp(x, x.bar(A_QFULL), nq & 1u)) {
         ok = false;
         break;
       }
-      ptx::tc_fence_after();
-      for (int k = 0; k < nbq * 4; ++k) {
-        const uint32_t off = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
-        const uint64_t ad = ptx::smem_desc(x.sbase + kSQ + off, 16, 1024, ptx::kLayoutSw128);
-        const uint64_t bd = ptx::smem_desc(x.sbase + kSK + s * kMaxDqkBoxes * kBox + off, 16, 1024,
-                                           ptx::kLayoutSw128);
-        ptx::mma_ss_elect(tmem + kColS + 128u * s, ad, bd, id_s, k ? 1u : 0u);
+      ++nq;
+      for (int j = 0; j < it.n_kt; ++j, ++jt) {
+        const int s = (int)(jt & 1u);
+        const uint32_t ph = (jt >> 1) & 1u;
+        if (!await_warp(x, x.bar(A_KFULL + s), ph)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        for (int k = 0; k < nbq * 4; ++k) {
+          const uint32_t off = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
+          const uint64_t ad = ptx::smem_desc(x.sbase + kSQ + off, 16, 1024, ptx::kLayoutSw128);
+          const uint64_t bd = ptx::smem_desc(x.sbase + kSK + s * kMaxDqkBoxes * kBox + off, 16,
+                                             1024, ptx::kLayoutSw128);
+          ptx::mma_ss_elect(tmem + kColS + 128u * s, ad, bd, id_s, k ? 1u : 0u);
+        }
+        ptx::mma_commit_elect(x.bar(A_SFULL + s));
+        ptx::mma_commit_elect(x.bar(A_KEMPTY + s));
+        if (j == it.n_kt - 1) ptx::mma_commit_elect(x.bar(A_QEMPTY));   // Q may be reloaded
+        if (pending && !issue_pv(pending_t, pending_first)) {
+          ok = false;
+          break;
+        }
+        pending = true;
+        pending_t = jt;
+        pending_first = (j == 0);
       }
-      ptx::mma_commit_elect(x.bar(A_SFULL + s));
-      ptx::mma_commit_elect(x.bar(A_KEMPTY + s));
-      if (j >= 1) ok = issue_pv(j - 1);
+      // the item's last P.V right away, so its epilogue need not wait for
+      // the next item's Q (loading meanwhile)
+      if (ok && pending) {
+        ok = issue_pv(pending_t, pending_first);
+        pending = false;
+      }
     }
-    if (ok) issue_pv(n_kt - 1);
     __syncwarp();
   } else if (warp >= kSoftWarp0) {
     // Two threads per query row: warp w works on 16 lanes (the first or the
@@ -264,108 +328,119 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const int sub = sw >> 2;
     const int half = lane >> 4;
     const int r = quad * 32 + sub * 16 + (lane & 15);
-    const int qi = qt * kTQ + r;
     const uint32_t lanes = (uint32_t)(quad * 32 + sub * 16) << 16;
     const float sl2 = args.scale_log2;
-    float m_ref = -INFINITY, l_f = 0.f;   // fp32 sum of this thread's columns (for lse)
+    uint32_t jt = 0;
     bool ok = true;
-    for (int j = 0; j < n_kt; ++j) {
-      const int s = j & 1;
-      if (!await_warp(x, x.bar(A_SFULL + s), ((uint32_t)j >> 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      float sv[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColS + 128u * s + 32u * c, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) sv[32 * c + k] = __uint_as_float(v[k]);
-      }
-      // keys past the sequence, or after the query when causal, get no weight
-      const int k0 = j * kTK + 64 * half;
-      const int lim = args.causal ? min(qi + 1, args.S) : args.S;
-      if (__any_sync(0xffffffffu, k0 + 64 > lim)) {
-#pragma unroll
-        for (int k = 0; k < 64; ++k)
-          if (k0 + k >= lim) sv[k] = -INFINITY;
-      }
-      float m4[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float* a = sv + 16 * q4;
-        m4[q4] = ptx::max3(ptx::max3(ptx::max3(a[0], a[1], a[2]), ptx::max3(a[3], a[4], a[5]),
-                                     ptx::max3(a[6], a[7], a[8])),
-                           ptx::max3(a[9], a[10], a[11]), ptx::max3(a[12], a[13], fmaxf(a[14], a[15])));
-      }
-      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // the row's other half
-      const float m_cand = fmaxf(m_ref, mx * sl2);
-      const bool rescale = (j > 0) && (m_cand > m_ref + kARescale);
-      float alpha = 1.0f;
-      if (j == 0) {
-        m_ref = m_cand;
-      } else if (rescale) {
-        alpha = ptx::ex2(m_ref - m_cand);
-        m_ref = m_cand;
-        l_f *= alpha;
-      }
-      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      uint32_t pk[32];
-      const uint64_t sc2 = ptx::f2_pack(sl2, sl2);
-      const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
-      uint64_t sf2[2] = {0ull, 0ull};
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        float xa, xc;
-        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[2 * k], sv[2 * k + 1]), sc2, nm2), xa, xc);
-        const float a = ptx::ex2(xa), c = ptx::ex2(xc);
-        sf2[k & 1] = ptx::f2_add(sf2[k & 1], ptx::f2_pack(a, c));
-        pk[k] = ptx::pack_bf16x2(a, c);
-      }
-      {
-        float fa, fc;
-        ptx::f2_unpack(ptx::f2_add(sf2[0], sf2[1]), fa, fc);
-        l_f += fa + fc;
-      }
-      // P (bf16 pairs) over the first 64 columns of the score tile: this
-      // thread's 64 keys are packed columns [32 half, +32)
-      ptx::tmem_st16x2<32>(tmem + lanes + kColS + 128u * s, pk);
-      ptx::tmem_wait_st();
-      // O must not be rescaled before the previous P.V has landed
-      if (j > 0 && !await_warp(x, x.bar(A_ODONE), ((uint32_t)(j - 1)) & 1u)) {
-        ok = false;
-        break;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
+    for (int item = (int)blockIdx.x; ok && item < total_items; item += (int)gridDim.x) {
+      const AItem it = att_item(args, item);
+      const int qi = it.qt * kTQ + r;
+      float m_ref = -INFINITY, l_f = 0.f;   // fp32 sum of this thread's columns (for lse)
+      for (int j = 0; j < it.n_kt; ++j, ++jt) {
+        const int s = (int)(jt & 1u);
+        if (!await_warp(x, x.bar(A_SFULL + s), (jt >> 1) & 1u)) {
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColO + 32u * c, o);
+        float sv[64];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-          ptx::tmem_st16x2<64>(tmem + lanes + kColO + 32u * c, o);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColS + 128u * s + 32u * c, v);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) sv[32 * c + k] = __uint_as_float(v[k]);
+        }
+        // keys past the sequence, or after the query when causal, get no weight
+        const int k0 = j * kTK + 64 * half;
+        const int lim = args.causal ? min(qi + 1, args.S) : args.S;
+        if (__any_sync(0xffffffffu, k0 + 64 > lim)) {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (k0 + k >= lim) sv[k] = -INFINITY;
+        }
+        float m4[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* a = sv + 16 * q4;
+          m4[q4] = ptx::max3(ptx::max3(ptx::max3(a[0], a[1], a[2]), ptx::max3(a[3], a[4], a[5]),
+                                       ptx::max3(a[6], a[7], a[8])),
+                             ptx::max3(a[9], a[10], a[11]), ptx::max3(a[12], a[13], fmaxf(a[14], a[15])));
+        }
+        float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));   // the row's other half
+        const float m_cand = fmaxf(m_ref, mx * sl2);
+        const bool rescale = (j > 0) && (m_cand > m_ref + kARescale);
+        float alpha = 1.0f;
+        if (j == 0) {
+          m_ref = m_cand;
+        } else if (rescale) {
+          alpha = ptx::ex2(m_ref - m_cand);
+          m_ref = m_cand;
+          l_f *= alpha;
+        }
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        uint32_t pk[32];
+        const uint64_t sc2 = ptx::f2_pack(sl2, sl2);
+        const uint64_t nm2 = ptx::f2_pack(neg_m, neg_m);
+        uint64_t sf2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          float xa, xc;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(sv[2 * k], sv[2 * k + 1]), sc2, nm2), xa, xc);
+          const float a = ptx::ex2(xa), c = ptx::ex2(xc);
+          sf2[k & 1] = ptx::f2_add(sf2[k & 1], ptx::f2_pack(a, c));
+          pk[k] = ptx::pack_bf16x2(a, c);
         }
         {
-          uint32_t l8[8];   // the row's P sums, 8 of the 16 columns per thread
-          ptx::tmem_ld16x2_x8_wait<8>(tmem + lanes + kColL, l8);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) l8[k] = __float_as_uint(__uint_as_float(l8[k]) * alpha);
-          ptx::tmem_st16x2_x8<8>(tmem + lanes + kColL, l8);
+          float fa, fc;
+          ptx::f2_unpack(ptx::f2_add(sf2[0], sf2[1]), fa, fc);
+          l_f += fa + fc;
         }
+        // P (bf16 pairs) over the first 64 columns of the score tile: this
+        // thread's 64 keys are packed columns [32 half, +32)
+        ptx::tmem_st16x2<32>(tmem + lanes + kColS + 128u * s, pk);
         ptx::tmem_wait_st();
+        // O must not be rescaled before the previous P.V has landed (waited
+        // on every tile but an item's first, which keeps the phase of the
+        // P.V barrier within one of this wait's parity)
+        if (j > 0 && !await_warp(x, x.bar(A_ODONE), (jt - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColO + 32u * c, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            ptx::tmem_st16x2<64>(tmem + lanes + kColO + 32u * c, o);
+          }
+          {
+            uint32_t l8[8];   // the row's P sums, 8 of the 16 columns per thread
+            ptx::tmem_ld16x2_x8_wait<8>(tmem + lanes + kColL, l8);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) l8[k] = __float_as_uint(__uint_as_float(l8[k]) * alpha);
+            ptx::tmem_st16x2_x8<8>(tmem + lanes + kColL, l8);
+          }
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(x.bar(A_PFULL + s));
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(A_PFULL + s));
-    }
-    // Epilogue: O / l and lse once the last P.V has landed; each thread
-    // writes its 64 of the row's 128 output dims.
-    l_f += __shfl_xor_sync(0xffffffffu, l_f, 16);
-    if (ok && await_warp(x, x.bar(A_ODONE), ((uint32_t)(n_kt - 1)) & 1u)) {
+      if (!ok) break;
+      // Epilogue: O / l and lse once the item's last P.V has landed; each
+      // thread writes its 64 of the row's 128 output dims.  The next item's
+      // first P.V (which overwrites O) waits for this item's P of its first
+      // tile, which these threads write only after this.
+      l_f += __shfl_xor_sync(0xffffffffu, l_f, 16);
+      if (!await_warp(x, x.bar(A_ODONE), (jt - 1) & 1u)) {
+        ok = false;
+        break;
+      }
       ptx::tc_fence_after();
       uint32_t l8[8];
       ptx::tmem_ld16x2_x8_wait<8>(tmem + lanes + kColL, l8);
@@ -373,7 +448,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const float inv_l = l_b > 0.f ? 1.0f / l_b : 0.f;
       const bool valid = qi < args.S;
       uint16_t* orow = static_cast<uint16_t*>(args.out) +
-                       (((int64_t)b * args.S + (valid ? qi : 0)) * args.H + h) * kAttDv + 64 * half;
+                       (((int64_t)it.b * args.S + (valid ? qi : 0)) * args.H + it.h) * kAttDv + 64 * half;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
@@ -390,11 +465,11 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
       }
       if (valid && half == 0)
-        args.lse[((int64_t)b * args.H + h) * args.S + qi] =
+        args.lse[((int64_t)it.b * args.H + it.h) * args.S + qi] =
             l_f > 0.f ? (m_ref + log2f(l_f)) * kALn2 : -INFINITY;
+      ptx::tc_fence_before();
     }
   }
-
   __syncthreads();
   if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) {
     const uint64_t t0 = ptx::globaltimer();
@@ -466,7 +541,9 @@ extern "C" int mla_attention_fwd(const void* q, const void* k, const void* v, vo
   a.n_qt = (int)n_qt;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = err;
-  mla_attention_kernel<<<(unsigned)grid, kAttThreads, kASmem, static_cast<cudaStream_t>(stream)>>>(
+  // persistent: one CTA per SM, each taking every grid-th work item
+  const unsigned ctas = (unsigned)(grid < (long long)sms ? grid : (long long)sms);
+  mla_attention_kernel<<<ctas, kAttThreads, kASmem, static_cast<cudaStream_t>(stream)>>>(
       mq, mk, mv, a);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
