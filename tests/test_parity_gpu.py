@@ -114,6 +114,9 @@ SMALL = [
     (118, 4, 2, 8, [1, 64, 65, 20000], 1),
     (119, 4, 4, 4, [0, 2, 900, 25000], 1),
     (124, 2, 1, 16, [20000, 9000], 0),
+    # fewer rows than the narrow kernel's 16: one head, and four heads
+    (127, 3, 1, 1, [9000, 70, 30000], 1),
+    (128, 2, 1, 4, [20000, 15000], 0),
 ]
 
 
@@ -137,6 +140,19 @@ def test_small_parity(torch_cuda, case, oracle_mod):
     assert_bf16_is_rounded_f32(out16, out32, f"case {seed}")
     if seed not in BF16_UNREPRESENTABLE:
         assert_parity(out16, lse16, ref_o, ref_l, f"case {seed} bf16 out")
+
+
+def test_narrow_cases_take_the_narrow_kernel(torch_cuda):
+    """The cases meant for the narrow kernel do run it (and the small ones
+    with few rows stay on the general kernel)."""
+    nc = libmla.mla_num_clusters(0)
+    for seed, B, s_q, h_q, seqlens, extra in SMALL:
+        inp = W.make_inputs(seed, B, s_q, h_q, seqlens, extra_pages=extra)
+        kind = libmla.mla_decode_kernel_kind(B, s_q, h_q, int(inp.block_table.shape[1]))
+        want = s_q * h_q <= 16 and B * inp.block_table.shape[1] > 4 * nc
+        assert kind == (1 if want else 0), (seed, kind)
+        if seed in (117, 118, 119, 124, 127, 128):
+            assert kind == 1, seed
 
 
 @pytest.mark.parametrize("case", [c for c in SMALL if c[0] in (104, 106, 113, 115, 117, 124)],
