@@ -492,7 +492,7 @@ def run_ours(args):
     else:
         achieved = w.flops() / attend_s / 1e12
         peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-    # which decode kernel this shape runs (the narrow one: <= 16 query rows)
+    # which decode kernel this shape runs (the narrow one: <= 32 query rows)
     narrow = libmla.mla_decode_kernel_kind(B, s_q, h_q, int(sets[0]["bt"].shape[1]), dev.index) == 1
     kernel_name = "mla_decode_narrow_kernel (attend)" if narrow else "mla_decode_kernel (attend)"
     traffic = traffic_per_launch(w.name, TRAFFIC_FILE, NARROW_SRC if narrow else DECODE_SRC)

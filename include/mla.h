@@ -85,7 +85,7 @@ int mla_num_clusters(int device);
 
 /* Which decode kernel mla_decode (and mla_decode_f32, mla_decode_attend)
  * runs for a call of this shape on `device`: 1 = the narrow kernel (at most
- * 16 query rows per entry, s_q * h_q <= 16, and a block table of more than 4
+ * 32 query rows per entry, s_q * h_q <= 32, and a block table of more than 4
  * pages per cluster, batch * max_pages > 4 * mla_num_clusters), 0 = the
  * general kernel; a negative code on error.  Both take the same plan and
  * workspace and meet the same tolerances; this only names the kernel a

@@ -1,5 +1,6 @@
-// MLA decode for few query rows per batch entry (s_q * h_q <= 16, e.g. the
-// 16 heads per GPU of a model with 128 heads split over 8 GPUs), sm_103a.
+// MLA decode for few query rows per batch entry (s_q * h_q <= 32, e.g. the
+// 16 or 32 heads per GPU of a model with 128 heads split over 8 or 4 GPUs,
+// or two speculative tokens of 16 heads), sm_103a.
 //
 // What it computes is the paged MLA decode of mla_decode_sm103.cu (the same
 // plan, the same partial results and combine, the same numerics): per query
@@ -8,25 +9,27 @@
 //
 // Why a second kernel.  The general kernel runs 128 query rows per tile on a
 // CTA pair that exchanges partial scores and probabilities every page,
-// because O for 128 rows x 512 dims fills a whole SM's TMEM.  With at most 16
-// rows the whole problem fits one SM, with room to spare:
+// because O for 128 rows x 512 dims fills a whole SM's TMEM.  With R <= 32
+// rows the whole problem fits one SM:
 //  * O is kept transposed: O^T = V^T P^T (M = 512 value dims in four blocks
-//    of 128 TMEM lanes, N = 16 rows, K = 64 keys), 64 TMEM columns.  V^T is
-//    the page stage itself read as an M/N-major A operand; P^T is a 2 KB
-//    K-major tile.
-//  * S = Q K^T runs with M = 128: TMEM lane m holds query row m % 16, so each
-//    row appears in 8 lanes (Q is stored 8 times in TMEM as the A operand,
-//    288 columns for 576 dims).  The tensor core does 8x the score work,
-//    which it has room for (the page is HBM-bound), and in exchange every one
-//    of 128 threads finds a whole score row in its own lane: it takes the
-//    row max itself and exponentiates 8 of the 64 columns (read through the
-//    16x32bx2 access shape), with no exchange between threads per page.
+//    of 128 TMEM lanes, N = R rows (16 or 32), K = 64 keys), 4 R TMEM
+//    columns.  V^T is the page stage itself read as an M/N-major A operand;
+//    P^T is an R x 64 K-major tile.
+//  * S = Q K^T runs with M = 128: TMEM lane m holds query row m % R, so each
+//    row appears in 128 / R lanes (Q is stored that many times in TMEM as the
+//    A operand, 288 columns for 576 dims).  The tensor core does the extra
+//    score work, which it has room for (the page is HBM-bound), and in
+//    exchange the 128 softmax threads each read a different slice of a row
+//    (64 R / 128 key columns) from TMEM in one load; the row max goes through
+//    a small table of the four warps' maxima (one meeting per page).
 //  * Each SM loads whole pages (72 KB, 9 boxes of 64 dims), three stages.
+//    With R = 16 two score tiles fit in TMEM beside Q and O^T; with R = 32
+//    one does (the next page's scores wait for this page's to be read).
 // The plan gives each cluster (CTA pair) a page range, as for the general
 // kernel; here the two CTAs take alternate pages of it and each runs its own
 // online softmax.  At the end of an entry they merge: each writes the other's
 // half of its O^T and its row statistics into rows of the split-partial
-// workspace that a plan of at most 16 rows never uses (see rec_ptr), and
+// workspace that a plan of at most R rows never uses (see rec_ptr), and
 // signals the other through an mbarrier (release/acquire at cluster scope);
 // each then finishes its half of the output dims.  The result (final output,
 // or one partial per split) is exactly what the general kernel writes, so
@@ -34,9 +37,9 @@
 //
 // Warp roles: warps 0-3 softmax, merge and epilogue (thread w * 32 + l owns
 // TMEM lane w * 32 + l), warp 4 the TMA producer, warp 5 the score MMA issuer
-// and TMEM owner, warp 6 the P.V MMA issuer.  Every wait is bounded (globaltimer): on expiry the kernel
-// records MLA_ERR_DEVICE_TIMEOUT, tells the peer CTA, lets in-flight copies
-// land, frees TMEM and returns.
+// and TMEM owner, warp 6 the P.V MMA issuer.  Every wait is bounded
+// (globaltimer): on expiry the kernel records MLA_ERR_DEVICE_TIMEOUT, tells
+// the peer CTA, lets in-flight copies land, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -58,34 +61,48 @@ constexpr int kNSoftThreads = 32 * kNSoftWarps;
 constexpr int kNProducerWarp = 4;
 constexpr int kNMmaWarp = 5;      // score MMAs; owns TMEM
 constexpr int kNPvWarp = 6;       // P.V MMAs
-constexpr int kNRows = 16;                    // query rows (TMEM lane m holds row m % 16)
 constexpr uint64_t kNWaitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kNDrainNs = 2000000ull;    // settle time after an abort
 constexpr float kNRescale = 8.0f;             // log2 units
 constexpr float kNLn2 = 0.69314718055994530942f;
 
-// Shared memory (offsets from a 1024-byte aligned base).
+// Shared memory (offsets from a 1024-byte aligned base): three whole-page
+// stages (72 KB each: nine 64-key x 64-dim boxes, 128-byte swizzle).
 constexpr int kNStages = 3;
 constexpr uint32_t kNBox = 8192;                        // 64 keys x 64 dims bf16, 128-byte swizzle
 constexpr uint32_t kNBoxes = kDqk / 64;                 // 9
 constexpr uint32_t kNStageBytes = kNBoxes * kNBox;      // one whole page
-constexpr uint32_t kNP = kNStages * kNStageBytes;       // 2 x P^T tile: 16 rows x 64 keys bf16
-constexpr uint32_t kNPBytes = 2048;
-constexpr uint32_t kNPmax = kNP + 2 * kNPBytes;         // 2 x float[16 rows][4 warps] page maxima
-constexpr uint32_t kNFac = kNPmax + 512;                // float[2][16] merge factors (with 1/l)
-constexpr uint32_t kNSums = kNFac + 128;                // float[2][16 rows][8 threads] l, lb
-constexpr uint32_t kNFlag = kNSums + 2 * 16 * 8 * 4;    // u32: the peer's records hold an O
-constexpr uint32_t kNBar = kNFlag + 16;
-constexpr uint32_t kNMisc = kNBar + 8 * 24;             // TMEM slot, abort flag
-constexpr uint32_t kNSmemAlloc = kNMisc + 16 + 1024;
-static_assert(kNP % 1024 == 0 && kNStageBytes % 1024 == 0, "swizzled buffers need 1 KB alignment");
-static_assert(kNSmemAlloc <= 232448, "shared memory");
-
-// TMEM columns.
 constexpr uint32_t kNTmemCols = 512;
-constexpr uint32_t kNColQ = 0;     // [0, 288): Q, bf16x2, row m % 16 in lane m
-constexpr uint32_t kNColS = 320;   // two 64-column score tiles
-constexpr uint32_t kNColO = 448;   // O^T: value dims 128 j + lane, column 16 j + row
+constexpr uint32_t kNColQ = 0;                          // [0, 288): Q, bf16x2
+constexpr uint32_t kNColS = 320;                        // score tiles, 64 columns each
+
+// Everything that depends on the row count R (16 or 32).
+template <int kR>
+struct NShape {
+  static_assert(kR == 16 || kR == 32, "16 or 32 query rows");
+  static constexpr int kSlots = kNSoftThreads / kR;      // softmax threads per row (= kRep)
+  static constexpr int kCols = 64 / kSlots;              // key columns per thread and page
+  static constexpr int kSBufs = kR == 16 ? 2 : 1;        // score tiles in TMEM
+  static constexpr uint32_t kColO = kR == 16 ? 448 : 384;   // O^T: 4 R columns
+  static constexpr uint32_t kPBytes = (uint32_t)kR * 128u;  // P^T tile: R rows x 64 keys bf16
+  static constexpr uint32_t kP = kNStages * kNStageBytes;   // 2 P^T tiles
+  static constexpr uint32_t kPmax = kP + 2 * kPBytes;       // 2 x float[R][4 warps] page maxima
+  static constexpr uint32_t kFlag = kPmax + 2 * (uint32_t)kR * 16u;   // u32: the peer has an O
+  static constexpr uint32_t kBar = kFlag + 16;
+  static constexpr uint32_t kMisc = kBar + 8 * 24;          // TMEM slot, abort flag
+  static constexpr uint32_t kSmemAlloc = kMisc + 16 + 1024;
+  // merge-time tables, in the P^T tiles (no P.V reads them then, and no
+  // probabilities of the next entry are written before the merge ends)
+  static constexpr uint32_t kSums = kP;                     // float[2][R][kSlots] l, lb
+  static constexpr uint32_t kFac = kP + 1024;               // float[2][R] merge factors
+  // merge records: rows [R, 128) of each 4-dim group of a partial slot
+  static constexpr int kRecPerGroup = (kTileRows - kR) * 4 / kR;
+  static_assert(kColO + 4 * kR <= kNTmemCols && kNColS + 64 * kSBufs <= kColO, "TMEM columns");
+  static_assert(kP % 1024 == 0 && kPBytes % 1024 == 0, "swizzled buffers need 1 KB alignment");
+  static_assert(2 * kPBytes >= 1024 + 8 * kR, "merge tables fit in the P^T tiles");
+  static_assert(kSmemAlloc <= 232448, "shared memory");
+  static_assert(259 / kRecPerGroup < kDv / 4, "merge records fit in the unused rows");
+};
 
 enum NBar : uint32_t {
   N_FULL = 0,                 // [3] page loaded (TMA tx)
@@ -105,23 +122,25 @@ enum NBar : uint32_t {
 static_assert(N_COUNT <= 24, "barrier space");
 
 // Merge records: sender rank r of cluster c writes into partial slot 2c + r,
-// in the rows [16, 128) of each group of four dims that a plan of <= 16 rows
-// never uses.  Record k (16 floats) sits in dim group k / 28 at row
-// 16 + 4 (k % 28).  Records 0-255: O^T of the receiver's 256 dims (relative
-// dim order), one row per float; 256-258: the sender's row max, sum of the
-// fp32 probabilities and sum of the bf16 probabilities; 259: flag (float 1 if
-// the sender had pages of the entry).
-constexpr int kRecPerGroup = 28;
+// in the rows [R, 128) of each group of four dims, which a plan of at most R
+// rows never uses.  Record k (R floats, one per row) sits in dim group
+// k / kRecPerGroup after the group's first R rows.  Records 0-255: O^T of the
+// receiver's 256 dims (relative dim order); 256-258: the sender's row max,
+// sum of the fp32 probabilities and sum of the bf16 probabilities; 259: flag
+// (float 1 if the sender had pages of the entry).
 constexpr int kRecMax = 256, kRecL = 257, kRecLb = 258, kRecFlag = 259;
+template <int kR>
 __device__ __forceinline__ float* rec_ptr(float* ws_o, int cluster, uint32_t sender, int k) {
+  constexpr int kPer = NShape<kR>::kRecPerGroup;
   return ws_o + (int64_t)(2 * cluster + (int)sender) * kSlotFloats +
-         (int64_t)(k / kRecPerGroup) * (kTileRows * 4) + 64 + (k % kRecPerGroup) * 16;
+         (int64_t)(k / kPer) * (kTileRows * 4) + 4 * kR + (k % kPer) * kR;
 }
 
 struct NCtx {
   uint32_t sbase, tmem, rank, peer, abort_addr, peer_abort_addr;
+  uint32_t bar0;   // the first mbarrier
   int* err;
-  __device__ __forceinline__ uint32_t bar(uint32_t i) const { return sbase + kNBar + 8u * i; }
+  __device__ __forceinline__ uint32_t bar(uint32_t i) const { return bar0 + 8u * i; }
 };
 
 __device__ __forceinline__ void n_abort(const NCtx& x) {
@@ -247,7 +266,9 @@ __device__ __forceinline__ bool n_producer(const NCtx& x, const NWork& w, const 
 //
 // Score issuer: S(g) = Q K^T once page g is loaded, its score tile is free
 // and the entry's Q is in TMEM.
+template <int kR>
 __device__ __forceinline__ bool n_mma_s(const NCtx& x, const NWork& w) {
+  using S = NShape<kR>;
   constexpr uint32_t id_s = ptx::idesc_bf16_f32(128, 64, 0, 0);
   OwnPages sc;
   sc.init(w, x.rank);
@@ -256,17 +277,19 @@ __device__ __forceinline__ bool n_mma_s(const NCtx& x, const NWork& w) {
     const uint32_t g = sc.g, s = g % kNStages;
     if (sc.k == 0 && !n_wait_warp(x, x.bar(N_QFULL), sq & 1u)) return false;
     if (!n_wait_warp(x, x.bar(N_FULL + s), (g / kNStages) & 1u)) return false;
-    if (g >= 2 && !n_wait_warp(x, x.bar(N_SEMPTY + (g & 1u)), ((g >> 1) & 1u) ^ 1u)) return false;
+    // the score tile is free once the softmax has read the page that used it
+    const uint32_t sb = g % S::kSBufs, su = g / S::kSBufs;
+    if (su >= 1 && !n_wait_warp(x, x.bar(N_SEMPTY + sb), (su & 1u) ^ 1u)) return false;
     ptx::tc_fence_after();
     const uint32_t st = x.sbase + s * kNStageBytes;
-    const uint32_t d_s = x.tmem + kNColS + (g & 1u) * 64u;
+    const uint32_t d_s = x.tmem + kNColS + sb * 64u;
 #pragma unroll
     for (uint32_t kk = 0; kk < 4 * kNBoxes; ++kk) {
       const uint64_t bd =
           ptx::smem_desc(st + (kk >> 2) * kNBox + (kk & 3u) * 32u, 16, 1024, ptx::kLayoutSw128);
       ptx::mma_ts_elect(d_s, x.tmem + kNColQ + 8u * kk, bd, id_s, kk ? 1u : 0u);
     }
-    ptx::mma_commit_elect(x.bar(N_SFULL + (g & 1u)));
+    ptx::mma_commit_elect(x.bar(N_SFULL + sb));
     if (sc.k == sc.n_own - 1) {
       ptx::mma_commit_elect(x.bar(N_QEMPTY));
       ++sq;
@@ -279,8 +302,10 @@ __device__ __forceinline__ bool n_mma_s(const NCtx& x, const NWork& w) {
 // P.V issuer: O^T += V^T P^T once page g's probabilities are written; its
 // commit hands the stage back to the producer and the P^T buffer to the
 // softmax warps.
+template <int kR>
 __device__ __forceinline__ bool n_mma_o(const NCtx& x, const NWork& w) {
-  constexpr uint32_t id_o = ptx::idesc_bf16_f32(128, kNRows, 1, 0);   // A = V^T, M/N-major
+  using S = NShape<kR>;
+  constexpr uint32_t id_o = ptx::idesc_bf16_f32(128, kR, 1, 0);   // A = V^T, M/N-major
   OwnPages oc;
   oc.init(w, x.rank);
   while (oc.valid) {
@@ -289,7 +314,7 @@ __device__ __forceinline__ bool n_mma_o(const NCtx& x, const NWork& w) {
     ptx::tc_fence_after();
     const bool first = (oc.k == 0);
     const uint32_t st = x.sbase + (gp % kNStages) * kNStageBytes;
-    const uint32_t pt = x.sbase + kNP + (gp & 1u) * kNPBytes;
+    const uint32_t pt = x.sbase + S::kP + (gp & 1u) * S::kPBytes;
 #pragma unroll
     for (uint32_t mb = 0; mb < 4; ++mb) {
 #pragma unroll
@@ -298,9 +323,10 @@ __device__ __forceinline__ bool n_mma_o(const NCtx& x, const NWork& w) {
         // apart along M), keys [16 k, +16): two 8-key groups 1 KB apart
         const uint64_t ad =
             ptx::smem_desc(st + 2u * mb * kNBox + k * 2048u, kNBox, 1024, ptx::kLayoutSw128);
-        // P^T: 16 rows of 64 keys (128 bytes), 8-row groups 1 KB apart
+        // P^T: R rows of 64 keys (128 bytes), 8-row groups 1 KB apart
         const uint64_t bd = ptx::smem_desc(pt + k * 32u, 16, 1024, ptx::kLayoutSw128);
-        ptx::mma_ss_elect(x.tmem + kNColO + 16u * mb, ad, bd, id_o, (first && k == 0) ? 0u : 1u);
+        ptx::mma_ss_elect(x.tmem + S::kColO + (uint32_t)kR * mb, ad, bd, id_o,
+                          (first && k == 0) ? 0u : 1u);
       }
     }
     ptx::mma_commit_elect(x.bar(N_EMPTY + gp % kNStages));
@@ -311,22 +337,28 @@ __device__ __forceinline__ bool n_mma_o(const NCtx& x, const NWork& w) {
 }
 
 // ------------------------------------------------------------------ softmax
-// Thread (warp q, lane l): TMEM lane 32 q + l, query row i = l % 16; key
-// columns [16 q + 8 (l / 16), +8) of every page; in the merge and epilogue,
-// value dims 128 j + 32 q + l.
+// Thread (warp q, lane l), TMEM lane t = 32 q + l: query row i = l % R, slot
+// t / R of the row's 128 / R threads, key columns [slot * cols, +cols) of
+// every page (cols = 64 R / 128); in the merge and epilogue, value dims
+// 128 j + t.
+template <int kR>
 __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const DecodeParams& prm,
                                           int warp, int lane) {
-  const int i = lane & 15;
-  const int half = lane >> 4;
-  const int col0 = 16 * warp + 8 * half;                  // this thread's 8 key columns
+  using S = NShape<kR>;
+  constexpr int kC = S::kCols;
   const int tl = 32 * warp + lane;                        // TMEM lane
+  const int i = lane % kR;                                // query row
+  const int slot = tl / kR;
+  const int col0 = slot * kC;                             // this thread's key columns
   const uint32_t lanes = (uint32_t)(32 * warp) << 16;
   const int R = prm.s_q * prm.h_q;
   const bool valid = i < R;
   const int qi = valid ? i / prm.h_q : 0;
   const float sl2 = prm.scale_log2;
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(prm.q);
-  const uint32_t prow = (uint32_t)i * 128u + ((((uint32_t)col0 >> 3) ^ ((uint32_t)i & 7u)) << 4);
+  // P^T row i, 16-byte chunks col0 / 8 .. (128-byte swizzle)
+  const uint32_t prow = (uint32_t)i * 128u;
+  const uint32_t pswz = (uint32_t)i & 7u;
   const uint32_t peer_merge = ptx::map_to_rank(x.bar(N_MERGE), x.peer);
   const uint32_t peer_mfree = ptx::map_to_rank(x.bar(N_MFREE), x.peer);
 
@@ -334,9 +366,9 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
   int b, pb, pe;
   uint32_t g = 0, nq = 0, n_item = 0, uses = 0;
   // Q row i of entry qb into this lane's 288 columns, once the previous
-  // entry's last score MMA is done (two rounds of 40 and 32 loads in flight).  The
-  // next entry's Q is loaded before this entry's merge, so its first score
-  // MMA runs while the merge does.
+  // entry's last score MMA is done (two rounds of 40 and 32 loads in
+  // flight).  The next entry's Q is loaded before this entry's merge, so its
+  // first score MMA runs while the merge does.
   auto load_q = [&](int qb) -> bool {
     if (!n_wait_warp(x, x.bar(N_QEMPTY), (nq & 1u) ^ 1u)) return false;
     const uint4* src = reinterpret_cast<const uint4*>(q + ((int64_t)qb * R + (valid ? i : 0)) * kDqk);
@@ -379,17 +411,24 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
 
     for (int k = 0; k < n_own; ++k, ++g) {
       const int pg = pb + (int)x.rank + 2 * k;
-      const uint32_t sb = g & 1u;
-      if (!n_wait_warp(x, x.bar(N_SFULL + sb), (g >> 1) & 1u)) return false;
+      const uint32_t pbf = g & 1u;                          // P^T tile and page-max table
+      const uint32_t sb = g % S::kSBufs, su = g / S::kSBufs;   // score tile and its use
+      if (!n_wait_warp(x, x.bar(N_SFULL + sb), su & 1u)) return false;
       ptx::tc_fence_after();
-      float mine[8];
-      {
-        uint32_t v8[8];
+      float mine[kC];
+      if constexpr (kR == 16) {
         // lanes 32 q + [0, 16) (rows 0-15): columns 16 q + [0, 8) to the
         // first half-warp, 16 q + [8, 16) to the second
+        uint32_t v8[8];
         ptx::tmem_ld16x2_x8_wait<8>(x.tmem + lanes + kNColS + sb * 64u + 16u * (uint32_t)warp, v8);
 #pragma unroll
         for (int j = 0; j < 8; ++j) mine[j] = __uint_as_float(v8[j]);
+      } else {
+        // this lane (row l), columns 16 q + [0, 16)
+        uint32_t v16[16];
+        ptx::tmem_ld32x16_wait(x.tmem + lanes + kNColS + sb * 64u + 16u * (uint32_t)warp, v16);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mine[j] = __uint_as_float(v16[j]);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -397,21 +436,22 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
       // keys past the row's visible count get no weight
       const int t0 = pg * kPageTokens + col0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < kC; ++j)
         if (t0 + j >= n_valid) mine[j] = -INFINITY;
-      // Row max of the page: this thread's 8 columns, its half-warp partner's
-      // 8, then the four warps' 16-column maxima through shared memory
-      // (double buffered by page parity, one meeting per page).
-      float pm = fmaxf(ptx::max3(mine[0], mine[1], mine[2]),
-                       fmaxf(ptx::max3(mine[3], mine[4], mine[5]), fmaxf(mine[6], mine[7])));
-      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
-      const uint32_t pmax = x.sbase + kNPmax + sb * 256u;   // float[16 rows][4 warps]
-      if (half == 0) ptx::st_shared_u32(pmax + (uint32_t)(i * 4 + warp) * 4u, __float_as_uint(pm));
+      // Row max of the page: this thread's columns (and, for R = 16, its
+      // half-warp partner's), then the four warps' maxima through shared
+      // memory (double buffered by page parity, one meeting per page).
+      float pm = mine[0];
+#pragma unroll
+      for (int j = 1; j < kC; ++j) pm = fmaxf(pm, mine[j]);
+      if constexpr (kR == 16) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+      const uint32_t pmax = x.sbase + S::kPmax + pbf * (uint32_t)kR * 16u;   // float[R][4 warps]
+      if (lane < kR) ptx::st_shared_u32(pmax + (uint32_t)(i * 4 + warp) * 4u, __float_as_uint(pm));
       if (!n_sync(x, uses, lane)) return false;
       // Lazy rescale (log2 domain): the reference max of a row moves only when
       // its max grows by more than 2^8.  Each thread decides for its own row
-      // (all threads of a row read the same four numbers); lanes r and r + 16
-      // of every warp hold row r, so a rescale of any row is seen warp-wide.
+      // (all threads of a row read the same four numbers); every warp holds
+      // every row, so a rescale of any row is seen warp-wide.
       float a_own = 1.0f;
       bool resc = false;
       {
@@ -431,9 +471,9 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
       l_run *= a_own;
       lb_run *= a_own;
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      uint32_t pk[4];
+      uint32_t pk[kC / 2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kC / 2; ++j) {
         const float a = ptx::ex2(fmaf(mine[2 * j], sl2, neg_m));
         const float c = ptx::ex2(fmaf(mine[2 * j + 1], sl2, neg_m));
         pk[j] = ptx::pack_bf16x2(a, c);
@@ -441,7 +481,7 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
         lb_run += __uint_as_float(pk[j] << 16) + __uint_as_float(pk[j] & 0xffff0000u);
       }
       // P^T buffer g % 2 is free once the P.V of page g - 2 is done
-      if (g >= 2 && !n_wait_warp(x, x.bar(N_PEMPTY + sb), ((g >> 1) & 1u) ^ 1u)) return false;
+      if (g >= 2 && !n_wait_warp(x, x.bar(N_PEMPTY + pbf), ((g >> 1) & 1u) ^ 1u)) return false;
       // Past the end of the sequence the last page's slots hold stale data:
       // their probabilities are 0, but 0 * NaN is NaN in the P.V MMA, so
       // zero those value rows first (latent boxes 0-7 of the stage).
@@ -454,29 +494,38 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
           ptx::st_shared_v4(st + box * kNBox + row * 128 + c16 * 16, 0u, 0u, 0u, 0u);
         }
       }
-      ptx::st_shared_v4(x.sbase + kNP + sb * kNPBytes + prow, pk[0], pk[1], pk[2], pk[3]);
-      ptx::fence_proxy_async_smem();
-      // O^T column r holds row r: rescale the columns whose factor is not 1
-      // (after the P.V of page g - 1 is done; this page's P.V waits for us)
-      if (any) {
-        float al[16];   // row r's factor, from lane r
+      {
+        const uint32_t pt = x.sbase + S::kP + pbf * S::kPBytes + prow;
 #pragma unroll
-        for (int r = 0; r < kNRows; ++r) al[r] = __shfl_sync(0xffffffffu, a_own, r);
-        if (!n_wait_warp(x, x.bar(N_PEMPTY + (sb ^ 1u)), ((g - 1) >> 1) & 1u)) return false;
+        for (int c = 0; c < kC / 8; ++c) {
+          const uint32_t chunk = (uint32_t)(col0 / 8 + c);
+          ptx::st_shared_v4(pt + ((chunk ^ pswz) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                            pk[4 * c + 3]);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      // O^T column r (of each 128-dim block) holds row r: rescale the columns
+      // whose factor is not 1 (after the P.V of page g - 1 is done; this
+      // page's P.V waits for us)
+      if (any) {
+        float al[kR];   // row r's factor, from lane r
+#pragma unroll
+        for (int r = 0; r < kR; ++r) al[r] = __shfl_sync(0xffffffffu, a_own, r);
+        if (!n_wait_warp(x, x.bar(N_PEMPTY + (pbf ^ 1u)), ((g - 1) >> 1) & 1u)) return false;
         ptx::tc_fence_after();
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
+        for (int h2 = 0; h2 < 4 * kR / 32; ++h2) {
           uint32_t o[32];
-          ptx::tmem_ld32_wait(x.tmem + lanes + kNColO + 32u * (uint32_t)h2, o);
+          ptx::tmem_ld32_wait(x.tmem + lanes + S::kColO + 32u * (uint32_t)h2, o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al[j & 15]);
-          ptx::tmem_st32(x.tmem + lanes + kNColO + 32u * (uint32_t)h2, o);
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * al[j % kR]);
+          ptx::tmem_st32(x.tmem + lanes + S::kColO + 32u * (uint32_t)h2, o);
         }
         ptx::tmem_wait_st();
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(x.bar(N_PFULL + sb));
+      if (lane == 0) ptx::mbar_arrive(x.bar(N_PFULL + pbf));
     }
     // the next entry's Q (its first score MMA then overlaps this merge)
     int nb = 0, npb = 0, npe = 0;
@@ -486,22 +535,25 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
     // ---- merge with the peer, then this CTA's half of the output dims ----
     const bool has = n_own > 0;
     // O^T blocks 2 rank, 2 rank + 1 (this CTA's output dims) and the peer's two
-    float own[32], oth[32];
+    float own[2 * kR], oth[2 * kR];
     if (has) {
       // every P.V of the entry is done once the last page's is
       const uint32_t gl = g - 1;
       if (!n_wait_warp(x, x.bar(N_PEMPTY + (gl & 1u)), (gl >> 1) & 1u)) return false;
       ptx::tc_fence_after();
-      uint32_t v[32];
-      ptx::tmem_ld32_wait(x.tmem + lanes + kNColO + 32u * x.rank, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) own[j] = __uint_as_float(v[j]);
-      ptx::tmem_ld32_wait(x.tmem + lanes + kNColO + 32u * x.peer, v);
+      for (int h2 = 0; h2 < 2 * kR / 32; ++h2) {
+        uint32_t v[32];
+        ptx::tmem_ld32_wait(x.tmem + lanes + S::kColO + 2u * kR * x.rank + 32u * h2, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) oth[j] = __uint_as_float(v[j]);
+        for (int j = 0; j < 32; ++j) own[32 * h2 + j] = __uint_as_float(v[j]);
+        ptx::tmem_ld32_wait(x.tmem + lanes + S::kColO + 2u * kR * x.peer + 32u * h2, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) oth[32 * h2 + j] = __uint_as_float(v[j]);
+      }
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) own[j] = oth[j] = 0.f;
+      for (int j = 0; j < 2 * kR; ++j) own[j] = oth[j] = 0.f;
     }
     // the peer has read the records of my previous entry
     if (n_item > 0 && !n_wait_warp(x, x.bar(N_MFREE), (n_item - 1) & 1u, true)) return false;
@@ -509,45 +561,45 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
       // the peer's dims: blocks 2 peer, 2 peer + 1 -> records 0-255 (relative)
 #pragma unroll
       for (int jb = 0; jb < 2; ++jb) {
-        float4* rec = reinterpret_cast<float4*>(rec_ptr(prm.ws_o, w.cluster, x.rank, 128 * jb + tl));
+        float4* rec = reinterpret_cast<float4*>(rec_ptr<kR>(prm.ws_o, w.cluster, x.rank, 128 * jb + tl));
 #pragma unroll
-        for (int r4 = 0; r4 < 4; ++r4)
-          rec[r4] = make_float4(oth[16 * jb + 4 * r4], oth[16 * jb + 4 * r4 + 1],
-                                oth[16 * jb + 4 * r4 + 2], oth[16 * jb + 4 * r4 + 3]);
+        for (int r4 = 0; r4 < kR / 4; ++r4)
+          rec[r4] = make_float4(oth[kR * jb + 4 * r4], oth[kR * jb + 4 * r4 + 1],
+                                oth[kR * jb + 4 * r4 + 2], oth[kR * jb + 4 * r4 + 3]);
       }
     }
-    // the row sums over the row's 8 threads
-    ptx::st_shared_u32(x.sbase + kNSums + (uint32_t)(i * 8 + 2 * warp + half) * 4u, __float_as_uint(l_run));
-    ptx::st_shared_u32(x.sbase + kNSums + 512u + (uint32_t)(i * 8 + 2 * warp + half) * 4u,
+    // the row sums over the row's threads (in the P^T tiles, idle now)
+    ptx::st_shared_u32(x.sbase + S::kSums + (uint32_t)(i * S::kSlots + slot) * 4u, __float_as_uint(l_run));
+    ptx::st_shared_u32(x.sbase + S::kSums + 512u + (uint32_t)(i * S::kSlots + slot) * 4u,
                        __float_as_uint(lb_run));
     if (!n_sync(x, uses, lane)) return false;
     float l_tot = 0.f, lb_tot = 0.f;
-    if (warp == 0 && half == 0) {
+    if (tl < kR) {   // warp 0, lane = row
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        l_tot += __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + kNSums + (uint32_t)(i * 8 + j) * 4u));
-        lb_tot += __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + kNSums + 512u + (uint32_t)(i * 8 + j) * 4u));
+      for (int j = 0; j < S::kSlots; ++j) {
+        l_tot += __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + S::kSums + (uint32_t)(i * S::kSlots + j) * 4u));
+        lb_tot += __uint_as_float(ptx::ld_shared_u32_volatile(x.sbase + S::kSums + 512u + (uint32_t)(i * S::kSlots + j) * 4u));
       }
-      rec_ptr(prm.ws_o, w.cluster, x.rank, kRecMax)[i] = has ? m_ref : -INFINITY;
-      rec_ptr(prm.ws_o, w.cluster, x.rank, kRecL)[i] = l_tot;
-      rec_ptr(prm.ws_o, w.cluster, x.rank, kRecLb)[i] = lb_tot;
-      if (i == 0) rec_ptr(prm.ws_o, w.cluster, x.rank, kRecFlag)[0] = has ? 1.0f : 0.0f;
+      rec_ptr<kR>(prm.ws_o, w.cluster, x.rank, kRecMax)[i] = has ? m_ref : -INFINITY;
+      rec_ptr<kR>(prm.ws_o, w.cluster, x.rank, kRecL)[i] = l_tot;
+      rec_ptr<kR>(prm.ws_o, w.cluster, x.rank, kRecLb)[i] = lb_tot;
+      if (i == 0) rec_ptr<kR>(prm.ws_o, w.cluster, x.rank, kRecFlag)[0] = has ? 1.0f : 0.0f;
     }
     __threadfence();
     if (!n_sync(x, uses, lane)) return false;
     if (warp == 0 && lane == 0) ptx::mbar_arrive_cluster_release(peer_merge);
     if (!n_wait_warp(x, x.bar(N_MERGE), n_item & 1u, true)) return false;
 
-    // Row factors: both halves scaled to the common max, with 1/l.  Row
+    // Row factors: both halves scaled to the common max, with 1/l.  The row
     // threads of warp 0 also write lse.
     const int ns = w.items[b * kItemWords + 1];
     const bool direct = (ns == 1);
     const int sidx = (n_item == 0) ? w.split0 : 0;
-    const int64_t slot = (int64_t)w.items[b * kItemWords + 2] + sidx;   // one tile
-    if (warp == 0 && half == 0) {
-      const float m_p = __ldcg(rec_ptr(prm.ws_o, w.cluster, x.peer, kRecMax) + i);
-      const float l_p = __ldcg(rec_ptr(prm.ws_o, w.cluster, x.peer, kRecL) + i);
-      const float lb_p = __ldcg(rec_ptr(prm.ws_o, w.cluster, x.peer, kRecLb) + i);
+    const int64_t slot_o = (int64_t)w.items[b * kItemWords + 2] + sidx;   // one tile
+    if (tl < kR) {
+      const float m_p = __ldcg(rec_ptr<kR>(prm.ws_o, w.cluster, x.peer, kRecMax) + i);
+      const float l_p = __ldcg(rec_ptr<kR>(prm.ws_o, w.cluster, x.peer, kRecL) + i);
+      const float lb_p = __ldcg(rec_ptr<kR>(prm.ws_o, w.cluster, x.peer, kRecLb) + i);
       const float m_o = has ? m_ref : -INFINITY;
       const float m = fmaxf(m_o, m_p);
       const float fo = (m_o == -INFINITY) ? 0.f : ptx::ex2(m_o - m);
@@ -555,26 +607,26 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
       const float lt = l_tot * fo + l_p * fp;
       const float lbt = lb_tot * fo + lb_p * fp;
       const float inv = lbt > 0.f ? 1.0f / lbt : 0.f;
-      ptx::st_shared_u32(x.sbase + kNFac + 4u * (uint32_t)i, __float_as_uint(fo * inv));
-      ptx::st_shared_u32(x.sbase + kNFac + 64u + 4u * (uint32_t)i, __float_as_uint(fp * inv));
+      ptx::st_shared_u32(x.sbase + S::kFac + 4u * (uint32_t)i, __float_as_uint(fo * inv));
+      ptx::st_shared_u32(x.sbase + S::kFac + 4u * kR + 4u * (uint32_t)i, __float_as_uint(fp * inv));
       if (i == 0)
-        ptx::st_shared_u32(x.sbase + kNFlag,
-                           __ldcg(rec_ptr(prm.ws_o, w.cluster, x.peer, kRecFlag)) != 0.f ? 1u : 0u);
+        ptx::st_shared_u32(x.sbase + S::kFlag,
+                           __ldcg(rec_ptr<kR>(prm.ws_o, w.cluster, x.peer, kRecFlag)) != 0.f ? 1u : 0u);
       if (x.rank == 0 && valid) {
         const float lse_v = lt > 0.f ? (m + log2f(lt)) * kNLn2 : -INFINITY;
         const int hh = i - qi * prm.h_q;
         if (direct)
           prm.lse[((int64_t)b * prm.h_q + hh) * prm.s_q + qi] = lse_v;
         else
-          prm.ws_lse[slot * kTileRows + i] = lse_v;
+          prm.ws_lse[slot_o * kTileRows + i] = lse_v;
       }
     }
     if (!n_sync(x, uses, lane)) return false;
-    float fo[16], fp[16];
+    float fo[kR], fp[kR];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 a = ptx::ld_shared_v4u(x.sbase + kNFac + 16u * (uint32_t)j);
-      const uint4 c = ptx::ld_shared_v4u(x.sbase + kNFac + 64u + 16u * (uint32_t)j);
+    for (int j = 0; j < kR / 4; ++j) {
+      const uint4 a = ptx::ld_shared_v4u(x.sbase + S::kFac + 16u * (uint32_t)j);
+      const uint4 c = ptx::ld_shared_v4u(x.sbase + S::kFac + 4u * kR + 16u * (uint32_t)j);
       fo[4 * j] = __uint_as_float(a.x);
       fo[4 * j + 1] = __uint_as_float(a.y);
       fo[4 * j + 2] = __uint_as_float(a.z);
@@ -584,15 +636,16 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
       fp[4 * j + 2] = __uint_as_float(c.z);
       fp[4 * j + 3] = __uint_as_float(c.w);
     }
-    const bool peer_has = ptx::ld_shared_u32_volatile(x.sbase + kNFlag) != 0u;
+    const bool peer_has = ptx::ld_shared_u32_volatile(x.sbase + S::kFlag) != 0u;
 #pragma unroll
     for (int jb = 0; jb < 2; ++jb) {
       const int mb = 2 * (int)x.rank + jb;
-      float op[16];
+      float op[kR];
       if (peer_has) {
-        const float4* rec = reinterpret_cast<const float4*>(rec_ptr(prm.ws_o, w.cluster, x.peer, 128 * jb + tl));
+        const float4* rec =
+            reinterpret_cast<const float4*>(rec_ptr<kR>(prm.ws_o, w.cluster, x.peer, 128 * jb + tl));
 #pragma unroll
-        for (int r4 = 0; r4 < 4; ++r4) {
+        for (int r4 = 0; r4 < kR / 4; ++r4) {
           const float4 v4 = __ldcg(rec + r4);
           op[4 * r4] = v4.x;
           op[4 * r4 + 1] = v4.y;
@@ -601,13 +654,13 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) op[j] = 0.f;
+        for (int j = 0; j < kR; ++j) op[j] = 0.f;
       }
       const int d = 128 * mb + tl;
 #pragma unroll
-      for (int r = 0; r < kNRows; ++r) {
+      for (int r = 0; r < kR; ++r) {
         if (r >= R) break;
-        const float val = own[16 * jb + r] * fo[r] + op[r] * fp[r];
+        const float val = own[kR * jb + r] * fo[r] + op[r] * fp[r];
         if (direct) {
           const int64_t oi = ((int64_t)b * R + r) * kDv + d;
           if (prm.out_f32)
@@ -615,11 +668,12 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
           else
             static_cast<__nv_bfloat16*>(prm.out)[oi] = __float2bfloat16_rn(val);
         } else {
-          prm.ws_o[slot * kSlotFloats + (int64_t)(d >> 2) * (kTileRows * 4) + r * 4 + (d & 3)] = val;
+          prm.ws_o[slot_o * kSlotFloats + (int64_t)(d >> 2) * (kTileRows * 4) + r * 4 + (d & 3)] = val;
         }
       }
     }
-    // my reads of the peer's records are done
+    // my reads of the peer's records (and of the tables in the P^T tiles)
+    // are done
     if (!n_sync(x, uses, lane)) return false;
     if (warp == 0 && lane == 0) ptx::mbar_arrive_cluster_release(peer_mfree);
     ++n_item;
@@ -631,18 +685,21 @@ __device__ __forceinline__ bool n_softmax(const NCtx& x, const NWork& w, const D
   return true;
 }
 
+template <int kR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNThreads, 1)
     mla_decode_narrow_kernel(const __grid_constant__ CUtensorMap tm_kv, const DecodeParams prm) {
+  using S = NShape<kR>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   NCtx x;
   x.sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
   x.rank = ptx::cluster_ctarank();
   x.peer = x.rank ^ 1u;
-  x.abort_addr = x.sbase + kNMisc + 4;
+  x.bar0 = x.sbase + S::kBar;
+  x.abort_addr = x.sbase + S::kMisc + 4;
   x.peer_abort_addr = ptx::map_to_rank(x.abort_addr, x.peer);
   x.err = prm.err;
-  const uint32_t tmem_slot = x.sbase + kNMisc;
+  const uint32_t tmem_slot = x.sbase + S::kMisc;
   const int cluster = (int)(blockIdx.x >> 1);
 
   if (threadIdx.x == 0) {
@@ -679,7 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // The plan must describe this call (one tile: at most 16 query rows).
+  // The plan must describe this call (one tile: at most R query rows).
   const int32_t* plan = prm.plan;
   NWork w = {};
   bool has_work = false;
@@ -689,7 +746,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNThreads, 1)
   const int e_b0 = cl[0], e_p0 = cl[1], e_b1 = cl[2], e_p1 = cl[3], e_s0 = cl[4];
   if (plan[H_MAGIC] != kPlanMagic || plan[H_BATCH] != prm.batch || plan[H_SQ] != prm.s_q ||
       plan[H_HQ] != prm.h_q || plan[H_NCLUSTERS] != nclusters || plan[H_GT] != gt_l ||
-      plan[H_TILES] != 1 || gt_l <= 0 || prm.s_q * prm.h_q > kNRows) {
+      plan[H_TILES] != 1 || gt_l <= 0 || prm.s_q * prm.h_q > kR) {
     if (threadIdx.x == 0 && x.rank == 0) atomicCAS(prm.err, 0, MLA_ERR_PLAN);
   } else if (cluster < plan[H_GUSED]) {
     w.b0 = e_b0;
@@ -713,13 +770,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNThreads, 1)
     if (lane == 0) n_producer(x, w, prm, &tm_kv);
     __syncwarp();
   } else if (warp == kNMmaWarp) {
-    n_mma_s(x, w);   // whole warp: one elected lane issues
+    n_mma_s<kR>(x, w);   // whole warp: one elected lane issues
     __syncwarp();
   } else if (warp == kNPvWarp) {
-    n_mma_o(x, w);
+    n_mma_o<kR>(x, w);
     __syncwarp();
   } else {
-    n_softmax(x, w, prm, warp, lane);
+    n_softmax<kR>(x, w, prm, warp, lane);
     __syncwarp();
   }
 
@@ -752,42 +809,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNThreads, 1)
 
 }  // namespace
 
-// At most 16 query rows, and enough pages for the CTA pair's per-entry merge
+// At most 32 query rows, and enough pages for the CTA pair's per-entry merge
 // (about 3 us: the partial O^T through L2 and a handshake) to pay off: the
 // pair runs a cluster's pages about 1.7x faster than the general kernel, so
 // calls whose block table holds at most 4 pages per cluster (latency-bound
 // either way) stay on the general kernel.
 bool narrow_decode_shape(int s_q, int h_q, int batch, int max_pages, int num_clusters) {
-  return s_q * h_q <= kNRows && (int64_t)batch * max_pages > 4 * (int64_t)num_clusters;
+  return s_q * h_q <= 32 && (int64_t)batch * max_pages > 4 * (int64_t)num_clusters;
 }
 
 cudaError_t narrow_kernel_setup() {
-  return cudaFuncSetAttribute(mla_decode_narrow_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kNSmemAlloc);
+  const cudaError_t e =
+      cudaFuncSetAttribute(mla_decode_narrow_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)NShape<16>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mla_decode_narrow_kernel<32>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)NShape<32>::kSmemAlloc);
 }
 
 int narrow_max_clusters() {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * 1024, 1, 1);
-  cfg.blockDim = dim3(kNThreads, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)kNSmemAlloc;
-  int m = 0;
-  return cudaOccupancyMaxActiveClusters(&m, mla_decode_narrow_kernel, &cfg) == cudaSuccess ? m : -1;
+  int n = -1;
+  for (int k = 0; k < 2; ++k) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 1024, 1, 1);
+    cfg.blockDim = dim3(kNThreads, 1, 1);
+    cfg.dynamicSmemBytes = k == 0 ? (size_t)NShape<16>::kSmemAlloc : (size_t)NShape<32>::kSmemAlloc;
+    int m = 0;
+    const cudaError_t e = k == 0 ? cudaOccupancyMaxActiveClusters(&m, mla_decode_narrow_kernel<16>, &cfg)
+                                 : cudaOccupancyMaxActiveClusters(&m, mla_decode_narrow_kernel<32>, &cfg);
+    if (e != cudaSuccess) return -1;
+    n = (n < 0 || m < n) ? m : n;
+  }
+  return n;
 }
 
 cudaError_t launch_decode_narrow(const CUtensorMap& kv_map, const DecodeParams& p, int num_clusters,
                                  cudaStream_t stream) {
+  const bool r16 = p.s_q * p.h_q <= 16;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_clusters);
   cfg.blockDim = dim3(kNThreads);
-  cfg.dynamicSmemBytes = kNSmemAlloc;
+  cfg.dynamicSmemBytes = r16 ? NShape<16>::kSmemAlloc : NShape<32>::kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_decode_narrow_kernel, kv_map, p);
+  return r16 ? cudaLaunchKernelEx(&cfg, mla_decode_narrow_kernel<16>, kv_map, p)
+             : cudaLaunchKernelEx(&cfg, mla_decode_narrow_kernel<32>, kv_map, p);
 }
 
 }  // namespace mla

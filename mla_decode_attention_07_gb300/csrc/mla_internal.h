@@ -51,7 +51,7 @@ cudaError_t launch_wait_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_decode(const TensorMaps& maps, const DecodeParams& p, int num_clusters,
                           cudaStream_t stream);
 
-// Decode kernel for at most 16 query rows per entry (mla_decode_narrow_sm103.cu):
+// Decode kernel for at most 32 query rows per entry (mla_decode_narrow_sm103.cu):
 // the same plan, partials and combine as the general kernel.  launch_decode
 // routes dense calls to it when narrow_decode_shape holds.
 bool narrow_decode_shape(int s_q, int h_q, int batch, int max_pages, int num_clusters);

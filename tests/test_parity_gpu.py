@@ -117,6 +117,13 @@ SMALL = [
     # fewer rows than the narrow kernel's 16: one head, and four heads
     (127, 3, 1, 1, [9000, 70, 30000], 1),
     (128, 2, 1, 4, [20000, 15000], 0),
+    # 17 to 32 rows: the narrow kernel's 32-row form (two speculative tokens
+    # of 16 heads with a row that sees no key, 32 heads, 3 tokens x 8 heads,
+    # many short entries)
+    (129, 4, 2, 16, [1, 700, 5000, 20000], 1),
+    (130, 3, 1, 32, [30000, 64, 129], 0),
+    (131, 2, 3, 8, [25000, 17], 1),
+    (132, 200, 2, 16, list(W.uniform_int(132, W.TENSOR_SEQLENS, 200, 1, 300)), 0),
 ]
 
 
@@ -149,9 +156,9 @@ def test_narrow_cases_take_the_narrow_kernel(torch_cuda):
     for seed, B, s_q, h_q, seqlens, extra in SMALL:
         inp = W.make_inputs(seed, B, s_q, h_q, seqlens, extra_pages=extra)
         kind = libmla.mla_decode_kernel_kind(B, s_q, h_q, int(inp.block_table.shape[1]))
-        want = s_q * h_q <= 16 and B * inp.block_table.shape[1] > 4 * nc
+        want = s_q * h_q <= 32 and B * inp.block_table.shape[1] > 4 * nc
         assert kind == (1 if want else 0), (seed, kind)
-        if seed in (117, 118, 119, 124, 127, 128):
+        if seed in (117, 118, 119, 124, 127, 128, 129, 130, 131, 132):
             assert kind == 1, seed
 
 
@@ -241,14 +248,16 @@ def test_deterministic_and_relabel_invariant(torch_cuda):
 
 
 @pytest.mark.parametrize("s_q,h_q,seqlens", [(1, 16, [12000, 7000]), (2, 8, [12000, 7000]),
+                                             (2, 16, [12000, 7000]),
                                              (1, 16, [3000, 1700]), (1, 128, [3000, 1700]),
                                              (2, 64, [3000, 1700])])
 def test_growing_scores_rescale(torch_cuda, oracle_mod, s_q, h_q, seqlens):
     """Scores that grow along the sequence (a rotary dim of every key set to
     a ramp, q's matching dim to 2) move the running max by more than the lazy
     rescale threshold many times per entry: O and the sums are rescaled on
-    the GPU (the narrow kernel for the first two, the general one for the
-    rest), and the result must still match the oracle."""
+    the GPU (the narrow kernel, 16- and 32-row forms, for the first three;
+    the general one for the rest), and the result must still match the
+    oracle."""
     inp = W.make_inputs(125, 2, s_q, h_q, seqlens, poison=False)
     d = W.D_QK - 1
     for b in range(inp.batch):
