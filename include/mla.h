@@ -266,8 +266,9 @@ int mla_cache_append(const void* kv_new, void* kv_cache, int num_pages,
  *   q_nope bf16 [batch, s_q, h_q, 128], q_rope bf16 [batch, s_q, h_q, 64],
  *   w_uk bf16 [h_q, 128, 512] (the key up-projection of each head),
  *   q bf16 [batch, s_q, h_q, 576]; all device, 16-byte aligned.
- * The contraction runs on the tensor cores as a GEMM batched over heads
- * (fp32 accumulation; q_latent rounded to bf16, nearest even).
+ * The contraction runs on the tensor cores, per head and taken transposed
+ * (latent dims x query rows; fp32 accumulation; q_latent rounded to bf16,
+ * nearest even).
  * Defined by: no passage (as mla_cache_append): DeepSeek MLA's absorbed
  * form, in which W_UK is folded into the query so that the scores are taken
  * against the 512-dim latent cache directly.

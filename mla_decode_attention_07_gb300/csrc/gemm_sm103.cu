@@ -2,17 +2,14 @@
 // MLA decode call: the new tokens' rows appended to the paged cache, and the
 // query absorbed through W_UK (a GEMM batched over heads).
 //
-// What the GEMM computes: C[b][m][n] = sum_k A[b][m][k] * B[b][k][n], A
-// K-contiguous and B N-contiguous, fp16 or bf16 inputs, fp32 accumulation on
-// the tensor cores, C stored as fp16, bf16 (round to nearest even) or fp32.
-// The GEMM tutorial summary ("Designing high-performance GPU kernels with
-// TileLang: Tensor-Core GEMM", its comparison table) measures exactly this
-// product in FP16 at 2048 x 2048 x 2048 against cuBLAS; the same kernel does
-// DeepSeek MLA's query absorption, q_latent[., h, :] = q_nope[., h, :] W_UK[h]
-// (d_nope 128 -> d_c 512 per head), with the heads as the batch; its
-// epilogue also copies each row's rotary part beside the latent part.
+// What the GEMM computes: C[m][n] = sum_k A[m][k] * B[k][n], A K-contiguous
+// and B N-contiguous, fp16 or bf16 inputs, fp32 accumulation on the tensor
+// cores, C stored as fp16, bf16 (round to nearest even) or fp32.  The GEMM
+// tutorial summary ("Designing high-performance GPU kernels with TileLang:
+// Tensor-Core GEMM", its comparison table) measures exactly this product in
+// FP16 at 2048 x 2048 x 2048 against cuBLAS.
 //
-// GB300 design:
+// GEMM design for GB300:
 //  * One CTA per SM, persistent over 128 x 256 output tiles.  Warp 0 issues
 //    the TMA loads (one elected lane), warp 1 owns TMEM and issues the MMAs
 //    (one elected lane of the converged warp), warps 2-5 drain accumulators
@@ -27,6 +24,20 @@
 //  * Every wait is bounded (2 s on %globaltimer): on expiry the kernel
 //    records MLA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land,
 //    frees TMEM and returns.  No trap.
+//
+// DeepSeek MLA's query absorption, q[r][h][0:512] = q_nope[r][h][:] W_UK[h]
+// (d_nope 128 -> d_c 512 per head) with q[r][h][512:576] = q_rope[r][h][:],
+// has its own kernel (mla_absorb_kernel, below).  A decode step has few
+// query rows per head (16 at batch 16), so the product is taken transposed,
+// q_latent^T = W_UK[h]^T q_nope^T: the 512 latent dims are the MMA's M (four
+// 128-row blocks) and the query rows its N (a multiple of 16, at most 128 per
+// tile), and no MMA row is spent on padding.  One CTA per (head, row tile);
+// W_UK[h] (128 KB) lands as eight 64-dim x 128-row boxes (the MN-major A
+// operand, 128-byte swizzle, read as stored) behind one barrier per M block,
+// so the first block's MMAs run while the rest arrive; the rows' q_nope is
+// the K-major B operand.  Its epilogue has one latent dim per thread (the
+// TMEM lane): a warp stores 32 consecutive dims (64 bytes) of a row at a
+// time, and copies the rows' rotary parts beside them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -63,9 +74,6 @@ struct GemmArgs {
   int M, N, K, batch, tiles_m, tiles_n;
   int out_type;             // MLA_DTYPE_F16 / BF16 / F32
   int* err;
-  // Query absorption only (else null): q_rope [M][batch][64] bf16, copied to
-  // the 64 elements that follow N in each row of C by the tiles with n = 0.
-  const uint4* rope;
 };
 
 struct GCtx {
@@ -245,15 +253,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int mt = rest % args.tiles_m, b = rest / args.tiles_m;
       const uint32_t acc = lt & 1u;
       const int row = mt * kBM + quad * 32 + lane;
-      // the row's rotary part (absorption, tiles with n = 0): loaded before
-      // the accumulator wait so that its latency overlaps the MMAs
-      const bool rope = args.rope != nullptr && nt == 0 && row < args.M;
-      uint4 rp[8];
-      if (rope) {
-        const uint4* src = args.rope + ((long long)row * args.batch + b) * 8;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) rp[j] = src[j];
-      }
       if (!gwait_warp(x, x.bar(G_ACC_FULL + acc), (lt >> 1) & 1u)) break;
       ptx::tc_fence_after();
       const int esize = args.out_type == MLA_DTYPE_F32 ? 4 : 2;
@@ -265,12 +264,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ptx::tmem_ld32_wait(tmem + ((uint32_t)(quad * 32) << 16) + acc * (uint32_t)kBN + ch * 32, v);
         const int n0 = nt * kBN + ch * 32;
         if (row < args.M && n0 < args.N) store_row32(args, crow, n0, v);
-      }
-      if (rope) {
-        // next to the row's absorbed latent part
-        uint4* dst = reinterpret_cast<uint4*>(crow + (long long)args.N * esize);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = rp[j];
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -318,6 +311,192 @@ __global__ void mla_cache_append_kernel(const uint4* __restrict__ kv_new, uint4*
   }
 }
 
+
+// ------------------------------------------------------------ absorption
+constexpr int kAbsNope = 128, kAbsC = 512;
+constexpr int kAbsMaxN = 128;                          // query rows per tile (TMEM: 4 x N columns)
+constexpr uint32_t kAbsWBox = 64 * kAbsNope * 2;      // 16 KB: 64 latent dims x 128 d_nope rows
+constexpr uint32_t kAbsQOff = 8 * kAbsWBox;            // 128 KB of W_UK[h], then the q_nope tile
+constexpr uint32_t kAbsStage = kAbsQOff + 2 * kAbsMaxN * 128;   // two output staging tiles
+constexpr uint32_t kAbsBar = kAbsStage + 2 * (2 * kAbsMaxN * 128);
+// barriers: FULL[4] (one per M block; block 0 also counts the q_nope tile),
+// SFREE (the MMAs are done with the operands), ACC_FULL, ACC_EMPTY
+constexpr int AB_FULL = 0, AB_SFREE = 4, AB_ACC_FULL = 5, AB_ACC_EMPTY = 6, AB_COUNT = 7;
+constexpr uint32_t kAbsMisc = kAbsBar + 8 * AB_COUNT;
+constexpr uint32_t kAbsSmem = kAbsMisc + 16 + 1024;
+static_assert(kAbsSmem <= 232448, "shared memory");
+
+struct AbsorbArgs {
+  uint16_t* q;              // bf16 [rows][heads][576]
+  const uint4* rope;        // bf16 [rows][heads][64] as 16-byte pieces
+  int rows, heads, n_tiles, nt;
+  int* err;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    mla_absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_out, const AbsorbArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  GCtx x;
+  x.sbase = (ptx::smem_addr(smem_raw) + 1023u) & ~1023u;
+  x.abort_addr = x.sbase + kAbsMisc + 4;
+  x.err = args.err;
+  const uint32_t tslot = x.sbase + kAbsMisc;
+  auto bar = [&](int i) { return x.sbase + kAbsBar + 8u * i; };
+  const int nt = args.nt;
+  const uint32_t qbox = (uint32_t)nt * 128u;          // one 64-deep K box of the row tile
+
+  if (threadIdx.x == 0) {
+    for (int m = 0; m < 4; ++m) ptx::mbar_init(bar(AB_FULL + m), 1);
+    ptx::mbar_init(bar(AB_SFREE), 1);
+    ptx::mbar_init(bar(AB_ACC_FULL), 1);
+    ptx::mbar_init(bar(AB_ACC_EMPTY), 4);
+    ptx::st_shared_u32(x.abort_addr, 0u);
+    ptx::fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tslot, kGTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tm_w);
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_out);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ptx::ld_shared_u32_volatile(tslot);
+  const int units = args.heads * args.n_tiles;
+
+  if (warp == 0) {
+    // TMA producer: a unit's operands, M block by M block
+    if (lane == 0) {
+      uint32_t lt = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+        const int h = u / args.n_tiles, j = u - h * args.n_tiles;
+        if (!gwait(x, bar(AB_SFREE), (lt & 1u) ^ 1u)) break;
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t fb = bar(AB_FULL + m);
+          ptx::mbar_arrive_expect_tx(fb, 2 * kAbsWBox + (m == 0 ? 2 * qbox : 0u));
+          if (m == 0) {
+            ptx::tma_load_3d(x.sbase + kAbsQOff, &tm_q, 0, h, j * nt, fb);
+            ptx::tma_load_3d(x.sbase + kAbsQOff + qbox, &tm_q, 64, h, j * nt, fb);
+          }
+          ptx::tma_load_3d(x.sbase + (2 * m) * kAbsWBox, &tm_w, 128 * m, 0, h, fb);
+          ptx::tma_load_3d(x.sbase + (2 * m + 1) * kAbsWBox, &tm_w, 128 * m + 64, 0, h, fb);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // MMA issuer: D[m] (128 latent dims x nt rows) = W^T (MN-major: 64-dim
+    // atoms 16 KB apart, 8-row groups 1024 B apart; a K step of 16 is 2 KB
+    // down the box) times q_nope^T (K-major, 128-byte swizzled rows).
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, nt, 1, 0);
+    uint32_t lt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
+      if (!gwait_warp(x, bar(AB_ACC_EMPTY), (lt & 1u) ^ 1u)) break;
+      ptx::tc_fence_after();
+      for (int m = 0; m < 4; ++m) {
+        if (!gwait_warp(x, bar(AB_FULL + m), lt & 1u)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kAbsNope / 16; ++k) {
+          const uint64_t ad = ptx::smem_desc(x.sbase + (2 * m) * kAbsWBox + k * 2048, kAbsWBox,
+                                             1024, ptx::kLayoutSw128);
+          const uint64_t bd = ptx::smem_desc(x.sbase + kAbsQOff + (k >> 2) * qbox + (k & 3) * 32,
+                                             16, 1024, ptx::kLayoutSw128);
+          ptx::mma_ss_elect(tmem + (uint32_t)(m * nt), ad, bd, idesc, k > 0 ? 1u : 0u);
+        }
+      }
+      if (!ok) break;
+      ptx::mma_commit_elect(bar(AB_SFREE));
+      ptx::mma_commit_elect(bar(AB_ACC_FULL));
+    }
+    __syncwarp();
+  } else {
+    // Epilogue: thread = latent dim 32 * quad + lane of each M block.  A
+    // block goes through a shared-memory tile (two 64-dim halves of nt rows
+    // x 128 bytes, double-buffered) and out by two TMA tensor stores, which
+    // skip the rows past the end; the rows' rotary parts are plain copies.
+    const int quad = warp & 3, et = threadIdx.x - 64;
+    const long long rstride = (long long)args.heads * kDqk;
+    const uint32_t my_col = (uint32_t)(quad >> 1) * qbox + (uint32_t)((quad & 1) * 32 + lane) * 2u;
+    uint32_t lt = 0, blk = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
+      const int h = u / args.n_tiles, j = u - h * args.n_tiles;
+      const int row0 = j * nt;
+      // the rows' rotary parts (8 pieces a row), loaded before the
+      // accumulator wait so that their latency overlaps the MMAs
+      uint4 rp[kAbsMaxN / 16];
+#pragma unroll
+      for (int i = 0; i < kAbsMaxN / 16; ++i) {
+        const int pc = et + 128 * i, r = row0 + (pc >> 3);
+        if (i < nt / 16 && r < args.rows) rp[i] = args.rope[((long long)r * args.heads + h) * 8 + (pc & 7)];
+      }
+      gwait_warp(x, bar(AB_ACC_FULL), lt & 1u);
+      // every epilogue warp comes here whether its wait succeeded or not, so
+      // the abort decision below is the same for all four
+      ptx::named_sync(1, 128);
+      if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) break;
+      ptx::tc_fence_after();
+      for (int m = 0; m < 4; ++m, ++blk) {
+        const uint32_t stg = x.sbase + kAbsStage + (blk & 1u) * 2u * qbox;
+        if (et == 0) ptx::bulk_wait_read<1>();   // the store that last read this buffer is done
+        ptx::named_sync(1, 128);
+        for (int c0 = 0; c0 < nt; c0 += 16) {
+          uint32_t v[16];
+          ptx::tmem_ld32x16_wait(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(m * nt + c0), v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint16_t b16 = (uint16_t)(ptx::pack_bf16x2(__uint_as_float(v[i]), 0.f) & 0xffffu);
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stg + my_col + (uint32_t)(c0 + i) * 128u),
+                         "h"(b16)
+                         : "memory");
+          }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_sync(1, 128);
+        if (et == 0) {
+          ptx::tma_store_3d(&tm_out, 128 * m, h, row0, stg);
+          ptx::tma_store_3d(&tm_out, 128 * m + 64, h, row0, stg + qbox);
+          ptx::bulk_commit();
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(AB_ACC_EMPTY));
+#pragma unroll
+      for (int i = 0; i < kAbsMaxN / 16; ++i) {
+        const int pc = et + 128 * i, r = row0 + (pc >> 3);
+        if (i < nt / 16 && r < args.rows)
+          reinterpret_cast<uint4*>(args.q + (long long)r * rstride + (long long)h * kDqk + kAbsC)[pc & 7] =
+              rp[i];
+      }
+    }
+    if (et == 0) ptx::bulk_wait_all();
+  }
+
+  __syncthreads();
+  if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < kGDrainNs) __nanosleep(1000);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kGTmemCols);
+  }
+}
+
 std::once_flag g_gemm_attr_once[64];
 cudaError_t g_gemm_attr_status[64];
 
@@ -329,6 +508,9 @@ cudaError_t gemm_setup(int device) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(mla_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kGSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mla_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kAbsSmem);
     g_gemm_attr_status[device] = e;
   });
   return g_gemm_attr_status[device];
@@ -401,34 +583,48 @@ int mla_q_absorb(const void* q_nope, const void* q_rope, const void* w_uk, void*
       (long long)batch * s_q * h_q >= (1ll << 31) || !aligned16(q_nope) || !aligned16(q_rope) ||
       !aligned16(w_uk) || !aligned16(q))
     return MLA_ERR_INVALID_ARG;
-  constexpr int kNope = 128, kC = 512, kRope = 64;
-  const long long rows = (long long)batch * s_q;
-  CUtensorMap ma, mb;
-  // A = q_nope [rows][h_q][128]: K contiguous, heads next, rows outermost
-  const uint64_t da[3] = {kNope, (uint64_t)h_q, (uint64_t)rows};
-  const uint64_t sa[2] = {kNope * 2, (uint64_t)h_q * kNope * 2};
-  const uint32_t ba[3] = {kBK, 1, kBM};
-  // B = W_UK [h_q][128][512]: N contiguous, K next, heads outermost
-  const uint64_t db[3] = {kC, kNope, (uint64_t)h_q};
-  const uint64_t sb[2] = {kC * 2, (uint64_t)kNope * kC * 2};
-  const uint32_t bb[3] = {64, kBK, 1};
-  if (!encode_tiled_map(&ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, da, sa, ba,
+  const int rows = batch * s_q;
+  // row tiles of equal size, a multiple of 16 and at most 128
+  const int n_tiles = (rows + kAbsMaxN - 1) / kAbsMaxN;
+  const int nt = ((rows + n_tiles - 1) / n_tiles + 15) / 16 * 16;
+  CUtensorMap mw, mq, mo;
+  // W_UK [h_q][128][512]: latent dims innermost, d_nope next, heads outermost
+  const uint64_t dw[3] = {kAbsC, kAbsNope, (uint64_t)h_q};
+  const uint64_t sw[2] = {kAbsC * 2, (uint64_t)kAbsNope * kAbsC * 2};
+  const uint32_t bw[3] = {64, kAbsNope, 1};
+  // q_nope [rows][h_q][128]: d_nope innermost, heads next, rows outermost
+  const uint64_t dq[3] = {kAbsNope, (uint64_t)h_q, (uint64_t)rows};
+  const uint64_t sq[2] = {kAbsNope * 2, (uint64_t)h_q * kAbsNope * 2};
+  const uint32_t bq[3] = {64, 1, (uint32_t)nt};
+  // q [rows][h_q][576] (stored into): dims innermost, heads next, rows outermost
+  const uint64_t dout[3] = {kDqk, (uint64_t)h_q, (uint64_t)rows};
+  const uint64_t sout[2] = {kDqk * 2, (uint64_t)h_q * kDqk * 2};
+  const uint32_t bout[3] = {64, 1, (uint32_t)nt};
+  if (!encode_tiled_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w_uk, dw, sw, bw,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_map(&mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, w_uk, db, sb, bb,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tiled_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_nope, dq, sq, bq,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dout, sout, bout,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
     return MLA_ERR_CUDA;
-  GemmArgs a = {};
-  a.c = q;                                  // the first 512 dims of each 576-wide row
-  a.ldc = (long long)h_q * kDqk;
-  a.c_batch = kDqk;
-  a.M = (int)rows;
-  a.N = kC;
-  a.K = kNope;
-  a.batch = h_q;
-  a.out_type = MLA_DTYPE_BF16;
+  int device = 0, sms = 0;
+  int* err = nullptr;
+  const int st = device_current(&device, &sms, &err);
+  if (st != MLA_OK) return st;
+  if (gemm_setup(device) != cudaSuccess) return MLA_ERR_CUDA;
+  AbsorbArgs a;
+  a.q = static_cast<uint16_t*>(q);
   a.rope = static_cast<const uint4*>(q_rope);
-  static_assert(kRope * 2 == 8 * 16, "the rotary part of a row is eight 16-byte pieces");
-  return launch_gemm(MLA_DTYPE_BF16, ma, mb, a, static_cast<cudaStream_t>(stream));
+  a.rows = rows;
+  a.heads = h_q;
+  a.n_tiles = n_tiles;
+  a.nt = nt;
+  a.err = err;
+  const long long units = (long long)h_q * n_tiles;
+  if (units >= (1ll << 31)) return MLA_ERR_INVALID_ARG;
+  const int grid = (int)(units < sms ? units : sms);
+  mla_absorb_kernel<<<grid, kGemmThreads, kAbsSmem, static_cast<cudaStream_t>(stream)>>>(mw, mq, mo, a);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 int mla_cache_append(const void* kv_new, void* kv_cache, int num_pages, const int32_t* block_table,

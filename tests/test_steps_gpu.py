@@ -85,6 +85,9 @@ ABSORB_CASES = [
     (313, 16, 1, 128),           # the batch-16 decode shape
     (314, 200, 1, 32),           # two row tiles, the second ragged
     (315, 132, 2, 128),          # the speculative decode shape: three row tiles
+    (317, 129, 1, 3),            # two row tiles of 80, the second ragged
+    (318, 1, 1, 1),              # one row, one head
+    (319, 300, 3, 4),            # 900 rows: eight tiles of 128, the last holding 4 rows
 ]
 
 
