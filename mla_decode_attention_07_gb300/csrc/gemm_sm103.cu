@@ -180,6 +180,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_u32_volatile(tslot);
+  // Launched as a programmatic dependent of the previous kernel on the
+  // stream: the set-up above overlaps its tail; its results (A, B) and its
+  // use of C are safe once it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int total = args.batch * args.tiles_m * args.tiles_n;
   const int kb_n = (args.K + kBK - 1) / kBK;
@@ -292,6 +297,8 @@ __global__ void mla_cache_append_kernel(const uint4* __restrict__ kv_new, uint4*
                                         int num_pages, const int32_t* __restrict__ block_table,
                                         int max_pages, const int32_t* __restrict__ seqlens,
                                         int s_q, long long pieces, int* err) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // as in mla_gemm_kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pieces;
        i += (long long)gridDim.x * blockDim.x) {
     const long long row = i / 72;
@@ -369,6 +376,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ptx::ld_shared_u32_volatile(tslot);
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // as in mla_gemm_kernel
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int units = args.heads * args.n_tiles;
 
   if (warp == 0) {
@@ -518,6 +527,25 @@ cudaError_t gemm_setup(int device) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch configuration with programmatic stream serialization: the kernel may
+// start while the previous one on the stream finishes, and waits for it
+// (griddepcontrol.wait) before touching global memory.
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(int grid, int threads, size_t smem, cudaStream_t stream) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
 // One batched GEMM launch.  A map: dims {K, batch, M}; B map: {N, K, batch}.
 int launch_gemm(int in_dtype, const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a,
                 cudaStream_t stream) {
@@ -532,11 +560,11 @@ int launch_gemm(int in_dtype, const CUtensorMap& ma, const CUtensorMap& mb, Gemm
   const long long total = (long long)a.batch * a.tiles_m * a.tiles_n;
   if (total >= (1ll << 31)) return MLA_ERR_INVALID_ARG;
   const int grid = (int)(total < sms ? total : sms);
-  if (in_dtype == MLA_DTYPE_BF16)
-    mla_gemm_kernel<1><<<grid, kGemmThreads, kGSmem, stream>>>(ma, mb, a);
-  else
-    mla_gemm_kernel<0><<<grid, kGemmThreads, kGSmem, stream>>>(ma, mb, a);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  PdlLaunch l(grid, kGemmThreads, kGSmem, stream);
+  const cudaError_t e = in_dtype == MLA_DTYPE_BF16
+                            ? cudaLaunchKernelEx(&l.cfg, mla_gemm_kernel<1>, ma, mb, a)
+                            : cudaLaunchKernelEx(&l.cfg, mla_gemm_kernel<0>, ma, mb, a);
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -623,8 +651,9 @@ int mla_q_absorb(const void* q_nope, const void* q_rope, const void* w_uk, void*
   const long long units = (long long)h_q * n_tiles;
   if (units >= (1ll << 31)) return MLA_ERR_INVALID_ARG;
   const int grid = (int)(units < sms ? units : sms);
-  mla_absorb_kernel<<<grid, kGemmThreads, kAbsSmem, static_cast<cudaStream_t>(stream)>>>(mw, mq, mo, a);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  PdlLaunch l(grid, kGemmThreads, kAbsSmem, static_cast<cudaStream_t>(stream));
+  return cudaLaunchKernelEx(&l.cfg, mla_absorb_kernel, mw, mq, mo, a) == cudaSuccess ? MLA_OK
+                                                                                      : MLA_ERR_CUDA;
 }
 
 int mla_cache_append(const void* kv_new, void* kv_cache, int num_pages, const int32_t* block_table,
@@ -641,10 +670,12 @@ int mla_cache_append(const void* kv_new, void* kv_cache, int num_pages, const in
   if (st != MLA_OK) return st;
   const long long pieces = (long long)batch * s_q * 72;
   const int grid = (int)((pieces + 255) / 256 < 2 * sms ? (pieces + 255) / 256 : 2 * sms);
-  mla_cache_append_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(kv_new), static_cast<uint4*>(kv_cache), num_pages, block_table,
-      max_pages, cache_seqlens, s_q, pieces, err);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  PdlLaunch l(grid, 256, 0, static_cast<cudaStream_t>(stream));
+  return cudaLaunchKernelEx(&l.cfg, mla_cache_append_kernel, static_cast<const uint4*>(kv_new),
+                            static_cast<uint4*>(kv_cache), num_pages, block_table, max_pages,
+                            cache_seqlens, s_q, pieces, err) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // extern "C"
