@@ -327,8 +327,10 @@ constexpr uint32_t kAbsQOff = 8 * kAbsWBox;            // 128 KB of W_UK[h], the
 constexpr uint32_t kAbsStage = kAbsQOff + 2 * kAbsMaxN * 128;   // two output staging tiles
 constexpr uint32_t kAbsBar = kAbsStage + 2 * (2 * kAbsMaxN * 128);
 // barriers: FULL[4] (one per M block; block 0 also counts the q_nope tile),
-// SFREE (the MMAs are done with the operands), ACC_FULL, ACC_EMPTY
-constexpr int AB_FULL = 0, AB_SFREE = 4, AB_ACC_FULL = 5, AB_ACC_EMPTY = 6, AB_COUNT = 7;
+// SFREE (the MMAs are done with the operands), ACC_FULL[4] (M block m's
+// accumulator is complete, so the epilogue drains it while later blocks'
+// operands still land), ACC_EMPTY
+constexpr int AB_FULL = 0, AB_SFREE = 4, AB_ACC_FULL = 5, AB_ACC_EMPTY = 9, AB_COUNT = 10;
 constexpr uint32_t kAbsMisc = kAbsBar + 8 * AB_COUNT;
 constexpr uint32_t kAbsSmem = kAbsMisc + 16 + 1024;
 static_assert(kAbsSmem <= 232448, "shared memory");
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (threadIdx.x == 0) {
     for (int m = 0; m < 4; ++m) ptx::mbar_init(bar(AB_FULL + m), 1);
     ptx::mbar_init(bar(AB_SFREE), 1);
-    ptx::mbar_init(bar(AB_ACC_FULL), 1);
+    for (int m = 0; m < 4; ++m) ptx::mbar_init(bar(AB_ACC_FULL + m), 1);
     ptx::mbar_init(bar(AB_ACC_EMPTY), 4);
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
@@ -405,6 +407,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // atoms 16 KB apart, 8-row groups 1024 B apart; a K step of 16 is 2 KB
     // down the box) times q_nope^T (K-major, 128-byte swizzled rows).
     const uint32_t idesc = ptx::idesc_bf16_f32(128, nt, 1, 0);
+    // one accumulator barrier per M block when every CTA has one unit (the
+    // epilogue drains the blocks as they finish), else one for the whole
+    // accumulator (extra commits between the blocks cost more than they give
+    // when the next unit's MMAs follow)
+    const bool per_block = units <= (int)gridDim.x;
     uint32_t lt = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++lt) {
@@ -424,10 +431,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                              16, 1024, ptx::kLayoutSw128);
           ptx::mma_ss_elect(tmem + (uint32_t)(m * nt), ad, bd, idesc, k > 0 ? 1u : 0u);
         }
+        if (per_block) ptx::mma_commit_elect(bar(AB_ACC_FULL + m));
       }
       if (!ok) break;
+      // the operands first: the next unit's loads start as early as possible
       ptx::mma_commit_elect(bar(AB_SFREE));
-      ptx::mma_commit_elect(bar(AB_ACC_FULL));
+      if (!per_block) ptx::mma_commit_elect(bar(AB_ACC_FULL + 3));
     }
     __syncwarp();
   } else {
@@ -438,6 +447,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quad = warp & 3, et = threadIdx.x - 64;
     const long long rstride = (long long)args.heads * kDqk;
     const uint32_t my_col = (uint32_t)(quad >> 1) * qbox + (uint32_t)((quad & 1) * 32 + lane) * 2u;
+    // the same choice as the MMA issuer's: per block, or the whole accumulator
+    const bool per_block = units <= (int)gridDim.x;
     uint32_t lt = 0, blk = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++lt) {
       const int h = u / args.n_tiles, j = u - h * args.n_tiles;
@@ -450,13 +461,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int pc = et + 128 * i, r = row0 + (pc >> 3);
         if (i < nt / 16 && r < args.rows) rp[i] = args.rope[((long long)r * args.heads + h) * 8 + (pc & 7)];
       }
-      gwait_warp(x, bar(AB_ACC_FULL), lt & 1u);
-      // every epilogue warp comes here whether its wait succeeded or not, so
-      // the abort decision below is the same for all four
-      ptx::named_sync(1, 128);
-      if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) break;
-      ptx::tc_fence_after();
-      for (int m = 0; m < 4; ++m, ++blk) {
+      // Every epilogue warp comes to the named barrier after an accumulator
+      // wait, whether the wait succeeded or not, so the abort decision after
+      // it is the same for all four.
+      bool aborted = false;
+      if (!per_block) {
+        gwait_warp(x, bar(AB_ACC_FULL + 3), lt & 1u);
+        ptx::named_sync(1, 128);
+        aborted = ptx::ld_shared_u32_volatile(x.abort_addr) != 0u;
+        ptx::tc_fence_after();
+      }
+      for (int m = 0; !aborted && m < 4; ++m, ++blk) {
+        if (per_block) {
+          gwait_warp(x, bar(AB_ACC_FULL + m), lt & 1u);
+          ptx::named_sync(1, 128);
+          if (ptx::ld_shared_u32_volatile(x.abort_addr) != 0u) {
+            aborted = true;
+            break;
+          }
+          ptx::tc_fence_after();
+        }
         const uint32_t stg = x.sbase + kAbsStage + (blk & 1u) * 2u * qbox;
         if (et == 0) ptx::bulk_wait_read<1>();   // the store that last read this buffer is done
         ptx::named_sync(1, 128);
@@ -479,6 +503,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::bulk_commit();
         }
       }
+      if (aborted) break;
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(AB_ACC_EMPTY));
