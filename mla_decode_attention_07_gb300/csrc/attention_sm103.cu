@@ -38,8 +38,10 @@
 //    are rescaled only when a row max grows by more than 2^8, and the final
 //    1/l and lse use the same reference max, so the result is exact.  out is
 //    normalised by the sum of the bf16 probabilities P.V multiplies, which
-//    the tensor core accumulates beside O (P times a block of ones, M=128
-//    N=16); lse comes from the softmax threads' fp32 sum.
+//    the tensor core accumulates beside O: the P.V MMA runs with N = d_v +
+//    16, its B operand the V tile followed by a box of bf16 ones (one MMA
+//    per K step instead of a second, tiny one); lse comes from the softmax
+//    threads' fp32 sum.
 //  * Every wait is bounded (2 s on %globaltimer): on expiry the kernel
 //    records MLA_ERR_DEVICE_TIMEOUT, lets in-flight copies and MMAs land,
 //    frees TMEM and returns.
@@ -65,14 +67,29 @@ constexpr int kAttDv = 128;
 constexpr int kMaxDqkBoxes = 3;               // d_qk <= 192
 constexpr int kChunk = 16;                    // (batch, head) pairs whose blocks run together
 constexpr uint32_t kBox = 16384;              // 128 rows x 64 bf16, 128-byte swizzle
+// Shared memory in 14 units of one box.  P.V runs with N = d_v + 16: the B
+// operand is the V tile (two 64-dim boxes) followed by a box of bf16 ones,
+// so the same MMA also accumulates each row's sum of P beside O.  An
+// M/N-major operand's 64-column boxes sit one stride (LBO) apart, so the
+// ones box lies two strides past each V stage's first box: stage 0's boxes
+// are units 11 and 12 (stride 1), stage 1's units 7 and 10 (stride 3), the
+// ones unit 13.  Q takes units 0-2 and the K stages the rest (each K step
+// addresses its box on its own).
 constexpr uint32_t kSQ = 0;
-constexpr uint32_t kSK = kSQ + kMaxDqkBoxes * kBox;             // 2 stages x 3 boxes
-constexpr uint32_t kSV = kSK + 2 * kMaxDqkBoxes * kBox;         // 2 stages x 2 boxes
-// bf16 ones, the B operand (16 columns x 128 keys) of an MMA that sums each
-// row of P; every element is 1, so the layout inside is immaterial
-constexpr uint32_t kSOnes = kSV + 2 * 2 * kBox;
-constexpr uint32_t kOnesBytes = 4096;
-constexpr uint32_t kABar = kSOnes + kOnesBytes;
+__host__ __device__ constexpr uint32_t k_box(int s, int c) {
+  return (s == 0 ? 3u + (uint32_t)c : (c == 0 ? 6u : 7u + (uint32_t)c)) * kBox;
+}
+__host__ __device__ constexpr uint32_t v_box(int s, int c) {
+  return (s == 0 ? 11u + (uint32_t)c : (c == 0 ? 7u : 10u)) * kBox;
+}
+__host__ __device__ constexpr uint32_t v_lbo(int s) { return s == 0 ? kBox : 3u * kBox; }
+constexpr uint32_t kSOnes = 13 * kBox;
+constexpr uint32_t kOnesBytes = kBox;
+static_assert(v_box(0, 0) + 2 * v_lbo(0) == kSOnes && v_box(1, 0) + 2 * v_lbo(1) == kSOnes,
+              "the ones box follows each V stage at two strides");
+static_assert(v_box(0, 1) == v_box(0, 0) + v_lbo(0) && v_box(1, 1) == v_box(1, 0) + v_lbo(1),
+              "V boxes one stride apart");
+constexpr uint32_t kABar = 14 * kBox;
 enum ABar : int {
   A_QFULL = 0,
   A_KFULL = 1,     // [2]
@@ -89,6 +106,7 @@ constexpr uint32_t kAMisc = kABar + 8 * 16;
 constexpr uint32_t kASmem = kAMisc + 16 + 1024;
 constexpr uint32_t kColS = 0, kColO = 256, kColL = 384, kATmemCols = 512;
 constexpr int kSumCols = 16;                  // P.1: every column holds the row's sum
+static_assert(kColL == kColO + kAttDv, "the P sums are the last 16 columns of the P.V result");
 constexpr float kARescale = 8.0f;
 constexpr float kALn2 = 0.69314718055994530942f;
 constexpr uint64_t kAWaitNs = 2000000000ull;
@@ -211,7 +229,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (!await_(x, x.bar(A_KEMPTY + s), ph ^ 1u)) return false;
         ptx::mbar_arrive_expect_tx(x.bar(A_KFULL + s), nbq * kBox);
         for (int c = 0; c < nbq; ++c)
-          ptx::tma_load_4d(x.sbase + kSK + (s * kMaxDqkBoxes + c) * kBox, &tm_k, 64 * c, it.h,
+          ptx::tma_load_4d(x.sbase + k_box(s, c), &tm_k, 64 * c, it.h,
                            j * kTK, it.b, x.bar(A_KFULL + s));
         return true;
       };
@@ -221,7 +239,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         if (!await_(x, x.bar(A_VEMPTY + s), ph ^ 1u)) return false;
         ptx::mbar_arrive_expect_tx(x.bar(A_VFULL + s), 2 * kBox);
         for (int c = 0; c < 2; ++c)
-          ptx::tma_load_4d(x.sbase + kSV + (s * 2 + c) * kBox, &tm_v, 64 * c, it.h, j * kTK, it.b,
+          ptx::tma_load_4d(x.sbase + v_box(s, c), &tm_v, 64 * c, it.h, j * kTK, it.b,
                            x.bar(A_VFULL + s));
         return true;
       };
@@ -248,8 +266,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     // S(t) = Q K(t)^T, then P(t-1).V(t-1) (+ P(t-1).1) within an item; an
     // item's last P.V follows its last score MMA
     constexpr uint32_t id_s = ptx::idesc_f32acc(kTQ, kTK, 0, 0, 1);
-    constexpr uint32_t id_o = ptx::idesc_f32acc(kTQ, kAttDv, 0, 1, 1);
-    constexpr uint32_t id_l = ptx::idesc_f32acc(kTQ, kSumCols, 0, 0, 1);
+    // P.V and P.1 in one MMA: N = d_v + 16 (V's columns, then the ones box)
+    constexpr uint32_t id_o = ptx::idesc_f32acc(kTQ, kAttDv + kSumCols, 0, 1, 1);
     auto issue_pv = [&](uint32_t tt, bool first) -> bool {
       const int s = (int)(tt & 1u);
       const uint32_t ph = (tt >> 1) & 1u;
@@ -258,17 +276,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       ptx::tc_fence_after();
 #pragma unroll
       for (int k = 0; k < kTK / 16; ++k) {
-        // V tile: 64-dim boxes 16 KB apart along N, 8-key groups 1 KB apart
-        const uint64_t bd = ptx::smem_desc(x.sbase + kSV + s * 2 * kBox + k * 2048, kBox, 1024,
+        // B: the stage's two V boxes and the ones box, one stride (LBO)
+        // apart along N; 8-key groups 1 KB apart, a K step 16 keys (2 KB).
+        // The last 16 result columns are the sums of the bf16 probabilities
+        // P.V multiplies, accumulated (and rescaled) beside O.
+        const uint64_t bd = ptx::smem_desc(x.sbase + v_box(s, 0) + k * 2048, v_lbo(s), 1024,
                                            ptx::kLayoutSw128);
         ptx::mma_ts_elect(tmem + kColO, tmem + kColS + 128u * s + 8u * k, bd, id_o,
-                          (!first || k > 0) ? 1u : 0u);
-        // the same P against ones: the sums of the bf16 probabilities P.V
-        // multiplies, accumulated (and rescaled) beside O
-        const uint64_t ld = ptx::smem_desc(x.sbase + kSOnes + (uint32_t)(k >> 2) * 2048u +
-                                               (uint32_t)(k & 3) * 32u,
-                                           16, 1024, ptx::kLayoutSw128);
-        ptx::mma_ts_elect(tmem + kColL, tmem + kColS + 128u * s + 8u * k, ld, id_l,
                           (!first || k > 0) ? 1u : 0u);
       }
       ptx::mma_commit_elect(x.bar(A_VEMPTY + s));
@@ -296,7 +310,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         for (int k = 0; k < nbq * 4; ++k) {
           const uint32_t off = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
           const uint64_t ad = ptx::smem_desc(x.sbase + kSQ + off, 16, 1024, ptx::kLayoutSw128);
-          const uint64_t bd = ptx::smem_desc(x.sbase + kSK + s * kMaxDqkBoxes * kBox + off, 16,
+          const uint64_t bd = ptx::smem_desc(x.sbase + k_box(s, k >> 2) + (uint32_t)(k & 3) * 32u, 16,
                                              1024, ptx::kLayoutSw128);
           ptx::mma_ss_elect(tmem + kColS + 128u * s, ad, bd, id_s, k ? 1u : 0u);
         }
