@@ -99,12 +99,16 @@ enum ABar : int {
   A_SFULL = 9,     // [2] score tile ready (MMA commit)
   A_PFULL = 11,    // [2] P written over the tile, O rescaled if needed (8 softmax warps)
   A_ODONE = 13,    // one phase per P.V MMA group
-  A_QEMPTY = 14,   // the item's last score MMA is done: Q may be reloaded
-  A_COUNT = 15
+  A_QEMPTY = 14,   // the item's Q has been copied into TMEM: its staging buffer may be reloaded
+  A_SDONE = 15,    // the item's last score MMA is done: Q's TMEM columns may be rewritten
+  A_COUNT = 16
 };
 constexpr uint32_t kAMisc = kABar + 8 * 16;
 constexpr uint32_t kASmem = kAMisc + 16 + 1024;
-constexpr uint32_t kColS = 0, kColO = 256, kColL = 384, kATmemCols = 512;
+// TMEM: two score tiles, O and the P sums (one P.V result), and Q (the A
+// operand of the score MMAs, d_qk / 2 columns of bf16 pairs)
+constexpr uint32_t kColS = 0, kColO = 256, kColL = 384, kColQ = 400, kATmemCols = 512;
+static_assert(kColQ + kMaxDqkBoxes * 64 / 2 <= kATmemCols, "Q fits beside O");
 constexpr int kSumCols = 16;                  // P.1: every column holds the row's sum
 static_assert(kColL == kColO + kAttDv, "the P sums are the last 16 columns of the P.V result");
 constexpr float kARescale = 8.0f;
@@ -196,6 +200,7 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       ptx::mbar_init(x.bar(A_PFULL + s), kSoftWarps);
     }
     ptx::mbar_init(x.bar(A_ODONE), 1);
+    ptx::mbar_init(x.bar(A_SDONE), 1);
     ptx::st_shared_u32(x.abort_addr, 0u);
     ptx::fence_mbarrier_init();
   }
@@ -294,11 +299,25 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     uint32_t pending_t = 0;
     for (int item = (int)blockIdx.x; ok && item < total_items; item += (int)gridDim.x) {
       const AItem it = att_item(args, item);
+      // The item's Q: staged in shared memory by the TMA (loaded while the
+      // previous item ran), copied into TMEM once the previous item's last
+      // score MMA is done; the staging buffer is free once the copy is.
       if (!await_warp(x, x.bar(A_QFULL), nq & 1u)) {
         ok = false;
         break;
       }
+      if (nq > 0 && !await_warp(x, x.bar(A_SDONE), (nq - 1) & 1u)) {
+        ok = false;
+        break;
+      }
       ++nq;
+      ptx::tc_fence_after();
+      for (int k = 0; k < nbq * 4; ++k)
+        ptx::tmem_cp_128x256b_elect(
+            tmem + kColQ + 8u * (uint32_t)k,
+            ptx::smem_desc(x.sbase + kSQ + (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u, 16,
+                           1024, ptx::kLayoutSw128));
+      ptx::mma_commit_elect(x.bar(A_QEMPTY));
       for (int j = 0; j < it.n_kt; ++j, ++jt) {
         const int s = (int)(jt & 1u);
         const uint32_t ph = (jt >> 1) & 1u;
@@ -308,15 +327,15 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         }
         ptx::tc_fence_after();
         for (int k = 0; k < nbq * 4; ++k) {
-          const uint32_t off = (uint32_t)(k >> 2) * kBox + (uint32_t)(k & 3) * 32u;
-          const uint64_t ad = ptx::smem_desc(x.sbase + kSQ + off, 16, 1024, ptx::kLayoutSw128);
+          // A = Q from TMEM (a K step of 16 dims is 8 columns), B = the K box
           const uint64_t bd = ptx::smem_desc(x.sbase + k_box(s, k >> 2) + (uint32_t)(k & 3) * 32u, 16,
                                              1024, ptx::kLayoutSw128);
-          ptx::mma_ss_elect(tmem + kColS + 128u * s, ad, bd, id_s, k ? 1u : 0u);
+          ptx::mma_ts_elect(tmem + kColS + 128u * s, tmem + kColQ + 8u * (uint32_t)k, bd, id_s,
+                            k ? 1u : 0u);
         }
         ptx::mma_commit_elect(x.bar(A_SFULL + s));
         ptx::mma_commit_elect(x.bar(A_KEMPTY + s));
-        if (j == it.n_kt - 1) ptx::mma_commit_elect(x.bar(A_QEMPTY));   // Q may be reloaded
+        if (j == it.n_kt - 1) ptx::mma_commit_elect(x.bar(A_SDONE));   // Q's columns may be rewritten
         if (pending && !issue_pv(pending_t, pending_first)) {
           ok = false;
           break;
@@ -325,8 +344,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
         pending_t = jt;
         pending_first = (j == 0);
       }
-      // the item's last P.V right away, so its epilogue need not wait for
-      // the next item's Q (loading meanwhile)
+      // the item's last P.V right away: the epilogue waits for it, and the
+      // next item's first score MMA would otherwise go ahead of it
       if (ok && pending) {
         ok = issue_pv(pending_t, pending_first);
         pending = false;

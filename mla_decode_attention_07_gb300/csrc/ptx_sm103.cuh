@@ -297,6 +297,18 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Copy of a 128-row x 256-bit tile from shared memory (described like an MMA
+// operand) into TMEM lanes 0-127, 8 columns from taddr, by the elected lane
+// of a converged warp.  It runs on the tensor pipe in order with the MMAs
+// this thread issues.
+__device__ __forceinline__ void tmem_cp_128x256b_elect(uint32_t taddr, uint64_t s_desc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(s_desc)
+      : "memory");
+}
 // tcgen05.commit by the elected lane (the same lane elect.sync picks for the
 // MMAs above in a converged warp, so it tracks those MMAs).
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
