@@ -121,6 +121,7 @@ struct AttArgs {
   void* out;       // bf16 [B, S, H, d_v]
   float* lse;      // fp32 [B, H, S]
   int B, S, H, dqk, causal, n_qt;
+  int out_v8;      // out is 32-byte aligned: each thread's 128 bytes go out as four 32-byte stores
   float scale_log2;
   int* err;
 };
@@ -482,19 +483,30 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       const bool valid = qi < args.S;
       uint16_t* orow = static_cast<uint16_t*>(args.out) +
                        (((int64_t)it.b * args.S + (valid ? qi : 0)) * args.H + it.h) * kAttDv + 64 * half;
-#pragma unroll 1
+      // this thread's 64 output dims as bf16 pairs, then out in 32-byte (or
+      // 16-byte) stores: a warp's rows lie H * d_v apart in memory, so whole
+      // sectors per store is what keeps the epilogue short
+      uint32_t pk[32];
+#pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         ptx::tmem_ld16x2_wait<64>(tmem + lanes + kColO + 32u * c, o);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            dst[q4] = make_uint4(
-                ptx::pack_bf16x2(__uint_as_float(o[8 * q4]) * inv_l, __uint_as_float(o[8 * q4 + 1]) * inv_l),
-                ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv_l, __uint_as_float(o[8 * q4 + 3]) * inv_l),
-                ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv_l, __uint_as_float(o[8 * q4 + 5]) * inv_l),
-                ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv_l, __uint_as_float(o[8 * q4 + 7]) * inv_l));
+        for (int k = 0; k < 16; ++k)
+          pk[16 * c + k] =
+              ptx::pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+      }
+      if (valid) {
+        if (args.out_v8) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ptx::st_global_v8(orow + 16 * q, pk[8 * q], pk[8 * q + 1], pk[8 * q + 2], pk[8 * q + 3],
+                              pk[8 * q + 4], pk[8 * q + 5], pk[8 * q + 6], pk[8 * q + 7]);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
       if (valid && half == 0)
@@ -572,6 +584,7 @@ extern "C" int mla_attention_fwd(const void* q, const void* k, const void* v, vo
   a.dqk = d_qk;
   a.causal = causal ? 1 : 0;
   a.n_qt = (int)n_qt;
+  a.out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = err;
   // persistent: one CTA per SM, each taking every grid-th work item

@@ -74,6 +74,27 @@ def test_attention_parity(torch_cuda, case, oracle_mod):
     assert el <= LSE_TOL, f"max|lse err| {el:.3e}"
 
 
+def test_attention_output_only_16_byte_aligned(torch_cuda, oracle_mod):
+    """out placed 16 bytes into a larger buffer (16- but not 32-byte
+    aligned), which takes the kernel's 16-byte store path; the words around
+    it stay untouched."""
+    ai = W.make_attention_inputs(408, 2, 300, 3, 192, 128, True)
+    ref_o, ref_l = oracle_mod.attention(ai)
+    t = lambda a: torch_cuda.from_numpy(np.ascontiguousarray(a.view(np.int16))).to("cuda").view(
+        torch_cuda.bfloat16)
+    n = 2 * 300 * 3 * 128
+    buf = torch_cuda.full((n + 32,), 7.0, dtype=torch_cuda.bfloat16, device="cuda")
+    out = buf[8:8 + n].view(2, 300, 3, 128)
+    assert out.data_ptr() % 32 == 16
+    lse = torch_cuda.empty((2, 3, 300), dtype=torch_cuda.float32, device="cuda")
+    libmla.mla_attention_fwd(t(ai.q), t(ai.k), t(ai.v), out, lse, ai.causal, ai.scale)
+    assert libmla.mla_check_device_error() == 0
+    b = buf.float().cpu().numpy()
+    assert (b[:8] == 7.0).all() and (b[8 + n:] == 7.0).all()
+    assert float(np.abs(out.float().cpu().numpy() - ref_o).max()) <= OUT_TOL
+    assert float(np.abs(lse.cpu().numpy() - ref_l).max()) <= LSE_TOL
+
+
 def test_attention_prefill_workload_sampled(torch_cuda, oracle_mod):
     """The MLA-prefill workload at full size through the call the benchmark
     times, 256 sampled rows (and the corners) against the oracle."""
