@@ -225,7 +225,12 @@ __global__ void __launch_bounds__(kAttThreads, 1)
   // Every role walks the same items (item = blockIdx.x + k * gridDim.x) and
   // counts K/V tiles across them (jt): stage, score tile and barrier phases
   // follow jt, so one item's tail overlaps the next one's head.
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
+    // Two producer threads: warp 0 loads Q and the K tiles, warp 2 the V
+    // tiles, so that a K tile goes out as soon as its stage is free (its
+    // score MMA two tiles back) and never waits behind a V tile (whose stage
+    // is freed later, by a P.V).
+    const bool kq = (warp == 0);
     if (lane == 0) {
       uint32_t jt = 0, nq = 0;
       bool ok = true;
@@ -251,9 +256,13 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       };
       for (int item = (int)blockIdx.x; ok && item < total_items; item += (int)gridDim.x) {
         const AItem it = att_item(args, item);
+        if (!kq) {
+          for (int j = 0; ok && j < it.n_kt; ++j, ++jt) ok = load_v(it, j);
+          continue;
+        }
         // the item's first K tile (its stage is freed by the score MMA two
-        // tiles back), then Q (once the previous item's last score MMA is
-        // done), then the rest in tile order
+        // tiles back), then Q (once the previous item's Q has been copied
+        // into TMEM), then the rest in tile order
         ok = load_k(it, 0);
         if (!ok) break;
         if (!await_(x, x.bar(A_QEMPTY), (nq & 1u) ^ 1u)) break;
@@ -262,9 +271,8 @@ __global__ void __launch_bounds__(kAttThreads, 1)
           ptx::tma_load_4d(x.sbase + kSQ + c * kBox, &tm_q, 64 * c, it.h, it.qt * kTQ, it.b,
                            x.bar(A_QFULL));
         ++nq;
-        ok = load_v(it, 0);
         ++jt;
-        for (int j = 1; ok && j < it.n_kt; ++j, ++jt) ok = load_k(it, j) && load_v(it, j);
+        for (int j = 1; ok && j < it.n_kt; ++j, ++jt) ok = load_k(it, j);
       }
     }
     __syncwarp();
@@ -366,8 +374,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
     const float sl2 = args.scale_log2;
     uint32_t jt = 0;
     bool ok = true;
+    AItem nit = att_item(args, (int)blockIdx.x);
     for (int item = (int)blockIdx.x; ok && item < total_items; item += (int)gridDim.x) {
-      const AItem it = att_item(args, item);
+      const AItem it = nit;
       const int qi = it.qt * kTQ + r;
       float m_ref = -INFINITY, l_f = 0.f;   // fp32 sum of this thread's columns (for lse)
       for (int j = 0; j < it.n_kt; ++j, ++jt) {
@@ -471,6 +480,9 @@ __global__ void __launch_bounds__(kAttThreads, 1)
       // first P.V (which overwrites O) waits for this item's P of its first
       // tile, which these threads write only after this.
       l_f += __shfl_xor_sync(0xffffffffu, l_f, 16);
+      // the next item's coordinates (integer divisions), while the last P.V
+      // runs
+      if (item + (int)gridDim.x < total_items) nit = att_item(args, item + (int)gridDim.x);
       if (!await_warp(x, x.bar(A_ODONE), (jt - 1) & 1u)) {
         ok = false;
         break;
