@@ -73,6 +73,7 @@ struct GemmArgs {
   long long ldc, c_batch;   // elements
   int M, N, K, batch, tiles_m, tiles_n;
   int out_type;             // MLA_DTYPE_F16 / BF16 / F32
+  int c_v8;                 // C's base and strides allow 32-byte stores
   int* err;
 };
 
@@ -109,7 +110,12 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, char* crow, int n
                                             const uint32_t (&v)[32]) {
   if (a.out_type == MLA_DTYPE_F32) {
     float* dst = reinterpret_cast<float*>(crow) + n0;
-    if (n0 + 32 <= a.N) {
+    if (n0 + 32 <= a.N && a.c_v8) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ptx::st_global_v8(dst + 8 * j, v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3],
+                          v[8 * j + 4], v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
+    } else if (n0 + 32 <= a.N) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         reinterpret_cast<float4*>(dst)[j] =
@@ -133,7 +139,12 @@ __device__ __forceinline__ void store_row32(const GemmArgs& a, char* crow, int n
       p[j] = ptx::pack_f16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
   }
   uint16_t* dst = reinterpret_cast<uint16_t*>(crow) + n0;
-  if (n0 + 32 <= a.N) {
+  if (n0 + 32 <= a.N && a.c_v8) {
+    // a row's 64 bytes in two 32-byte stores (rows lie ldc apart: whole
+    // sectors per store)
+    ptx::st_global_v8(dst, p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]);
+    ptx::st_global_v8(dst + 16, p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]);
+  } else if (n0 + 32 <= a.N) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       reinterpret_cast<uint4*>(dst)[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
@@ -627,6 +638,10 @@ int mla_gemm(const void* A, const void* B, void* C, int M, int N, int K, int in_
   a.K = K;
   a.batch = 1;
   a.out_type = out_dtype;
+  {
+    const size_t es = out_dtype == MLA_DTYPE_F32 ? 4 : 2;
+    a.c_v8 = (reinterpret_cast<uintptr_t>(C) & 31u) == 0 && ((size_t)N * es) % 32 == 0;
+  }
   return launch_gemm(in_dtype, ma, mb, a, static_cast<cudaStream_t>(stream));
 }
 
