@@ -21,19 +21,25 @@
 //    grid takes the longest tiles first.  The roles count K/V tiles across
 //    items, so the loads, score MMAs and softmax of one item overlap the
 //    tail of the one before (set-up, Q and the first K/V tiles are no
-//    longer paid per item).  Warp 0 issues TMA loads (Q per item, then K and
-//    V tiles of 128 keys through two-deep rings of their own), warp 1 owns
-//    TMEM and issues the MMAs, warps 4-11 run the softmax and the epilogue
-//    with two threads per query row, 64 key columns each (warp w reaches 16
-//    lanes of TMEM lane quadrant w % 4 through the 16x32bx2 access shape).
-//  * S = Q K^T (M=128, N=128, K=d_qk, both operands K-major from shared
-//    memory) lands in one of two 128-column TMEM tiles.  The softmax writes
-//    P as bf16 over the first 64 columns of the same tile, and P.V reads P
-//    from TMEM as its A operand (M=128, N=d_v, K=128) with V as the MN-major
-//    B operand: P never goes through shared memory, O (d_v fp32 columns)
-//    stays in TMEM until the epilogue.
+//    longer paid per item).  Warp 0 issues the TMA loads of Q (per item) and
+//    of the K tiles, warp 2 those of the V tiles (128 keys each, two-deep
+//    rings of their own), so a K tile never waits behind a V tile; warp 1
+//    owns TMEM and issues the MMAs; warps 4-11 run the softmax and the
+//    epilogue with two threads per query row, 64 key columns each (warp w
+//    reaches 16 lanes of TMEM lane quadrant w % 4 through the 16x32bx2
+//    access shape).
+//  * S = Q K^T (M=128, N=128, K=d_qk) takes Q from TMEM and K (K-major)
+//    from shared memory and lands in one of two 128-column TMEM tiles.  Q is
+//    staged in shared memory by the TMA while the previous item runs and
+//    copied into TMEM with tcgen05.cp (in order with the MMAs) once that
+//    item's last score MMA is done.  The softmax writes P as bf16 over the
+//    first 64 columns of the score tile, and P.V reads P from TMEM as its A
+//    operand with V as the MN-major B operand: P never goes through shared
+//    memory, O (d_v fp32 columns) stays in TMEM until the epilogue, which
+//    writes each row's 128 bytes per thread as 32-byte stores.
 //  * The MMAs are issued in the order S(j), P.V(j-1): the score MMA of the
-//    next tile runs on the tensor pipe while this tile's softmax computes.
+//    next tile runs on the tensor pipe while this tile's softmax computes;
+//    an item's last P.V goes out right after its probabilities.
 //  * Online softmax in the log2 domain with a lazy rescale: O and the sums
 //    are rescaled only when a row max grows by more than 2^8, and the final
 //    1/l and lse use the same reference max, so the result is exact.  out is
