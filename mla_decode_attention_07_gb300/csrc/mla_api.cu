@@ -605,6 +605,7 @@ int prepare_decode(const void* q, const void* kv_cache, int num_pages, const int
   p->topk = 0;
   p->plan = static_cast<const int32_t*>(tile_meta);
   p->out = out;
+  p->out_v8 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
   p->lse = lse;
   p->out_f32 = 0;
   const int64_t slots = workspace_slots(d.num_clusters);

@@ -866,20 +866,22 @@ __device__ __forceinline__ bool run_pages(const Ctx& x, const Work& w, const Dec
         if (valid_e) {
           const int d0 = (int)x.rank * 256 + ch * 32;
           if (direct && !prm.out_f32) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(prm.out) +
-                                                  orow * kDv + d0);
+            // a row's 32 dims: 64 bytes, rows 1 KB apart (32-byte stores
+            // when out allows: whole sectors)
+            uint32_t pk[16];
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              uint4 u;
-              u.x = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 0]) * inv_l,
-                                     __uint_as_float(o[8 * qq + 1]) * inv_l);
-              u.y = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 2]) * inv_l,
-                                     __uint_as_float(o[8 * qq + 3]) * inv_l);
-              u.z = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 4]) * inv_l,
-                                     __uint_as_float(o[8 * qq + 5]) * inv_l);
-              u.w = ptx::pack_bf16x2(__uint_as_float(o[8 * qq + 6]) * inv_l,
-                                     __uint_as_float(o[8 * qq + 7]) * inv_l);
-              dst[qq] = u;
+            for (int k = 0; k < 16; ++k)
+              pk[k] = ptx::pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l,
+                                       __uint_as_float(o[2 * k + 1]) * inv_l);
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(prm.out) + orow * kDv + d0;
+            if (prm.out_v8) {
+              ptx::st_global_v8(dst, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+              ptx::st_global_v8(dst + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+            } else {
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq)
+                reinterpret_cast<uint4*>(dst)[qq] =
+                    make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
             }
           } else {
             // fp32: the final output row (fp32 out), or this split's partial

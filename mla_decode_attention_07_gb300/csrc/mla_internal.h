@@ -28,6 +28,7 @@ struct DecodeParams {
   int* err;           // device error word
   int batch, s_q, h_q, max_pages, num_pages;
   int out_f32;        // 1: out is fp32 (the normalised fp32 result, unrounded)
+  int out_v8;         // 1: out is 32-byte aligned (row pieces go out as 32-byte stores)
   float scale_log2;   // softmax_scale * log2(e)
 };
 
