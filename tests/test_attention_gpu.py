@@ -111,3 +111,32 @@ def test_attention_prefill_workload_sampled(torch_cuda, oracle_mod):
     assert float(np.abs(got_o - ref_o).max()) <= OUT_TOL
     assert float(np.abs(got_l - ref_l).max()) <= LSE_TOL
     assert not np.isnan(out).any() and not np.isnan(lse).any()
+
+
+MULTI_ITEM_CASES = [
+    # seed, batch, seqlen, heads, d_qk, causal: several work items per CTA
+    # (query tiles x heads x batch well above the SM count), so each CTA runs
+    # item switches (the next item's Q staged during the previous one)
+    (409, 3, 1500, 40, 192, True),     # 1440 items, ragged last query tile
+    (410, 2, 1100, 72, 128, False),    # 1296 items, full rows
+]
+
+
+@pytest.mark.parametrize("case", MULTI_ITEM_CASES,
+                         ids=lambda c: f"s{c[0]}_b{c[1]}_s{c[2]}_h{c[3]}_d{c[4]}"
+                         f"_{'causal' if c[5] else 'full'}")
+def test_attention_many_items_per_cta_sampled(torch_cuda, case, oracle_mod):
+    seed, B, S, H, dqk, causal = case
+    ai = W.make_attention_inputs(seed, B, S, H, dqk, 128, causal)
+    out, lse = run_attention(torch_cuda, ai)
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, B, 192), rng.integers(0, H, 192), rng.integers(0, S, 192)],
+                    axis=1)
+    corners = [[0, 0, 0], [B - 1, H - 1, S - 1], [B - 1, 0, S - 1], [0, H - 1, 127], [0, 1, 128]]
+    rows = np.concatenate([corners, rows]).astype(np.int32)
+    ref_o, ref_l = oracle_mod.attention_rows(ai, rows)
+    got_o = out[rows[:, 0], rows[:, 2], rows[:, 1]]
+    got_l = lse[rows[:, 0], rows[:, 1], rows[:, 2]]
+    assert not np.isnan(out).any() and not np.isnan(lse).any()
+    assert float(np.abs(got_o - ref_o).max()) <= OUT_TOL
+    assert float(np.abs(got_l - ref_l).max()) <= LSE_TOL
