@@ -381,11 +381,13 @@ def run_ours(args):
     # still rotate for L2.  Steps are pipelined the way a serving loop would
     # run them: the inputs of the next step and the results of the previous
     # one move on two copy streams while a step computes (each input set has
-    # its own out/lse, and a set is refilled only after its last step's
-    # results are copied out), and a window of steps is captured once as a
-    # CUDA graph so that the host issues one launch per window.  A step's
-    # inputs sit in one pinned buffer and its out + lse in one device buffer,
-    # so each direction is a single copy.
+    # its own out/lse and tile metadata, and a set is refilled only after its
+    # last step's results are copied out), and a window of steps is captured
+    # once as a CUDA graph so that the host issues one launch per window.  A
+    # step's plan needs only its sequence lengths, so it runs on the input
+    # stream right after they land, while the previous step decodes.  A
+    # step's inputs sit in one pinned buffer and its out + lse in one device
+    # buffer, so each direction is a single copy.
     def packed(parts, device=None, pin=False):
         """One byte buffer holding several tensors (16-byte aligned views), so
         that a step's inputs, or its outputs, move in a single copy."""
@@ -414,6 +416,7 @@ def run_ours(args):
     ns = min(len(sets), win)         # input sets the window rotates through
     d_in = [packed(in_parts, device=dev) for _ in range(ns)]
     d_res = [packed(out_parts, device=dev) for _ in range(ns)]
+    d_meta = [libmla.alloc_plan_and_workspace(B, s_q, h_q, dev.index)[0] for _ in range(ns)]
     h_res = [packed(out_parts, pin=True)[0] for _ in range(ns)]
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
     d2h = out.numel() * 2 + lse.numel() * 4
@@ -421,8 +424,8 @@ def run_ours(args):
     def e2e_window(cap):
         """Enqueue `win` pipelined steps on `cap` (and two copy streams that
         fork from and join back into it).  Per step: one host-to-device copy
-        of the packed inputs, plan + decode, one device-to-host copy of the
-        packed out + lse."""
+        of the packed inputs and the plan (input stream), the decode (`cap`),
+        one device-to-host copy of the packed out + lse (output stream)."""
         hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         hs.wait_stream(cap)
         ds.wait_stream(cap)
@@ -438,12 +441,12 @@ def run_ours(args):
                 if j >= ns:
                     hs.wait_event(done[j - ns])
                 ibuf.copy_(h_in, non_blocking=True)
+                libmla.mla_decode_plan(sl_i, s_q, h_q, d_meta[i], hs)
                 ready[j].record(hs)
             cap.wait_event(ready[j])
             if j >= ns:
                 cap.wait_event(back[j - ns])
-            libmla.mla_decode_plan(sl_i, s_q, h_q, meta, cap)
-            libmla.mla_decode(q_i, kv, bt_i, sl_i, meta, out_i, lse_i, scale, ws, cap)
+            libmla.mla_decode(q_i, kv, bt_i, sl_i, d_meta[i], out_i, lse_i, scale, ws, cap)
             done[j].record(cap)
             with torch.cuda.stream(ds):
                 ds.wait_event(done[j])
@@ -555,7 +558,8 @@ def run_ours(args):
                 "d2h_bytes_per_step": int(d2h),
                 "steps": reps * win,
                 "note": "every step: q/block_table/seqlens copied in from pinned host memory, "
-                        "mla_decode_plan + mla_decode, out+lse copied back (one packed copy "
+                        "mla_decode_plan (on the input stream, overlapping the previous "
+                        "step's decode) + mla_decode, out+lse copied back (one packed copy "
                         "each way); cache pages resident; " + e2e_mode},
         "clocks": clocks,
     }
