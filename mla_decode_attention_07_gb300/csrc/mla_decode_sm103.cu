@@ -291,7 +291,8 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
 // ((c ^ ((r / 2) % 4)) << 4) (64-byte swizzle).  One instruction copies one
 // row's 512 latent bytes (lane = chunk), so each is four whole 128-byte
 // lines; eight more copy the rotary parts of eight rows each.  Rows past the
-// entry's count are zero-filled.
+// entry's count are zero-filled (the copy form with a source size); listed
+// rows use the plain 16-byte form, which retires faster.
 //
 // The row each lane resolves (rows lane and lane + 32: list position, then
 // block-table entry) is ready one chunk ahead, and the list positions two
@@ -374,18 +375,22 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
 #pragma unroll 4
       for (int r = kGatherRows * half; r < kGatherRows * (half + 1); ++r) {
         const int rr = __shfl_sync(0xffffffffu, row, r & (kGatherRows - 1));
-        const char* src = rr >= 0 ? kv + (size_t)rr * (kDqk * 2) + lat_off : kv;
-        ptx::cp_async16(box + (uint32_t)r * 128u + ((((uint32_t)lane & 7u) ^ ((uint32_t)r & 7u)) << 4),
-                        src, rr >= 0 ? 16u : 0u);
+        const uint32_t dst = box + (uint32_t)r * 128u + ((((uint32_t)lane & 7u) ^ ((uint32_t)r & 7u)) << 4);
+        if (rr >= 0)
+          ptx::cp_async16_full(dst, kv + (size_t)rr * (kDqk * 2) + lat_off);
+        else
+          ptx::cp_async16(dst, kv, 0u);
       }
 #pragma unroll
       for (int i = 0; i < kGatherRows / 8; ++i) {
         const int r = kGatherRows * half + 8 * i + (lane >> 2);
         const int rr = __shfl_sync(0xffffffffu, row, r & (kGatherRows - 1));
-        const char* src = rr >= 0 ? kv + (size_t)rr * (kDqk * 2) + rope_off : kv;
-        ptx::cp_async16(st + kStageRope + (uint32_t)r * 64u +
-                            ((((uint32_t)lane & 3u) ^ (((uint32_t)r >> 1) & 3u)) << 4),
-                        src, rr >= 0 ? 16u : 0u);
+        const uint32_t dst = st + kStageRope + (uint32_t)r * 64u +
+                             ((((uint32_t)lane & 3u) ^ (((uint32_t)r >> 1) & 3u)) << 4);
+        if (rr >= 0)
+          ptx::cp_async16_full(dst, kv + (size_t)rr * (kDqk * 2) + rope_off);
+        else
+          ptx::cp_async16(dst, kv, 0u);
       }
       ptx::cp_async_commit();
       if (g >= announced + kGatherLag) {
