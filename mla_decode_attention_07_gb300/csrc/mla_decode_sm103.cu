@@ -292,7 +292,8 @@ __device__ __forceinline__ bool run_producer(const Ctx& x, const Work& w, const 
 // row's 512 latent bytes (lane = chunk), so each is four whole 128-byte
 // lines; eight more copy the rotary parts of eight rows each.  Rows past the
 // entry's count are zero-filled (the copy form with a source size); listed
-// rows use the plain 16-byte form, which retires faster.
+// rows use the plain 16-byte form, which retires faster, with an L2
+// evict-first policy (each row is read once).
 //
 // The row each lane resolves (rows lane and lane + 32: list position, then
 // block-table entry) is ready one chunk ahead, and the list positions two
@@ -309,6 +310,7 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
                                                     const DecodeParams& prm,
                                                     const CUtensorMap* tm_q_rope, int lane,
                                                     int half) {
+  const uint64_t gpolicy = ptx::policy_evict_first();
   SegIter it{w.b0, w.p0, w.b1, w.p1, w.items};
   int b, pb, pe;
   uint32_t g = 0, announced = 0, n_item = 0;
@@ -377,7 +379,7 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
         const int rr = __shfl_sync(0xffffffffu, row, r & (kGatherRows - 1));
         const uint32_t dst = box + (uint32_t)r * 128u + ((((uint32_t)lane & 7u) ^ ((uint32_t)r & 7u)) << 4);
         if (rr >= 0)
-          ptx::cp_async16_full(dst, kv + (size_t)rr * (kDqk * 2) + lat_off);
+          ptx::cp_async16_full_hint(dst, kv + (size_t)rr * (kDqk * 2) + lat_off, gpolicy);
         else
           ptx::cp_async16(dst, kv, 0u);
       }
@@ -388,7 +390,7 @@ __device__ __forceinline__ bool run_producer_sparse(const Ctx& x, const Work& w,
         const uint32_t dst = st + kStageRope + (uint32_t)r * 64u +
                              ((((uint32_t)lane & 3u) ^ (((uint32_t)r >> 1) & 3u)) << 4);
         if (rr >= 0)
-          ptx::cp_async16_full(dst, kv + (size_t)rr * (kDqk * 2) + rope_off);
+          ptx::cp_async16_full_hint(dst, kv + (size_t)rr * (kDqk * 2) + rope_off, gpolicy);
         else
           ptx::cp_async16(dst, kv, 0u);
       }
